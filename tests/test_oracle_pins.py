@@ -1,0 +1,323 @@
+"""Pins of the fp64 oracle to facts the method's description fixes.
+
+Each test checks the oracle against something other than itself: closed-form
+hand-walked trees (tests/golden/hand_trees.json), the Appendix-A Jensen
+sandwich ("Block Sparse Attention with Log-Linear Complexity", "Scoring:
+LogSumExp, and why not the mean"), textbook log-sum-exp from scipy, a
+brute-force flat Top-K for the case the walk reduces to it, and invariances.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy.special import logsumexp
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_trees.json")
+D = 64
+SCALE = 1.0 / math.sqrt(D)
+_ENV = {"log": math.log, "exp": math.exp, "min": min, "inf": math.inf}
+
+
+def _ev(expr: str) -> float:
+    return float(eval(expr, {"__builtins__": {}}, _ENV))
+
+
+def _hand_inputs(case):
+    N, G = case["N"], case["G"]
+    vals = case.get("leaf_values")
+    keys = np.zeros((1, N, 1, D), np.float32)
+    if vals is not None:
+        for i, v in enumerate(vals):
+            s, e = 64 * i, min(64 * (i + 1), N)
+            for h, x in enumerate(v):
+                keys[0, s:e, 0, h] = x
+    q = np.zeros((1, N, G, D), np.float32)
+    for h in range(G):
+        q[0, :, h, h] = math.sqrt(D)
+    return q, keys
+
+
+def _golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("case", _golden()["cases"], ids=lambda c: c["name"])
+def test_hand_walked_trees(case):
+    q, keys = _hand_inputs(case)
+    t = case["t"]
+    r = oracle.select(q[:, t:t + 1], keys, K=case["K"], causal=case["causal"], t_list=[t])
+    assert r["idx"][0, 0, 0].tolist() == case["expect_idx"]
+    exp_scores = [_ev(e) for e in case["expect_scores"]]
+    for got, want in zip(r["scores"][0, 0, 0], exp_scores):
+        if math.isinf(want):
+            assert got == want
+        else:
+            assert abs(got - want) < 1e-12, (got, want)
+    want_gap = _ev(case["expect_min_gap"])
+    got_gap = r["min_gap"][0, 0, 0]
+    if math.isinf(want_gap):
+        assert got_gap == want_gap
+    else:
+        assert abs(got_gap - want_gap) < 1e-12, (got_gap, want_gap)
+    assert r["n_scored"][0, 0, 0] == case["expect_n_scored"]
+
+
+@pytest.mark.parametrize("case", _golden()["pyramid_cases"], ids=lambda c: c["name"])
+def test_hand_pyramids(case):
+    N = case["N"]
+    keys = np.zeros((1, N, 1, D), np.float32)
+    if "leaf_values" in case:
+        for i, v in enumerate(case["leaf_values"]):
+            keys[0, 64 * i:min(64 * (i + 1), N), 0, 0] = v[0]
+    else:
+        keys[0, :, 0, 0] = np.arange(N, dtype=np.float32) / 64.0
+    for recursive in (False, True):
+        pyr = oracle.build_pyramid(keys, recursive=recursive)[0, 0]
+        off = 0
+        for lvl in case["expect_levels"]:
+            for i, expr in enumerate(lvl):
+                assert abs(pyr[off + i, 0] - _ev(expr)) < 1e-12
+                assert np.all(pyr[off + i, 1:] == 0.0)
+            off += len(lvl)
+        assert off == pyr.shape[0]
+
+
+@pytest.mark.parametrize("case", _golden()["level_sizes"], ids=lambda c: str(c["N"]))
+def test_level_sizes(case):
+    assert oracle.level_sizes(case["N"]) == case["expect"]
+    assert oracle.total_nodes(case["N"]) == sum(case["expect"])
+
+
+def _rand(shape, rng, grid=None):
+    x = rng.standard_normal(shape).astype(np.float32)
+    if grid:
+        x = np.round(x * grid) / grid
+    return x
+
+
+def test_pyramid_means_match_brute_force_and_recursive_route():
+    rng = np.random.default_rng(11)
+    B, N, Hkv = 2, 1000, 3  # ragged: 16 leaves, the last one of 40 keys
+    keys = _rand((B, N, Hkv, D), rng)
+    direct = oracle.build_pyramid(keys)
+    rec = oracle.build_pyramid(keys, recursive=True)
+    np.testing.assert_allclose(direct, rec, rtol=0, atol=1e-12)
+    sizes = oracle.level_sizes(N)
+    off = 0
+    k64 = keys.astype(np.float64)
+    for lvl, m in enumerate(sizes, start=1):
+        width = 64 * 2 ** (lvl - 1)
+        for i in range(m):
+            s, e = i * width, min((i + 1) * width, N)
+            want = k64[:, s:e].mean(axis=1)  # [B, Hkv, d]
+            np.testing.assert_allclose(direct[:, :, off + i], want, rtol=0, atol=1e-12)
+        off += m
+
+
+def _jensen_setup(rng, child_const=False, equal_child_means=False):
+    """One KV head, one query head, N = 512 (8 leaves): level-3 node 0 has the
+    full level-2 children 0 and 1 (128 keys each)."""
+    N = 512
+    keys = rng.standard_normal((1, N, 1, D))
+    if child_const:  # keys constant inside each level-2 child
+        for j in range(4):
+            keys[0, 128 * j:128 * (j + 1)] = keys[0, 128 * j]
+    if equal_child_means:  # every level-2 child has the same mean
+        common = rng.standard_normal(D)
+        for j in range(4):
+            blk = keys[0, 128 * j:128 * (j + 1), 0]
+            keys[0, 128 * j:128 * (j + 1), 0] = blk - blk.mean(axis=0) + common
+    keys = keys.astype(np.float32)
+    q = (rng.standard_normal((1, D)) * 1.5).astype(np.float32)
+    return q, keys
+
+
+def _sandwich_terms(q, keys, level, node):
+    """(mean of child logits, score - log g, true normalised raw-key LSE of the node)."""
+    N = keys.shape[1]
+    pyr = oracle.build_pyramid(keys)[0, 0]
+    sizes = oracle.level_sizes(N)
+    off = sum(sizes[: level - 2])  # offset of level (level-1)
+    kids = [2 * node, 2 * node + 1]
+    m = [SCALE * float(np.dot(q[0].astype(np.float64), pyr[off + c])) for c in kids]
+    score = oracle.node_score(q, keys, level=level, node=node, t=N - 1, causal=False)
+    width = 64 * 2 ** (level - 1)
+    kb = keys[0, node * width:(node + 1) * width, 0].astype(np.float64)
+    logits = SCALE * kb @ q[0].astype(np.float64)
+    F = logsumexp(logits) - math.log(len(logits))
+    return float(np.mean(m)), score - math.log(2.0), F
+
+
+def test_jensen_sandwich_holds_on_random_blocks():
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        q, keys = _jensen_setup(rng)
+        for level, node in ((3, 0), (3, 1), (4, 0), (2, 3)):
+            lo, mid, hi = _sandwich_terms(q, keys, level, node)
+            assert lo <= mid + 1e-12
+            assert mid <= hi + 1e-12
+
+
+def test_jensen_sandwich_right_equality_when_children_are_constant():
+    rng = np.random.default_rng(6)
+    for _ in range(5):
+        q, keys = _jensen_setup(rng, child_const=True)
+        lo, mid, hi = _sandwich_terms(q, keys, 3, 0)
+        assert abs(mid - hi) < 1e-12
+        assert lo < mid - 1e-6
+
+
+def test_jensen_sandwich_left_equality_when_child_logits_are_equal():
+    rng = np.random.default_rng(7)
+    for _ in range(5):
+        q, keys = _jensen_setup(rng, equal_child_means=True)
+        lo, mid, hi = _sandwich_terms(q, keys, 3, 0)
+        assert abs(lo - mid) < 1e-12
+        assert mid < hi - 1e-6
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_leaf_score_is_textbook_lse(causal):
+    rng = np.random.default_rng(8)
+    B, N, Hq, Hkv = 1, 300, 6, 2
+    G = Hq // Hkv
+    q = _rand((B, N, Hq, D), rng)
+    keys = _rand((B, N, Hkv, D), rng)
+    k64 = keys.astype(np.float64)
+    for t in (0, 37, 63, 64, 130, 299):
+        for kv in range(Hkv):
+            for leaf in range(t // 64 + 1 if causal else 5):
+                s, e = 64 * leaf, min(64 * (leaf + 1), N)
+                if causal:
+                    e = min(e, t + 1)
+                want = 0.0
+                for h in range(kv * G, (kv + 1) * G):
+                    logits = SCALE * k64[0, s:e, kv] @ q[0, t, h].astype(np.float64)
+                    want += logsumexp(logits)
+                got = oracle.node_score(q[0, t], keys, level=1, node=leaf, t=t, kv=kv, causal=causal)
+                assert abs(got - want) < 1e-10 * max(1.0, abs(want))
+
+
+def _flat_topk(q, keys, t, kv, G, K, causal):
+    """Brute-force flat selection: exact head-summed raw-key LSE of every eligible
+    leaf, Top-K (lower index on ties), ascending, padded with -1."""
+    N = keys.shape[1]
+    M1 = -(-N // 64)
+    k64 = keys.astype(np.float64)
+    scores = []
+    for leaf in range(M1):
+        s = 64 * leaf
+        if causal and s > t:
+            break
+        e = min(s + 64, N)
+        if causal:
+            e = min(e, t + 1)
+        tot = 0.0
+        for h in range(kv * G, (kv + 1) * G):
+            tot += logsumexp(SCALE * k64[0, s:e, kv] @ q[h].astype(np.float64))
+        scores.append((tot, leaf))
+    ranked = sorted(scores, key=lambda x: (-x[0], x[1]))[:K]
+    sel = sorted(l for _, l in ranked)
+    return sel + [-1] * (K - len(sel)), {l: s for s, l in scores}
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_walk_equals_flat_topk_when_level2_fits_in_K(causal):
+    # tiny shape: 32 leaves, 16 level-2 nodes; with K = 16 every leaf reaches the leaf level
+    rng = np.random.default_rng(9)
+    B, N, Hq, Hkv, K = 1, 2048, 8, 2, 16
+    q = _rand((B, N, Hq, D), rng)
+    keys = _rand((B, N, Hkv, D), rng)
+    ts = np.array([0, 5, 63, 64, 500, 1023, 1024, 1500, 2047])
+    r = oracle.select(q[:, ts], keys, K=K, causal=causal, t_list=ts)
+    for it, t in enumerate(ts):
+        for kv in range(Hkv):
+            want, sc = _flat_topk(q[0, t], keys, t, kv, Hq // Hkv, K, causal)
+            assert r["idx"][0, kv, it].tolist() == want
+            for j, leaf in enumerate(want):
+                if leaf >= 0:
+                    assert abs(r["scores"][0, kv, it, j] - sc[leaf]) < 1e-9
+    assert r["n_scored"].max() <= 1
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_every_leaf_selected_when_K_covers_all(causal):
+    rng = np.random.default_rng(10)
+    N, K = 2048, 32
+    q = _rand((1, N, 4, D), rng)
+    keys = _rand((1, N, 1, D), rng)
+    ts = np.array([0, 100, 1000, 2047])
+    r = oracle.select(q[:, ts], keys, K=K, causal=causal, t_list=ts)
+    for it, t in enumerate(ts):
+        n_el = t // 64 + 1 if causal else 32
+        want = list(range(n_el)) + [-1] * (K - n_el)
+        assert r["idx"][0, 0, it].tolist() == want
+    assert r["n_scored"].max() == 0
+
+
+def test_shift_invariance():
+    # adding one vector c to every key moves each head's logits by s*q_h.c:
+    # indices are unchanged and every score moves by sum_h s*q_h.c
+    rng = np.random.default_rng(12)
+    N, Hq, Hkv, K = 4096, 4, 1, 4
+    q = _rand((1, N, Hq, D), rng, grid=8)
+    keys = _rand((1, N, Hkv, D), rng, grid=8)
+    c = np.round(rng.standard_normal(D) * 8) / 8
+    ts = np.arange(0, N, 97)
+    a = oracle.select(q[:, ts], keys, K=K, t_list=ts)
+    b = oracle.select(q[:, ts], (keys + c.astype(np.float32)), K=K, t_list=ts)
+    np.testing.assert_array_equal(a["idx"], b["idx"])
+    shift = SCALE * (q[0, ts].astype(np.float64) @ c).sum(axis=1)  # [n_t]
+    valid = a["idx"] >= 0
+    diff = b["scores"][valid] - a["scores"][valid]
+    np.testing.assert_allclose(diff, np.broadcast_to(shift[None, None, :, None], a["idx"].shape)[valid],
+                               atol=1e-9)
+
+
+def test_head_permutation_within_group_invariance():
+    rng = np.random.default_rng(13)
+    N, Hq, Hkv, K = 4096, 8, 2, 8
+    q = _rand((1, N, Hq, D), rng)
+    keys = _rand((1, N, Hkv, D), rng)
+    perm = np.array([2, 0, 3, 1, 5, 7, 4, 6])  # stays inside each group of 4
+    ts = np.arange(0, N, 61)
+    a = oracle.select(q[:, ts], keys, K=K, t_list=ts)
+    b = oracle.select(q[:, ts][:, :, perm], keys, K=K, t_list=ts)
+    np.testing.assert_array_equal(a["idx"], b["idx"])
+    np.testing.assert_allclose(a["scores"], b["scores"], atol=1e-9)
+
+
+def test_decode_equals_prefill_last_query():
+    rng = np.random.default_rng(14)
+    B, n_cap, Hq, Hkv, K = 3, 3000, 4, 2, 8
+    keys = _rand((B, n_cap, Hkv, D), rng)
+    q_new = _rand((B, Hq, D), rng)
+    lengths = np.array([1, 1500, 2999])
+    dec = oracle.select_last(q_new, keys, lengths, K=K)
+    for b in range(B):
+        n = lengths[b]
+        pre = oracle.select(q_new[b][None, None], keys[b:b + 1, :n], K=K, t_list=[n - 1])
+        np.testing.assert_array_equal(dec["idx"][b], pre["idx"][0, :, 0])
+        np.testing.assert_allclose(dec["scores"][b], pre["scores"][0, :, 0], rtol=0, atol=0)
+
+
+def test_candidates_per_level_bounded_and_output_well_formed():
+    rng = np.random.default_rng(15)
+    N, K = 16421, 32
+    q = _rand((1, N, 4, D), rng)
+    keys = _rand((1, N, 2, D), rng)
+    ts = np.array([0, 63, 64, 2047, 2048, 16420])
+    r = oracle.select(q[:, ts], keys, K=K, t_list=ts)
+    for it, t in enumerate(ts):
+        for kv in range(2):
+            row = r["idx"][0, kv, it]
+            sel = row[row >= 0]
+            assert np.all(np.diff(sel) > 0)
+            assert np.all(sel <= t // 64)
+            assert len(sel) == min(K, t // 64 + 1)
+            assert np.all(row[len(sel):] == -1)
