@@ -1,0 +1,156 @@
+/*
+ * pisa.h -- C ABI of the GB300 (sm_103a) PISA pyramid Top-K block selector.
+ *
+ * The library computes the block-selection stage of PISA block-sparse
+ * attention ("Block Sparse Attention with Log-Linear Complexity", §3.1 Fine to
+ * coarse: building the pyramid; §3.2 Coarse to fine: narrowing the Top-K;
+ * "Scoring: LogSumExp, and why not the mean"; §4.1 the GQA head sum; §5.1 the
+ * prefill and decoding kernels).  Keys are mean-pooled into a pyramid (leaves
+ * of C tokens, then merges of g up to one root); each query then walks it
+ * coarse-to-fine, scoring at most g*K candidates per level by a LogSumExp over
+ * their children's summaries (raw keys at the leaf level), summed over the
+ * query heads of its GQA group, and keeping the Top-K.
+ *
+ * Conventions shared by every call
+ *   - All pointers named "device" are CUDA device pointers owned by the
+ *     caller; the library never allocates device memory.  Host pointers are
+ *     named as such.
+ *   - bf16 tensors are passed as `const void*` (IEEE bfloat16, little endian).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     is asynchronous on it; outputs are valid once the stream reaches them.
+ *   - Layouts are dense, row-major, 16-byte aligned:
+ *       Q       [B, N, Hq,  d]  bf16      K      [B, n_cap, Hkv, d] bf16
+ *       summary [B, Hkv, pisa_pyramid_nodes(n_cap, C, g), d] fp32, levels
+ *               leaf-first (level 1 = leaves, then level 2, ... root last),
+ *               level sizes M_1 = ceil(n_cap/C), M_l = ceil(M_{l-1}/g).
+ *     Query head h belongs to KV head h / (Hq/Hkv) (contiguous groups).
+ *   - Supported sizes: d = 64, C = 64, g = 2, 1 <= K <= 32,
+ *     Hq/Hkv in {1, 2, 4, 8, 16}, 1 <= Hkv <= 32, N <= 2^30.  Anything
+ *     else returns PISA_ERR_UNSUPPORTED (or PISA_ERR_INVALID_ARG when
+ *     malformed).
+ *   - Readings fixed by this library where the method's description is
+ *     silent: logits are q.k/sqrt(d); a ragged node (sequence tail) is the
+ *     mean over the tokens present; causal eligibility of a node for query t
+ *     is "first token <= t", and a child that starts after t is left out of
+ *     its parent's LSE (keys after t are masked in the leaf LSE); the LSE is
+ *     un-normalised; Top-K ties go to the lower node index; the output lists
+ *     the selected leaves in ascending order, padded with -1.
+ *   - Errors: every call returns a pisa_status.  Argument errors are caught
+ *     on the host before anything is launched.  Errors raised inside a
+ *     kernel (a bounded wait that timed out) are recorded in a status word at
+ *     the start of the caller's workspace; read it with
+ *     pisa_check_device_status().  No C++ exception crosses this ABI.
+ */
+#ifndef PISA_H_
+#define PISA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PISA_OK = 0,
+  PISA_ERR_INVALID_ARG = 1,          /* NULL pointer, negative size, N > n_cap, ... */
+  PISA_ERR_UNSUPPORTED = 2,          /* a size outside the supported set above      */
+  PISA_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes below the *_workspace_bytes value  */
+  PISA_ERR_CUDA = 4,                 /* a CUDA runtime / launch error               */
+  PISA_ERR_DEVICE_TIMEOUT = 5,       /* a kernel's bounded wait gave up             */
+  PISA_ERR_DEVICE_BOUNDS = 6         /* a kernel's index check failed               */
+} pisa_status;
+
+/*
+ * Pyramid descriptor (plain struct, all memory caller-owned).
+ *   summaries : device fp32 [B, Hkv, pisa_pyramid_nodes(n_cap, C, g), d]
+ *   keys      : device bf16 [B, n_cap, Hkv, d]; the raw keys the leaf level
+ *               scores against (borrowed; decode appends into it)
+ *   lengths   : device int32 [B], tokens present per sequence (decode); may
+ *               be NULL for prefill-only use
+ *   n_cap     : capacity in tokens; the node layout is fixed by n_cap so a
+ *               decode cache never moves as it grows
+ */
+typedef struct {
+  float* summaries;
+  void* keys;
+  int32_t* lengths;
+  int B, Hkv, d, C, g, n_cap;
+} pisa_pyramid;
+
+/* Number of levels holding nodes for n tokens (1 for n <= C), or -1. */
+int pisa_num_levels(int64_t n, int C, int g);
+
+/* Sum over levels of the node counts for a capacity of n_cap tokens, or -1. */
+int64_t pisa_pyramid_nodes(int64_t n_cap, int C, int g);
+
+/* Row offset of level `level` (1 = leaves) inside one (b, kv) summary block. */
+int64_t pisa_level_offset(int64_t n_cap, int C, int g, int level);
+
+/*
+ * pisa_build_pyramid -- fine-to-coarse mean pooling (§3.1).
+ * Builds every summary of the first N tokens of each sequence from pyr->keys:
+ * leaf i = mean of keys [iC, min((i+1)C, N)); a node of level l >= 2 = the
+ * token-count-weighted mean of its children (= mean of all its raw keys).
+ * Nodes outside the first N tokens are left untouched.  If pyr->lengths is
+ * not NULL, every entry is set to N.  Requires 1 <= N <= n_cap.
+ */
+int pisa_build_pyramid(const pisa_pyramid* pyr, int64_t N, void* stream);
+
+/* Workspace bytes pisa_select_prefill needs for these sizes (0 on bad sizes). */
+size_t pisa_select_workspace_bytes(int B, int64_t N, int Hq, int Hkv, int K);
+
+/*
+ * pisa_select_prefill -- coarse-to-fine Top-K walk for every query (§3.2).
+ *   Q      : device bf16 [B, N, Hq, d]
+ *   pyr    : a pyramid built over the same N tokens (pyr->n_cap may exceed N)
+ *   K      : blocks to keep per query and KV head
+ *   causal : nonzero = query t sees tokens <= t only
+ *   idx    : device int32 [B, Hkv, N, K] out: selected leaf blocks, ascending,
+ *            -1 where fewer than K leaves are eligible
+ *   scores : device fp32 [B, Hkv, N, K] out (may be NULL): the exact leaf score
+ *            (raw-key LSE summed over the group's heads) of each selected
+ *            leaf; -inf in padded slots
+ *   ws     : device workspace of at least pisa_select_workspace_bytes(...)
+ *            bytes, 256-byte aligned; its content is scratch on entry
+ */
+int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K,
+                        int causal, int32_t* idx, float* scores, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* Workspace bytes pisa_decode_append_and_select needs (0 on bad sizes). */
+size_t pisa_decode_workspace_bytes(int B, int Hq, int Hkv, int K);
+
+/*
+ * pisa_decode_append_and_select -- one decoding step ([P1]/§5.1: the decoder
+ * keeps the mean pyramid cached, updates only the new token's leaf mean and its
+ * ancestor path, then walks for the new query).
+ *   q_new  : device bf16 [B, Hq, d], the query of the token being appended
+ *   k_new  : device bf16 [B, Hkv, d], its key
+ *   pyr    : pyramid with keys [B, n_cap, Hkv, d], summaries and lengths (all
+ *            required); for each b the key is written at position
+ *            lengths[b], the leaf and ancestor summaries are refreshed, the
+ *            walk runs for t = lengths[b] (causal), and lengths[b] grows by 1.
+ *            Every lengths[b] must be < n_cap (checked on the device: a full
+ *            sequence is left unchanged and flags PISA_ERR_DEVICE_BOUNDS).
+ *   idx    : device int32 [B, Hkv, K] out; scores: device fp32 [B, Hkv, K] or NULL
+ *   ws     : device workspace of at least pisa_decode_workspace_bytes(...) bytes
+ */
+int pisa_decode_append_and_select(const void* q_new, const void* k_new, int Hq,
+                                  const pisa_pyramid* pyr, int K, int32_t* idx, float* scores,
+                                  void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronises `stream` and returns the status word that kernels of the last
+ * select / decode call on this workspace left in `ws` (PISA_OK if none).
+ */
+int pisa_check_device_status(const void* ws, void* stream);
+
+/* Static, human-readable text for a pisa_status value. */
+const char* pisa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PISA_H_ */

@@ -1,0 +1,238 @@
+"""GB300-native PISA pyramid Top-K block selection.
+
+Thin Python binding over the C ABI of ``include/pisa.h`` (library
+``_build/libpisa.so``, built in-tree by ``build.py``).  This module only
+marshals arguments: PyTorch provides device memory and the current CUDA
+stream; every step of the selection runs in the library's CUDA kernels.  There
+is no CPU fallback: if the library cannot be loaded, every call raises.
+
+Method: "Block Sparse Attention with Log-Linear Complexity" (§3.1 pyramid of
+mean-pooled keys, §3.2 coarse-to-fine Top-K walk, "Scoring: LogSumExp", §4.1
+GQA head sum, §5.1 prefill and decoding kernels).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "PisaError", "Pyramid", "load", "num_levels", "pyramid_nodes", "level_offset",
+    "build_pyramid", "select_workspace_bytes", "select_prefill", "decode_workspace_bytes",
+    "decode_append_and_select", "check_device_status", "status_string", "D", "C", "G_MERGE",
+]
+
+D, C, G_MERGE = 64, 64, 2
+
+_lib = None
+
+
+class PisaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the CUDA library and declare its ABI."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if path is None:
+        path = _build.LIB if os.path.exists(_build.LIB) else _build.build()
+    lib = ctypes.CDLL(path)
+    i32, i64, sz, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+    lib.pisa_num_levels.argtypes = [i64, i32, i32]
+    lib.pisa_num_levels.restype = i32
+    lib.pisa_pyramid_nodes.argtypes = [i64, i32, i32]
+    lib.pisa_pyramid_nodes.restype = i64
+    lib.pisa_level_offset.argtypes = [i64, i32, i32, i32]
+    lib.pisa_level_offset.restype = i64
+    lib.pisa_build_pyramid.argtypes = [vp, i64, vp]
+    lib.pisa_build_pyramid.restype = i32
+    lib.pisa_select_workspace_bytes.argtypes = [i32, i64, i32, i32, i32]
+    lib.pisa_select_workspace_bytes.restype = sz
+    lib.pisa_select_prefill.argtypes = [vp, i32, vp, i64, i32, i32, vp, vp, vp, sz, vp]
+    lib.pisa_select_prefill.restype = i32
+    lib.pisa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.pisa_decode_workspace_bytes.restype = sz
+    lib.pisa_decode_append_and_select.argtypes = [vp, vp, i32, vp, i32, vp, vp, vp, sz, vp]
+    lib.pisa_decode_append_and_select.restype = i32
+    lib.pisa_check_device_status.argtypes = [vp, vp]
+    lib.pisa_check_device_status.restype = i32
+    lib.pisa_status_string.argtypes = [i32]
+    lib.pisa_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+class _PyrStruct(ctypes.Structure):
+    _fields_ = [
+        ("summaries", ctypes.c_void_p),
+        ("keys", ctypes.c_void_p),
+        ("lengths", ctypes.c_void_p),
+        ("B", ctypes.c_int),
+        ("Hkv", ctypes.c_int),
+        ("d", ctypes.c_int),
+        ("C", ctypes.c_int),
+        ("g", ctypes.c_int),
+        ("n_cap", ctypes.c_int),
+    ]
+
+
+def status_string(status: int) -> str:
+    return load().pisa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise PisaError(status, what)
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def num_levels(n: int) -> int:
+    return int(load().pisa_num_levels(n, C, G_MERGE))
+
+
+def pyramid_nodes(n_cap: int) -> int:
+    return int(load().pisa_pyramid_nodes(n_cap, C, G_MERGE))
+
+
+def level_offset(n_cap: int, level: int) -> int:
+    return int(load().pisa_level_offset(n_cap, C, G_MERGE, level))
+
+
+@dataclass
+class Pyramid:
+    """Caller-owned pyramid storage: borrowed keys [B, n_cap, Hkv, 64] bf16,
+    summaries [B, Hkv, nodes(n_cap), 64] fp32 and optional lengths [B] int32."""
+
+    keys: torch.Tensor
+    summaries: torch.Tensor
+    lengths: torch.Tensor | None = None
+
+    @classmethod
+    def allocate(cls, keys: torch.Tensor, with_lengths: bool = False) -> "Pyramid":
+        if keys.dtype != torch.bfloat16 or keys.dim() != 4 or not keys.is_cuda:
+            raise ValueError("keys must be a CUDA bf16 tensor [B, n_cap, Hkv, d]")
+        B, n_cap, Hkv, d = keys.shape
+        nodes = pyramid_nodes(n_cap)
+        summ = torch.empty(B, Hkv, nodes, d, dtype=torch.float32, device=keys.device)
+        lengths = torch.zeros(B, dtype=torch.int32, device=keys.device) if with_lengths else None
+        return cls(keys.contiguous(), summ, lengths)
+
+    @property
+    def B(self):
+        return self.keys.shape[0]
+
+    @property
+    def n_cap(self):
+        return self.keys.shape[1]
+
+    @property
+    def Hkv(self):
+        return self.keys.shape[2]
+
+    def struct(self) -> _PyrStruct:
+        return _PyrStruct(self.summaries.data_ptr(), self.keys.data_ptr(),
+                          self.lengths.data_ptr() if self.lengths is not None else None,
+                          self.B, self.Hkv, self.keys.shape[3], C, G_MERGE, self.n_cap)
+
+    def level(self, level: int, n: int | None = None) -> torch.Tensor:
+        """View of the summaries of one level [B, Hkv, M_level(n), d]."""
+        n = self.n_cap if n is None else n
+        off = level_offset(self.n_cap, level)
+        m = -(-n // (C << (level - 1)))
+        return self.summaries[:, :, off:off + m]
+
+
+def build_pyramid(keys: torch.Tensor | Pyramid, N: int | None = None, with_lengths: bool = False,
+                  stream=None) -> Pyramid:
+    """Mean pyramid over the first N tokens (§3.1).  Accepts raw keys or a Pyramid."""
+    pyr = keys if isinstance(keys, Pyramid) else Pyramid.allocate(keys, with_lengths)
+    N = pyr.n_cap if N is None else N
+    st = pyr.struct()
+    _check(load().pisa_build_pyramid(ctypes.byref(st), N, _stream(stream)), "pisa_build_pyramid")
+    return pyr
+
+
+def select_workspace_bytes(B: int, N: int, Hq: int, Hkv: int, K: int) -> int:
+    return int(load().pisa_select_workspace_bytes(B, N, Hq, Hkv, K))
+
+
+def select_prefill(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True, N: int | None = None,
+                   with_scores: bool = True, workspace: torch.Tensor | None = None,
+                   out: tuple | None = None, stream=None):
+    """Coarse-to-fine Top-K for every query (§3.2).
+
+    Q [B, N, Hq, 64] bf16 (CUDA).  Returns (idx [B, Hkv, N, K] int32, scores
+    [B, Hkv, N, K] fp32 or None).
+    """
+    if Q.dtype != torch.bfloat16 or not Q.is_cuda or Q.dim() != 4:
+        raise ValueError("Q must be a CUDA bf16 tensor [B, N, Hq, d]")
+    B, NQ, Hq, _ = Q.shape
+    N = NQ if N is None else N
+    lib = load()
+    need = lib.pisa_select_workspace_bytes(B, N, Hq, pyr.Hkv, K)
+    if need == 0:
+        _check(2, "pisa_select_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    if out is None:
+        idx = torch.empty(B, pyr.Hkv, N, K, dtype=torch.int32, device=Q.device)
+        scores = torch.empty(B, pyr.Hkv, N, K, dtype=torch.float32, device=Q.device) if with_scores else None
+    else:
+        idx, scores = out
+    st = pyr.struct()
+    _check(lib.pisa_select_prefill(_ptr(Q), Hq, ctypes.byref(st), N, K, int(causal), _ptr(idx),
+                                   _ptr(scores), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "pisa_select_prefill")
+    return idx, scores
+
+
+def decode_workspace_bytes(B: int, Hq: int, Hkv: int, K: int) -> int:
+    return int(load().pisa_decode_workspace_bytes(B, Hq, Hkv, K))
+
+
+def decode_append_and_select(q_new: torch.Tensor, k_new: torch.Tensor, pyr: Pyramid, K: int,
+                             with_scores: bool = True, workspace: torch.Tensor | None = None,
+                             out: tuple | None = None, stream=None):
+    """One decoding step: append k_new at lengths[b], refresh that leaf and its
+    ancestors, then select for q_new.  Returns (idx [B, Hkv, K], scores)."""
+    if pyr.lengths is None:
+        raise ValueError("decode needs a Pyramid with lengths")
+    B, Hq, _ = q_new.shape
+    lib = load()
+    need = lib.pisa_decode_workspace_bytes(B, Hq, pyr.Hkv, K)
+    if need == 0:
+        _check(2, "pisa_decode_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_new.device)
+    if out is None:
+        idx = torch.empty(B, pyr.Hkv, K, dtype=torch.int32, device=q_new.device)
+        scores = torch.empty(B, pyr.Hkv, K, dtype=torch.float32, device=q_new.device) if with_scores else None
+    else:
+        idx, scores = out
+    st = pyr.struct()
+    _check(lib.pisa_decode_append_and_select(_ptr(q_new), _ptr(k_new), Hq, ctypes.byref(st), K, _ptr(idx),
+                                             _ptr(scores), _ptr(workspace), workspace.numel(),
+                                             _stream(stream)),
+           "pisa_decode_append_and_select")
+    return idx, scores
+
+
+def check_device_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and return the kernels' status word (0 = ok)."""
+    return int(load().pisa_check_device_status(_ptr(workspace), _stream(stream)))

@@ -1,0 +1,22 @@
+// api.cuh -- host-side launchers shared between the C ABI layer and kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace pisa {
+
+cudaError_t launch_build_pyramid(const __nv_bfloat16* keys, float* summ, const Levels& lv,
+                                 long long N, long long n_cap, int B, int Hkv, int32_t* lengths,
+                                 cudaStream_t s);
+
+cudaError_t launch_prefill_warp(const __nv_bfloat16* Q, const float* summ, const __nv_bfloat16* keys,
+                                const Levels& lv, long long N, long long n_cap, int B, int Hq,
+                                int Hkv, int K, int causal, int32_t* surv, int32_t* idx,
+                                float* scores, cudaStream_t s);
+
+cudaError_t launch_decode_warp(const __nv_bfloat16* q_new, const __nv_bfloat16* k_new,
+                               __nv_bfloat16* keys, float* summ, int32_t* lengths,
+                               const Levels& cap_lv, long long n_cap, int B, int Hq, int Hkv, int K,
+                               int32_t* idx, float* scores, int* status, cudaStream_t s);
+
+}  // namespace pisa

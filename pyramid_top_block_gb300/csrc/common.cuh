@@ -1,0 +1,98 @@
+// common.cuh -- shared device helpers of the GB300 PISA selector.
+//
+// Fixed geometry of this build: head dim d = 64, leaf size C = 64, merge
+// factor g = 2 ("Block Sparse Attention with Log-Linear Complexity", §7.3:
+// d = 64, C = 64, g = 2).  A node of level l >= 1 spans 64 * 2^(l-1) tokens;
+// level 0 is the raw keys.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pisa.h"
+
+namespace pisa {
+
+constexpr int kD = 64;          // head dimension
+constexpr int kC = 64;          // leaf size (tokens)
+constexpr int kLog2C = 6;
+constexpr int kMaxLevels = 32;  // N <= 2^30 tokens -> at most 25 levels
+constexpr int kMaxK = 32;
+constexpr float kScale = 0.125f;  // 1/sqrt(64), exact in fp32
+
+// Level geometry passed by value to kernels.  Sizes M[l] are those of the
+// current sequence length; row offsets off[l] come from the capacity n_cap so
+// that a decode cache keeps its layout while it grows.
+struct Levels {
+  int L;                         // levels that hold nodes for the current length
+  int M[kMaxLevels + 1];         // M[l], l = 1..L (M[0] = tokens)
+  long long off[kMaxLevels + 1]; // row offset of level l inside one (b, kv) block
+  long long total;               // rows per (b, kv) block (from n_cap)
+};
+
+// M_1 = ceil(n / C), M_l = ceil(M_{l-1} / 2) = ceil(n / (C * 2^(l-1))).
+__host__ __device__ inline int num_levels_for(long long n) {
+  long long m = (n + kC - 1) >> kLog2C;
+  int L = 1;
+  while (m > 1) {
+    m = (m + 1) >> 1;
+    ++L;
+  }
+  return L;
+}
+
+__host__ __device__ inline long long level_size_for(long long n, int l) {
+  if (l == 0) return n;
+  long long w = (long long)kC << (l - 1);
+  return (n + w - 1) / w;
+}
+
+// First token of node i at level l (level 0: the raw key i itself).
+__host__ __device__ inline long long node_start(int l, long long i) {
+  return l == 0 ? i : (i << (kLog2C + l - 1));
+}
+
+// Tokens node i of level l holds when the sequence has n tokens.
+__host__ __device__ inline int node_count(int l, long long i, long long n) {
+  long long s = node_start(l, i);
+  long long e = (i + 1) << (kLog2C + l - 1);
+  if (e > n) e = n;
+  return (int)(e - s);
+}
+
+__device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Unpack 8 bf16 held in a 16-byte vector into fp32 (exact).
+__device__ __forceinline__ void unpack8(const uint4 v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// Token-count-weighted mean of two children (exact formula, no contraction):
+// parent = (m0 * n0 + m1 * n1) / (n0 + n1).  A parent with one child equals it.
+// Shared by the prefill build and the decode path update so both produce the
+// same bits for the same node.
+__device__ __forceinline__ float merge_mean(float m0, int n0, float m1, int n1) {
+  if (n1 <= 0) return m0;
+  float s = __fadd_rn(__fmul_rn(m0, (float)n0), __fmul_rn(m1, (float)n1));
+  return __fdiv_rn(s, (float)(n0 + n1));
+}
+
+// Record a device-side error in the caller's workspace status word (first
+// error wins).
+__device__ __forceinline__ void set_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// log(exp(a) + exp(b)) without overflow.
+__device__ __forceinline__ float lse2(float a, float b) {
+  float m = fmaxf(a, b);
+  return m + log1pf(expf(-fabsf(a - b)));
+}
+
+}  // namespace pisa

@@ -1,0 +1,181 @@
+// pisa_api.cu -- the C ABI (include/pisa.h): argument checks, workspace
+// layout and launch sequencing.  No allocation, no exceptions, one stream.
+#include <cmath>
+#include <cstring>
+
+#include "api.cuh"
+
+using namespace pisa;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kStatusBytes = 256;  // status word + reserved counters
+
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+bool pow2_group(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16; }
+
+// Level geometry for a sequence of n tokens stored in a layout for n_cap.
+Levels make_levels(long long n, long long n_cap) {
+  Levels lv;
+  std::memset(&lv, 0, sizeof(lv));
+  lv.L = num_levels_for(n);
+  const int Lcap = num_levels_for(n_cap);
+  lv.M[0] = (int)n;
+  long long off = 0;
+  for (int l = 1; l <= Lcap; ++l) {
+    lv.off[l] = off;
+    off += level_size_for(n_cap, l);
+    if (l <= lv.L) lv.M[l] = (int)level_size_for(n, l);
+  }
+  lv.total = off;
+  return lv;
+}
+
+// Sizes the library handles; returns PISA_OK or the status to report.
+int check_geometry(int B, long long N, int Hq, int Hkv, int d, int C, int g, int K) {
+  if (B < 1 || N < 1 || Hq < 1 || Hkv < 1 || d < 1 || C < 1 || g < 1 || K < 1)
+    return PISA_ERR_INVALID_ARG;
+  if (Hq % Hkv) return PISA_ERR_UNSUPPORTED;
+  if (d != kD || C != kC || g != 2) return PISA_ERR_UNSUPPORTED;
+  if (K > kMaxK || !pow2_group(Hq / Hkv) || Hkv > 32) return PISA_ERR_UNSUPPORTED;
+  if (N > (1LL << 30)) return PISA_ERR_UNSUPPORTED;
+  return PISA_OK;
+}
+
+int check_pyr(const pisa_pyramid* p) {
+  if (!p || !p->summaries || !p->keys) return PISA_ERR_INVALID_ARG;
+  if (p->B < 1 || p->Hkv < 1 || p->n_cap < 1) return PISA_ERR_INVALID_ARG;
+  if (p->d != kD || p->C != kC || p->g != 2 || p->Hkv > 32) return PISA_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(p->summaries) | reinterpret_cast<uintptr_t>(p->keys)) & 15)
+    return PISA_ERR_INVALID_ARG;
+  return PISA_OK;
+}
+
+// Workspace of the prefill selection: [status 256 B][surv2: B*Hkv*N*K int32].
+struct PrefillWs {
+  size_t status, surv, total;
+};
+
+PrefillWs prefill_layout(int B, long long N, int Hkv, int K) {
+  PrefillWs w;
+  size_t o = 0;
+  w.status = o;
+  o += align_up(kStatusBytes);
+  w.surv = o;
+  o += align_up(sizeof(int32_t) * (size_t)B * Hkv * (size_t)N * K);
+  w.total = o;
+  return w;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PISA_OK : PISA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int pisa_num_levels(int64_t n, int C, int g) {
+  if (n < 1 || C != kC || g != 2) return -1;
+  return num_levels_for(n);
+}
+
+int64_t pisa_pyramid_nodes(int64_t n_cap, int C, int g) {
+  if (n_cap < 1 || C != kC || g != 2) return -1;
+  return make_levels(n_cap, n_cap).total;
+}
+
+int64_t pisa_level_offset(int64_t n_cap, int C, int g, int level) {
+  if (n_cap < 1 || C != kC || g != 2) return -1;
+  const Levels lv = make_levels(n_cap, n_cap);
+  if (level < 1 || level > lv.L) return -1;
+  return lv.off[level];
+}
+
+int pisa_build_pyramid(const pisa_pyramid* pyr, int64_t N, void* stream) {
+  int st = check_pyr(pyr);
+  if (st) return st;
+  if (N < 1 || N > pyr->n_cap) return PISA_ERR_INVALID_ARG;
+  if (N > (1LL << 30) || pyr->n_cap > (1LL << 30)) return PISA_ERR_UNSUPPORTED;
+  const Levels lv = make_levels(N, pyr->n_cap);
+  return cuda_status(launch_build_pyramid(static_cast<const __nv_bfloat16*>(pyr->keys), pyr->summaries, lv,
+                                          N, pyr->n_cap, pyr->B, pyr->Hkv, pyr->lengths,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+size_t pisa_select_workspace_bytes(int B, int64_t N, int Hq, int Hkv, int K) {
+  if (check_geometry(B, N, Hq, Hkv, kD, kC, 2, K) != PISA_OK) return 0;
+  return prefill_layout(B, N, Hkv, K).total;
+}
+
+int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
+                        int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream) {
+  int st = check_pyr(pyr);
+  if (st) return st;
+  if (!Q || !idx || !ws) return PISA_ERR_INVALID_ARG;
+  st = check_geometry(pyr->B, N, Hq, pyr->Hkv, pyr->d, pyr->C, pyr->g, K);
+  if (st) return st;
+  if (N > pyr->n_cap) return PISA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(Q) & 15) || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)))
+    return PISA_ERR_INVALID_ARG;
+  const PrefillWs w = prefill_layout(pyr->B, N, pyr->Hkv, K);
+  if (ws_bytes < w.total) return PISA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws);
+  cudaError_t e = cudaMemsetAsync(base + w.status, 0, kStatusBytes, s);
+  if (e != cudaSuccess) return PISA_ERR_CUDA;
+  const Levels lv = make_levels(N, pyr->n_cap);
+  e = launch_prefill_warp(static_cast<const __nv_bfloat16*>(Q), pyr->summaries,
+                          static_cast<const __nv_bfloat16*>(pyr->keys), lv, N, pyr->n_cap, pyr->B, Hq,
+                          pyr->Hkv, K, causal, reinterpret_cast<int32_t*>(base + w.surv), idx, scores, s);
+  return cuda_status(e);
+}
+
+size_t pisa_decode_workspace_bytes(int B, int Hq, int Hkv, int K) {
+  if (check_geometry(B, 1, Hq, Hkv, kD, kC, 2, K) != PISA_OK) return 0;
+  return align_up(kStatusBytes);
+}
+
+int pisa_decode_append_and_select(const void* q_new, const void* k_new, int Hq, const pisa_pyramid* pyr,
+                                  int K, int32_t* idx, float* scores, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  int st = check_pyr(pyr);
+  if (st) return st;
+  if (!q_new || !k_new || !idx || !ws || !pyr->lengths) return PISA_ERR_INVALID_ARG;
+  st = check_geometry(pyr->B, pyr->n_cap, Hq, pyr->Hkv, pyr->d, pyr->C, pyr->g, K);
+  if (st) return st;
+  if (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) return PISA_ERR_INVALID_ARG;
+  if (ws_bytes < align_up(kStatusBytes)) return PISA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes, s);
+  if (e != cudaSuccess) return PISA_ERR_CUDA;
+  const Levels cap_lv = make_levels(pyr->n_cap, pyr->n_cap);
+  e = launch_decode_warp(static_cast<const __nv_bfloat16*>(q_new), static_cast<const __nv_bfloat16*>(k_new),
+                         static_cast<__nv_bfloat16*>(pyr->keys), pyr->summaries, pyr->lengths, cap_lv,
+                         pyr->n_cap, pyr->B, Hq, pyr->Hkv, K, idx, scores, static_cast<int*>(ws), s);
+  return cuda_status(e);
+}
+
+int pisa_check_device_status(const void* ws, void* stream) {
+  if (!ws) return PISA_ERR_INVALID_ARG;
+  int h = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&h, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return PISA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PISA_ERR_CUDA;
+  return h;
+}
+
+const char* pisa_status_string(int status) {
+  switch (status) {
+    case PISA_OK: return "ok";
+    case PISA_ERR_INVALID_ARG: return "invalid argument";
+    case PISA_ERR_UNSUPPORTED: return "unsupported size (needs d=64, C=64, g=2, K<=32, Hq/Hkv in {1,2,4,8,16})";
+    case PISA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PISA_ERR_CUDA: return "CUDA runtime or launch error";
+    case PISA_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
+    case PISA_ERR_DEVICE_BOUNDS: return "a kernel's bounds check failed (e.g. decode cache full)";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"
