@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Selection-latency benchmark of the GB300 PISA block selector.
+
+One step = one full selection pass on the workload of the pages' latency
+benchmark ("Block Sparse Attention with Log-Linear Complexity", §7.3: random
+bf16 Q/K with a fixed seed, B=1, Hq=32, Hkv=2, d=64, C=64, K=8, g=2; timing
+covers summary construction and all selection levels, not attention):
+pisa_build_pyramid + pisa_select_prefill at N = 262144, causal.
+
+Prints one JSON line (rank 0).  `value` is query-rows/s (B*N per pass) over all
+ranks; `ms_per_step` the mean device time of one pass (CUDA events, L2 flushed
+between passes).  `--impl reference` times the fp64 CPU oracle instead, on a
+bounded sample of query rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selection ms/pass and query-rows/s at 32K–256K; % of roofline (1×GB300)"
+UNIT = "query-rows/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def level_sizes(n, C=64):
+    m = -(-n // C)
+    out = [m]
+    while m > 1:
+        m = -(-m // 2)
+        out.append(m)
+    return out
+
+
+def algorithmic(w):
+    """North-star work model of one pass (non-causal upper bound).
+
+    FLOPs = Hq*B*N*[g*K*C*2d (leaf) + (#scored intermediate levels)*g*K*g*2d]
+    bytes = Q + K read once + pyramid written and read once + idx written.
+    A level is scored when it has more than K candidates: with g = 2 the walk
+    reaches level l with min(M_l, 2K) candidates.
+    """
+    B, N, Hq, Hkv, K, d, C, g = w["B"], w["N"], w["Hq"], w["Hkv"], w["K"], 64, 64, 2
+    sizes = level_sizes(N, C)
+    L = len(sizes)
+    scored_inter = sum(1 for lvl in range(2, L) if min(sizes[lvl - 1], g * K) > K)
+    leaf_scored = min(sizes[0], g * K) > K
+    leaf_flops = Hq * B * N * g * K * C * 2 * d if leaf_scored else 0
+    inter_flops = Hq * B * N * scored_inter * g * K * g * 2 * d
+    pyr_bytes = B * Hkv * sum(sizes) * d * 4
+    byts = B * N * Hq * d * 2 + B * N * Hkv * d * 2 + 2 * pyr_bytes + B * Hkv * N * K * 4
+    return dict(flops=leaf_flops + inter_flops, leaf_flops=leaf_flops, inter_flops=inter_flops,
+                bytes=byts, scored_intermediate_levels=scored_inter, levels=L)
+
+
+class Clocks:
+    """nvidia-smi sampler for the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                     power=float(parts[3]) if parts[3] not in ("[N/A]", "") else 0.0,
+                                     hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_rows_per_s(q, k, w, target_s: float):
+    """Time the fp64 oracle (as it stands, all host threads) on a bounded sample:
+    its pyramid build over all N tokens, plus the walks of n query rows (all KV
+    heads) spread evenly over the sequence.  A full pass is then
+    t_build + (B*N) * t_row, and the value is B*N over that time."""
+    import oracle
+    oracle.build()
+    N = w["N"]
+    kf = k.float().numpy()
+    t0 = time.perf_counter()
+    oracle.build_pyramid(kf)
+    t_build = time.perf_counter() - t0
+
+    def run(n):
+        t = np.unique(np.linspace(0, N - 1, n).round().astype(np.int64))
+        qr = q[:, t].float().numpy()
+        t0 = time.perf_counter()
+        oracle.select(qr, kf, K=w["K"], t_list=t)
+        return len(t), max(time.perf_counter() - t0 - t_build, 1e-9)
+
+    n0, s0 = run(16)
+    per = s0 / n0
+    n = int(max(16, min(N, (target_s - t_build) / max(per, 1e-9))))
+    n, secs = run(n)
+    t_row = secs / (n * w["B"])
+    t_full = t_build + w["B"] * N * t_row
+    return dict(value=w["B"] * N / t_full, unit=UNIT, cores=oracle.max_threads(), kind="oracle",
+                seconds=secs + t_build, rows=n * w["B"],
+                sample=f"fp64 pyramid build over all N={N} tokens ({t_build:.2f} s) + walks of {n} query "
+                       f"rows x {w['Hkv']} KV heads evenly spaced over the sequence ({secs:.2f} s); "
+                       f"full pass extrapolated as build + B*N rows")
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    from pyramid_top_block_gb300 import synth
+    q, k, w = synth.make(args.workload)
+    vals = []
+    info = None
+    per_step = max(0.5, min(args.ref_step_s, 150.0 / (args.warmup + args.steps)))
+    for i in range(args.warmup + args.steps):
+        r = oracle_rows_per_s(q, k, w, target_s=per_step)
+        if i >= args.warmup:
+            vals.append(r["value"])
+            info = r
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * w["B"] * w["N"] / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": cfg(w, args),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": info["cores"], "kind": "oracle",
+                             "sample": info["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cfg(w, args):
+    return {"workload": args.workload, "B": w["B"], "N": w["N"], "Hq": w["Hq"], "Hkv": w["Hkv"], "d": 64,
+            "C": 64, "g": 2, "K": w["K"], "causal": True, "seed": w["seed"],
+            "inputs": "bf16 i.i.d. N(0,1) Q/K" if w["kind"] == "iid" else "bf16 structured",
+            "l2": "flushed between timed passes (256 MiB write)", "accumulate": "fp32"}
+
+
+def run_ours(args):
+    import torch
+    import pyramid_top_block_gb300 as pisa
+    from pyramid_top_block_gb300 import synth
+
+    world, rank, local = dist_setup()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pk, pk_kind = peaks()
+    q, k, w = synth.make(args.workload)
+    alg = algorithmic(w)
+    K = w["K"]
+    lib = pisa.load()
+    qd, kd = q.to(dev), k.to(dev)
+    pyr = pisa.Pyramid.allocate(kd)
+    B, N, Hq, Hkv = w["B"], w["N"], w["Hq"], w["Hkv"]
+    ws = torch.empty(pisa.select_workspace_bytes(B, N, Hq, Hkv, K), dtype=torch.uint8, device=dev)
+    idx = torch.empty(B, Hkv, N, K, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    phases = pisa.prefill_phases()
+
+    def step(ev_build=None):
+        pisa.build_pyramid(pyr)
+        if ev_build is not None:
+            ev_build.record(stream)
+        pisa.select_prefill(qd, pyr, K, workspace=ws, out=(idx, None), with_scores=False)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    n = args.steps
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    ev_s = [mk() for _ in range(n)]
+    ev_e = [mk() for _ in range(n)]
+    ev_b = [mk() for _ in range(n)]
+    ev_p = [[mk() for _ in range(len(phases) + 1)] for _ in range(n)]
+    for evs in ev_p:  # torch creates the CUDA event at its first record
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+    clocks = Clocks(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = pisa.kernel_launches()
+    for i in range(n):
+        flush.zero_()
+        pisa.set_phase_events(ev_p[i])
+        ev_s[i].record(stream)
+        step(ev_b[i])
+        ev_e[i].record(stream)
+    torch.cuda.synchronize()
+    launches = pisa.kernel_launches() - launches0
+    pisa.set_phase_events(None)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(n)]
+    total = sum(ms)
+    if dist:
+        t = torch.tensor([total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total = float(t.item())
+    ms_step = total / n
+    value = world * B * N / (ms_step / 1000.0)
+    phase_ms = {"build": statistics.mean(ev_s[i].elapsed_time(ev_b[i]) for i in range(n))}
+    for j, name in enumerate(phases):
+        phase_ms[name] = statistics.mean(pisa.event_elapsed_ms(ev_p[i][j], ev_p[i][j + 1]) for i in range(n))
+
+    # dominant kernel roofline (algorithmic work of that kernel / its event time)
+    dom = max(phase_ms, key=phase_ms.get)
+    tf_peak = pk["bf16_tflops"]
+    if dom == "build":
+        bytes_build = B * N * Hkv * 64 * 2 + B * Hkv * pisa.pyramid_nodes(N) * 64 * 4
+        achieved = bytes_build / (phase_ms[dom] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": None}
+    else:
+        fl = alg["leaf_flops"] if dom == "leaf" else alg["inter_flops"]
+        achieved = fl / (phase_ms[dom] / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": achieved / tf_peak, "traffic": None}
+    roof.update({"kernel": dom, "peak_source": f"{pk_kind} bf16 burst" if roof["unit"] == "TFLOP/s"
+                 else f"{pk_kind} HBM copy"})
+    t_tensor = alg["flops"] / (tf_peak * 1e12) * 1e3
+    t_hbm = alg["bytes"] / (pk["hbm_gbs"] * 1e9) * 1e3
+    pass_roof = {"flops": alg["flops"], "min_bytes": alg["bytes"], "t_tensor_ms": t_tensor, "t_hbm_ms": t_hbm,
+                 "t_roofline_ms": max(t_tensor, t_hbm), "frac": max(t_tensor, t_hbm) / ms_step,
+                 "peaks": f"{pk_kind}: {tf_peak} TFLOP/s bf16 burst, {pk['hbm_gbs']} GB/s"}
+
+    # end to end through the public API with host buffers (pinned), copies inside
+    e2e = None
+    if not args.no_e2e:
+        qh = q.pin_memory()
+        kh = k.pin_memory()
+        idx_h = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+        for _ in range(2):
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            step()
+            idx_h.copy_(idx, non_blocking=True)
+        torch.cuda.synchronize()
+        ne = max(3, min(n, 20))
+        es, ee = mk(), mk()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        es.record(stream)
+        for _ in range(ne):
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            step()
+            idx_h.copy_(idx, non_blocking=True)
+        ee.record(stream)
+        torch.cuda.synchronize()
+        e_ms = es.elapsed_time(ee) / ne
+        if dist:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * B * N / (e_ms / 1e3), "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": qh.numel() * 2 + kh.numel() * 2,
+               "d2h_bytes_per_step": idx_h.numel() * 4}
+
+    decode = None
+    if not args.no_decode and rank == 0:
+        decode = bench_decode(torch, pisa, synth, dev, args)
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        cpu = oracle_rows_per_s(q, k, w, target_s=args.cpu_s)
+        cpu.pop("seconds", None)
+        cpu.pop("rows", None)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg(w, args),
+                "roofline": roof, "roofline_pass": pass_roof, "phases_ms": phase_ms,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+                "decode": decode}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def bench_decode(torch, pisa, synth, dev, args):
+    """µs per decode step: 16 sequences with a 131072-token cached pyramid,
+    Hq=32, Hkv=2, K=8; each step appends one key per sequence and selects."""
+    B, Hq, Hkv, K, n_ctx, steps = 16, 32, 2, 8, 131072, args.decode_steps
+    n_cap = n_ctx + steps + 8
+    cache, g = synth.decode_context(B, n_ctx, n_cap, Hkv, seed=2)
+    pyr = pisa.Pyramid.allocate(cache.to(dev), with_lengths=True)
+    del cache
+    pisa.build_pyramid(pyr, N=n_ctx)
+    qs, ks = [], []
+    for _ in range(steps):
+        a, b = synth.decode_step(g, B, Hq, Hkv)
+        qs.append(a)
+        ks.append(b)
+    qd = torch.stack(qs).to(dev)
+    kd = torch.stack(ks).to(dev)
+    ws = torch.empty(pisa.decode_workspace_bytes(B, Hq, Hkv, K), dtype=torch.uint8, device=dev)
+    idx = torch.empty(B, Hkv, K, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for s in range(steps):
+        pisa.decode_append_and_select(qd[s], kd[s], pyr, K, workspace=ws, out=(idx, None), with_scores=False)
+    ee.record(stream)
+    torch.cuda.synchronize()
+    st = pisa.check_device_status(ws)
+    return {"us_per_step": es.elapsed_time(ee) * 1000.0 / steps, "steps": steps, "B": B, "n_ctx": n_ctx,
+            "Hq": Hq, "Hkv": Hkv, "K": K, "status": st}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="latency-256k")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-s", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-step-s", type=float, default=6.0, help="seconds of oracle work per reference step")
+    ap.add_argument("--decode-steps", type=int, default=256)
+    args = ap.parse_args()
+    from pyramid_top_block_gb300 import synth
+    if args.workload not in synth.WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}")
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -146,6 +146,24 @@ int pisa_decode_append_and_select(const void* q_new, const void* k_new, int Hq,
  */
 int pisa_check_device_status(const void* ws, void* stream);
 
+/*
+ * Profiling aids (host-side, not thread-safe: call from one host thread).
+ * pisa_kernel_launches: kernels this library has launched since it was loaded.
+ * pisa_set_phase_events: attach n_events cudaEvent_t handles (created by the
+ *   caller, passed as void*); pisa_select_prefill then records event i at the
+ *   start of phase i on its stream and event pisa_prefill_phase_count() at its
+ *   end.  n_events = 0 detaches.  Returns PISA_OK or PISA_ERR_INVALID_ARG.
+ * pisa_prefill_phase_count / pisa_prefill_phase_name: the phases of
+ *   pisa_select_prefill in launch order (static strings).
+ * pisa_event_elapsed_ms: milliseconds between two recorded events (cudaEvent_t
+ *   passed as void*), for events the library recorded on the caller's behalf.
+ */
+uint64_t pisa_kernel_launches(void);
+int pisa_event_elapsed_ms(void* start, void* end, float* ms);
+int pisa_set_phase_events(void* const* events, int n_events);
+int pisa_prefill_phase_count(void);
+const char* pisa_prefill_phase_name(int phase);
+
 /* Static, human-readable text for a pisa_status value. */
 const char* pisa_status_string(int status);
 

@@ -23,7 +23,8 @@ from . import build as _build
 __all__ = [
     "PisaError", "Pyramid", "load", "num_levels", "pyramid_nodes", "level_offset",
     "build_pyramid", "select_workspace_bytes", "select_prefill", "decode_workspace_bytes",
-    "decode_append_and_select", "check_device_status", "status_string", "D", "C", "G_MERGE",
+    "decode_append_and_select", "check_device_status", "status_string", "kernel_launches",
+    "prefill_phases", "set_phase_events", "D", "C", "G_MERGE",
 ]
 
 D, C, G_MERGE = 64, 64, 2
@@ -66,6 +67,16 @@ def load(path: str | None = None):
     lib.pisa_check_device_status.restype = i32
     lib.pisa_status_string.argtypes = [i32]
     lib.pisa_status_string.restype = ctypes.c_char_p
+    lib.pisa_kernel_launches.argtypes = []
+    lib.pisa_kernel_launches.restype = ctypes.c_uint64
+    lib.pisa_set_phase_events.argtypes = [ctypes.c_void_p, i32]
+    lib.pisa_set_phase_events.restype = i32
+    lib.pisa_prefill_phase_count.argtypes = []
+    lib.pisa_prefill_phase_count.restype = i32
+    lib.pisa_prefill_phase_name.argtypes = [i32]
+    lib.pisa_prefill_phase_name.restype = ctypes.c_char_p
+    lib.pisa_event_elapsed_ms.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_float)]
+    lib.pisa_event_elapsed_ms.restype = i32
     _lib = lib
     return lib
 
@@ -231,6 +242,37 @@ def decode_append_and_select(q_new: torch.Tensor, k_new: torch.Tensor, pyr: Pyra
                                              _stream(stream)),
            "pisa_decode_append_and_select")
     return idx, scores
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched since it was loaded."""
+    return int(load().pisa_kernel_launches())
+
+
+def prefill_phases() -> list[str]:
+    lib = load()
+    return [lib.pisa_prefill_phase_name(i).decode() for i in range(lib.pisa_prefill_phase_count())]
+
+
+def set_phase_events(events: list | None) -> None:
+    """Attach torch.cuda.Event objects recorded at the prefill phase boundaries
+    (len = number of phases + 1), or None to detach."""
+    lib = load()
+    if not events:
+        _check(lib.pisa_set_phase_events(None, 0), "pisa_set_phase_events")
+        return
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    set_phase_events._keep = arr
+    _check(lib.pisa_set_phase_events(arr, len(events)), "pisa_set_phase_events")
+
+
+def event_elapsed_ms(start, end) -> float:
+    """Milliseconds between two torch.cuda.Event objects, either of which may
+    have been recorded by the library (phase events)."""
+    out = ctypes.c_float()
+    _check(load().pisa_event_elapsed_ms(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(end.cuda_event),
+                                        ctypes.byref(out)), "pisa_event_elapsed_ms")
+    return float(out.value)
 
 
 def check_device_status(workspace: torch.Tensor, stream=None) -> int:

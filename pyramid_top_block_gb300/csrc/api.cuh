@@ -5,6 +5,14 @@
 
 namespace pisa {
 
+// Counts kernels this library launched (a profiling aid, not synchronised with
+// the device).  Every launcher calls note_launch() once per <<<>>> launch.
+void note_launch(int n = 1);
+
+// Records the caller's profiling event for phase boundary `i` of the current
+// select call on stream s, if the caller attached events (no-op otherwise).
+void mark_phase(int i, cudaStream_t s);
+
 cudaError_t launch_build_pyramid(const __nv_bfloat16* keys, float* summ, const Levels& lv,
                                  long long N, long long n_cap, int B, int Hkv, int32_t* lengths,
                                  cudaStream_t s);

@@ -1,5 +1,6 @@
 // pisa_api.cu -- the C ABI (include/pisa.h): argument checks, workspace
 // layout and launch sequencing.  No allocation, no exceptions, one stream.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -8,8 +9,22 @@
 using namespace pisa;
 
 namespace {
+std::atomic<unsigned long long> g_launches{0};
+cudaEvent_t g_phase_events[16];
+int g_n_phase_events = 0;
+}  // namespace
+
+namespace pisa {
+void note_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+void mark_phase(int i, cudaStream_t s) {
+  if (i >= 0 && i < g_n_phase_events && g_phase_events[i]) cudaEventRecord(g_phase_events[i], s);
+}
+}  // namespace pisa
+
+namespace {
 
 constexpr size_t kAlign = 256;
+constexpr int kPrefillPhases = 2;
 constexpr size_t kStatusBytes = 256;  // status word + reserved counters
 
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
@@ -125,6 +140,7 @@ int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t 
   cudaError_t e = cudaMemsetAsync(base + w.status, 0, kStatusBytes, s);
   if (e != cudaSuccess) return PISA_ERR_CUDA;
   const Levels lv = make_levels(N, pyr->n_cap);
+  mark_phase(0, s);
   e = launch_prefill_warp(static_cast<const __nv_bfloat16*>(Q), pyr->summaries,
                           static_cast<const __nv_bfloat16*>(pyr->keys), lv, N, pyr->n_cap, pyr->B, Hq,
                           pyr->Hkv, K, causal, reinterpret_cast<int32_t*>(base + w.surv), idx, scores, s);
@@ -163,6 +179,29 @@ int pisa_check_device_status(const void* ws, void* stream) {
   if (cudaMemcpyAsync(&h, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return PISA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return PISA_ERR_CUDA;
   return h;
+}
+
+uint64_t pisa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int pisa_set_phase_events(void* const* events, int n_events) {
+  if (n_events < 0 || n_events > 16 || (n_events > 0 && !events)) return PISA_ERR_INVALID_ARG;
+  for (int i = 0; i < n_events; ++i) g_phase_events[i] = static_cast<cudaEvent_t>(events[i]);
+  g_n_phase_events = n_events;
+  return PISA_OK;
+}
+
+int pisa_prefill_phase_count(void) { return kPrefillPhases; }
+
+int pisa_event_elapsed_ms(void* start, void* end, float* ms) {
+  if (!start || !end || !ms) return PISA_ERR_INVALID_ARG;
+  return cudaEventElapsedTime(ms, static_cast<cudaEvent_t>(start), static_cast<cudaEvent_t>(end)) == cudaSuccess
+             ? PISA_OK
+             : PISA_ERR_CUDA;
+}
+
+const char* pisa_prefill_phase_name(int i) {
+  static const char* names[] = {"walk", "leaf"};
+  return (i >= 0 && i < kPrefillPhases) ? names[i] : "";
 }
 
 const char* pisa_status_string(int status) {

@@ -14,7 +14,7 @@
 //       leaves up log2(LPB) levels in shared memory.
 //   pyramid_top_kernel    : one CTA per (b, kv) merges the remaining levels up
 //       to the root.
-#include "common.cuh"
+#include "api.cuh"
 
 namespace pisa {
 
@@ -140,15 +140,18 @@ cudaError_t launch_build_pyramid(const __nv_bfloat16* keys, float* summ, const L
   const int threads = lpb * Hkv * 8;
   const size_t smem = (size_t)lpb * Hkv * kD * sizeof(float);
   pyramid_leaves_kernel<<<grid, threads, smem, s>>>(keys, summ, lv, N, n_cap, Hkv, lpb, merge_levels);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (merge_levels + 2 <= lv.L) {
     pyramid_top_kernel<<<B * Hkv, 256, 0, s>>>(summ, lv, N, Hkv, merge_levels + 2);
+    note_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (lengths) {
     fill_lengths_kernel<<<(B + 127) / 128, 128, 0, s>>>(lengths, B, (int)N);
+    note_launch();
     e = cudaGetLastError();
   }
   return e;

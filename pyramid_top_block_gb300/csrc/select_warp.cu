@@ -3,6 +3,7 @@
 // is fp32 on the CUDA cores with bf16 inputs, fp32 summaries and fp32
 // accumulation ("Block Sparse Attention with Log-Linear Complexity", §7.3: dot
 // products accumulated in FP32).
+#include "api.cuh"
 #include "walk.cuh"
 
 namespace pisa {
@@ -140,11 +141,16 @@ static cudaError_t launch_prefill_warp_G(const __nv_bfloat16* Q, const float* su
   const long long jobs = (long long)B * Hkv * N;
   const unsigned grid = (unsigned)((jobs + kWarps - 1) / kWarps);
   walk_kernel<G><<<grid, kWarps * 32, 0, s>>>(Q, summ, lv, N, Hq, Hkv, K, causal, jobs, surv);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  mark_phase(1, s);
   leaf_kernel<G><<<grid, kWarps * 32, 0, s>>>(Q, keys, lv, N, n_cap, Hq, Hkv, K, causal, jobs, surv,
                                               idx, scores);
-  return cudaGetLastError();
+  note_launch();
+  e = cudaGetLastError();
+  mark_phase(2, s);
+  return e;
 }
 
 cudaError_t launch_prefill_warp(const __nv_bfloat16* Q, const float* summ, const __nv_bfloat16* keys,
@@ -168,9 +174,11 @@ static cudaError_t launch_decode_G(const __nv_bfloat16* q_new, const __nv_bfloat
                                    int K, int32_t* idx, float* scores, int* status, cudaStream_t s) {
   decode_kernel<G><<<B * Hkv, 64, 0, s>>>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, Hq, Hkv,
                                           K, idx, scores, status);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   bump_lengths_kernel<<<(B + 127) / 128, 128, 0, s>>>(lengths, B, n_cap);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -87,7 +87,6 @@ WORKLOADS = {
 def make(name: str):
     """Q, K for a named prefill workload, plus its parameters."""
     w = dict(WORKLOADS[name])
-    kind = w.pop("kind")
-    fn = iid if kind == "iid" else structured
+    fn = iid if w["kind"] == "iid" else structured
     q, k = fn(w["B"], w["N"], w["Hq"], w["Hkv"], 64, seed=w["seed"])
     return q, k, w
