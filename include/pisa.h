@@ -141,6 +141,33 @@ int pisa_decode_append_and_select(const void* q_new, const void* k_new, int Hq,
                                   void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * pisa_select_prefill_noalloc -- the prefill selection above for callers that
+ * cannot allocate device memory: no workspace argument.  (The paper has no
+ * counterpart; this is a deployment convenience of this library.)
+ *
+ * For callers whose host framework owns all device memory and passes them
+ * only input and output buffers, or whose request path may not call
+ * cudaMalloc (an allocation can synchronise the device or fail mid-request).
+ * The scratch it needs is a fixed device array inside this library of
+ * PISA_NOALLOC_SCRATCH_BYTES bytes (32 MiB), held by every GPU that loads the
+ * library until the process exits.
+ *   Arguments, outputs and layouts are those of pisa_select_prefill.
+ *   Returns PISA_ERR_WORKSPACE_TOO_SMALL, launching nothing, when
+ *   pisa_select_workspace_bytes(B, N, Hq, Hkv, K) exceeds that size; call
+ *   that function to know in advance which sizes fit.
+ *   The first call on a device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture.  It allocates nothing and calls no allocating routine.
+ *   All calls share the one array: calls that overlap on the GPU (different
+ *   streams, or unordered host threads) race and give wrong results.  Each
+ *   call clears what must start at zero.  Kernel-side status cannot be read
+ *   back for this entry point (pisa_check_device_status needs a workspace).
+ */
+#define PISA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int pisa_select_prefill_noalloc(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K,
+                                int causal, int32_t* idx, float* scores, void* stream);
+
+/*
  * Synchronises `stream` and returns the status word that kernels of the last
  * select / decode call on this workspace left in `ws` (PISA_OK if none).
  */

@@ -22,7 +22,8 @@ from . import build as _build
 
 __all__ = [
     "PisaError", "Pyramid", "load", "num_levels", "pyramid_nodes", "level_offset",
-    "build_pyramid", "select_workspace_bytes", "select_prefill", "decode_workspace_bytes",
+    "build_pyramid", "select_workspace_bytes", "select_prefill", "select_prefill_noalloc",
+    "decode_workspace_bytes",
     "decode_append_and_select", "check_device_status", "status_string", "kernel_launches",
     "prefill_phases", "set_phase_events", "D", "C", "G_MERGE",
 ]
@@ -75,6 +76,8 @@ def load(path: str | None = None):
     lib.pisa_prefill_phase_count.restype = i32
     lib.pisa_prefill_phase_name.argtypes = [i32]
     lib.pisa_prefill_phase_name.restype = ctypes.c_char_p
+    lib.pisa_select_prefill_noalloc.argtypes = [vp, i32, vp, i64, i32, i32, vp, vp, vp]
+    lib.pisa_select_prefill_noalloc.restype = i32
     lib.pisa_event_elapsed_ms.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_float)]
     lib.pisa_event_elapsed_ms.restype = i32
     _lib = lib
@@ -210,6 +213,24 @@ def select_prefill(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True, N
     _check(lib.pisa_select_prefill(_ptr(Q), Hq, ctypes.byref(st), N, K, int(causal), _ptr(idx),
                                    _ptr(scores), _ptr(workspace), workspace.numel(), _stream(stream)),
            "pisa_select_prefill")
+    return idx, scores
+
+
+def select_prefill_noalloc(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True,
+                           with_scores: bool = True, out: tuple | None = None, stream=None):
+    """select_prefill without a workspace: the library's built-in 32 MiB device
+    scratch is used instead (for callers that cannot allocate device memory).
+    Calls sharing that scratch must not overlap on the GPU."""
+    B, N, Hq, _ = Q.shape
+    if out is None:
+        idx = torch.empty(B, pyr.Hkv, N, K, dtype=torch.int32, device=Q.device)
+        scores = torch.empty(B, pyr.Hkv, N, K, dtype=torch.float32, device=Q.device) if with_scores else None
+    else:
+        idx, scores = out
+    st = pyr.struct()
+    _check(load().pisa_select_prefill_noalloc(_ptr(Q), Hq, ctypes.byref(st), N, K, int(causal), _ptr(idx),
+                                              _ptr(scores), _stream(stream)),
+           "pisa_select_prefill_noalloc")
     return idx, scores
 
 
