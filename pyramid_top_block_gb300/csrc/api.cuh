@@ -17,10 +17,30 @@ cudaError_t launch_build_pyramid(const __nv_bfloat16* keys, float* summ, const L
                                  long long N, long long n_cap, int B, int Hkv, int32_t* lengths,
                                  cudaStream_t s);
 
-cudaError_t launch_prefill_warp(const __nv_bfloat16* Q, const float* summ, const __nv_bfloat16* keys,
-                                const Levels& lv, long long N, long long n_cap, int B, int Hq,
-                                int Hkv, int K, int causal, int32_t* surv, int32_t* idx,
-                                float* scores, cudaStream_t s);
+// Everything the leaf level of the prefill walk needs (buffers are caller
+// workspace slices; see pisa_api.cu for the layout).
+struct LeafTcLaunch {
+  const __nv_bfloat16* Q;
+  const __nv_bfloat16* keys;
+  int B, Hq, Hkv, K, causal;
+  long long N, n_cap;
+  int M2, nchunks, chunk_shift, nb;
+  const int32_t* surv;
+  int* count;
+  int* cursor;
+  int* bucket_off;
+  int* tile_off;
+  uint32_t* list;
+  float* leaf_scores;
+  int32_t* idx;
+  float* scores;
+  int* status;
+};
+
+cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s);
+
+cudaError_t launch_prefill_walk(const __nv_bfloat16* Q, const float* summ, const Levels& lv, long long N,
+                                int B, int Hq, int Hkv, int K, int causal, int32_t* surv, cudaStream_t s);
 
 cudaError_t launch_decode_warp(const __nv_bfloat16* q_new, const __nv_bfloat16* k_new,
                                __nv_bfloat16* keys, float* summ, int32_t* lengths,

@@ -20,6 +20,7 @@ constexpr int kLog2C = 6;
 constexpr int kMaxLevels = 32;  // N <= 2^30 tokens -> at most 25 levels
 constexpr int kMaxK = 32;
 constexpr float kScale = 0.125f;  // 1/sqrt(64), exact in fp32
+constexpr unsigned kFull = 0xffffffffu;  // all lanes of a warp
 
 // Level geometry passed by value to kernels.  Sizes M[l] are those of the
 // current sequence length; row offsets off[l] come from the capacity n_cap so

@@ -1,0 +1,554 @@
+// leaf_tc.cu -- the leaf level of the prefill walk on the 5th-generation tensor
+// cores, with queries clustered by the key block they need.
+//
+// "Block Sparse Attention with Log-Linear Complexity", "Scoring: LogSumExp"
+// (at the leaf level the score of a block is the exact log-sum-exp over its raw
+// keys), §4.1 (summed over the query heads of a GQA group) and §5.1 (the prefill
+// kernel clusters the queries that need the same key block so that each loaded
+// block is reused by all of them).
+//
+// After the intermediate levels every query holds <= K level-2 survivors p; its
+// leaf candidates are the two children 2p, 2p+1 of each, i.e. the 128 keys
+// [128p, 128p+128).  Pipeline (all on one stream):
+//   leaf_hist_kernel    count (query, survivor) pairs per bucket, a bucket being
+//                       (b, kv, query chunk, p); a chunk of 2^chunk_shift query
+//                       positions keeps the gathered query rows L2-resident
+//   leaf_scan_kernel    exclusive scans: entry offsets and tile offsets
+//   leaf_scatter_kernel write each pair (t << 5 | slot) into its bucket
+//   leaf_tc_kernel      persistent, warp-specialised: per tile of R = 128/max(G,8)
+//                       queries of one bucket, D[128 x 128] = Q_rows[128 x 64] x
+//                       K_block[128 x 64]^T on tcgen05 (bf16 in, fp32 in TMEM),
+//                       then per row two masked log-sum-exps and a sum over the
+//                       group's heads
+//   leaf_final_kernel   Top-K of the <= 2K leaf scores per query
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "api.cuh"
+#include "tc.cuh"
+
+namespace pisa {
+
+constexpr int kLeafStages = 6;    // query-row tiles in flight (16 KB each)
+constexpr int kAccBufs = 4;       // TMEM accumulators of 128 fp32 columns
+constexpr int kLeafWarps = 10;    // producer, MMA, 2 epilogue warpgroups
+constexpr int kTileBlock = 8;     // consecutive tiles handled by one CTA in a row
+constexpr int kTileBytes = 128 * 128;  // 128 rows of 64 bf16
+constexpr size_t kLeafSmem = (size_t)(kLeafStages + 2) * kTileBytes + 1024;
+
+struct LeafTcParams {
+  const uint32_t* list;
+  const int* bucket_off;
+  const int* tile_off;
+  int nb;
+  int Hkv, G, Gp, R, K;
+  long long N, n_cap;
+  int M2, nchunks;
+  int causal;
+  float* leaf_scores;
+  int* status;
+};
+
+struct Bucket {
+  int b, kv, p;
+};
+
+__device__ __forceinline__ Bucket decode_bucket(int bkt, int M2, int nchunks, int Hkv) {
+  Bucket r;
+  r.p = bkt % M2;
+  const int bkv = bkt / M2 / nchunks;
+  r.kv = bkv % Hkv;
+  r.b = bkv / Hkv;
+  return r;
+}
+
+// Largest bucket whose first tile is <= tile (tile_off is non-decreasing).
+__device__ __forceinline__ int find_bucket(const int* tile_off, int nb, int tile) {
+  int lo = 0, hi = nb - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(tile_off + mid) <= tile)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// Iterates the tiles of this CTA in order: blocks of kTileBlock consecutive
+// tiles, block j handled by CTA j % gridDim.x.  Every warp role walks the
+// same sequence, so they agree on tile k's stage, buffers and bucket.
+struct TileIter {
+  int total, blk, i, i1, bkt;
+  const int* tile_off;
+  int nb;
+  __device__ void init(const int* to, int n_b) {
+    tile_off = to;
+    nb = n_b;
+    total = __ldg(to + n_b);
+    blk = blockIdx.x;
+    start_block();
+  }
+  __device__ void start_block() {
+    i = blk * kTileBlock;
+    i1 = min(i + kTileBlock, total);
+    if (i < total) bkt = find_bucket(tile_off, nb, i);
+  }
+  __device__ bool valid() const { return i < total; }
+  __device__ void next() {
+    ++i;
+    if (i >= i1) {
+      blk += gridDim.x;
+      start_block();
+    } else {
+      while (__ldg(tile_off + bkt + 1) <= i) ++bkt;
+    }
+  }
+};
+
+__device__ __forceinline__ void leaf_abort(volatile int* abort, int* status) {
+  *abort = 1;
+  set_status(status, PISA_ERR_DEVICE_TIMEOUT);
+}
+
+// Masked log-sum-exp of one 64-key half: x holds the raw q.k dot products,
+// lim the number of leading keys that count (1..64).  Exponents are taken
+// relative to the first key's logit (exp2 of (x - x0) * log2(e)/8); if that
+// overflows, the sum is redone relative to the true maximum.
+__device__ __forceinline__ float half_lse(const float* x, int lim, bool full) {
+  constexpr float kL2e8 = 0.18033688011112042f;  // log2(e) / sqrt(64)
+  constexpr float kLn2 = 0.69314718055994531f;
+  const float ref = x[0];
+  const float nb = -ref * kL2e8;
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  if (full) {
+#pragma unroll
+    for (int c = 0; c < 64; c += 4) {
+      s0 += ex2_approx(fmaf(x[c], kL2e8, nb));
+      s1 += ex2_approx(fmaf(x[c + 1], kL2e8, nb));
+      s2 += ex2_approx(fmaf(x[c + 2], kL2e8, nb));
+      s3 += ex2_approx(fmaf(x[c + 3], kL2e8, nb));
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 64; c += 4) {
+      s0 += c < lim ? ex2_approx(fmaf(x[c], kL2e8, nb)) : 0.f;
+      s1 += c + 1 < lim ? ex2_approx(fmaf(x[c + 1], kL2e8, nb)) : 0.f;
+      s2 += c + 2 < lim ? ex2_approx(fmaf(x[c + 2], kL2e8, nb)) : 0.f;
+      s3 += c + 3 < lim ? ex2_approx(fmaf(x[c + 3], kL2e8, nb)) : 0.f;
+    }
+  }
+  float s = (s0 + s1) + (s2 + s3);
+  float r = ref;
+  if (!(s <= 3.0e38f)) {  // overflow (or NaN input): redo against the maximum
+    float m = x[0];
+#pragma unroll
+    for (int c = 1; c < 64; ++c)
+      if (c < lim) m = fmaxf(m, x[c]);
+    const float nm = -m * kL2e8;
+    s = 0.f;
+#pragma unroll
+    for (int c = 0; c < 64; ++c)
+      if (c < lim) s += ex2_approx(fmaf(x[c], kL2e8, nm));
+    r = m;
+  }
+  return r * 0.125f + lg2_approx(s) * kLn2;
+}
+
+__global__ void __launch_bounds__(kLeafWarps * 32, 1)
+    leaf_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                   LeafTcParams P) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sA = sm;
+  unsigned char* sB = sm + kLeafStages * kTileBytes;
+  __shared__ uint64_t a_full[kLeafStages], a_empty[kLeafStages], b_full[2], b_empty[2];
+  __shared__ uint64_t acc_full[kAccBufs], acc_empty[kAccBufs], mma_done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  volatile int* abort = &abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kLeafStages; ++s) {
+      mbar_init(&a_full[s], 1);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int s = 0; s < kAccBufs; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], 128);
+    }
+    mbar_init(&mma_done, 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc<kAccBufs * 128>(&tmem_base);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  const int R = P.R, Gp = P.Gp, G = P.G;
+
+  if (warp == 0) {
+    // ---------------- producer: TMA loads of key blocks and query rows
+    if (lane == 0) {
+      TileIter it;
+      it.init(P.tile_off, P.nb);
+      int k = 0, nbchg = 0, prev = -1;
+      for (; it.valid(); it.next(), ++k) {
+        const Bucket bk = decode_bucket(it.bkt, P.M2, P.nchunks, P.Hkv);
+        if (it.bkt != prev) {
+          const int bb = nbchg & 1;
+          if (nbchg >= 2 && !mbar_wait(&b_empty[bb], ((nbchg >> 1) - 1) & 1, abort)) {
+            leaf_abort(abort, P.status);
+            break;
+          }
+          mbar_expect_tx(&b_full[bb], kTileBytes);
+          tma_load_3d(sB + bb * kTileBytes, &kmap, 0, bk.kv, (int)(bk.b * P.n_cap + 128LL * bk.p), &b_full[bb]);
+          ++nbchg;
+          prev = it.bkt;
+        }
+        const int s = k % kLeafStages;
+        if (k >= kLeafStages && !mbar_wait(&a_empty[s], ((k / kLeafStages) - 1) & 1, abort)) {
+          leaf_abort(abort, P.status);
+          break;
+        }
+        const int e0 = __ldg(P.bucket_off + it.bkt) + (it.i - __ldg(P.tile_off + it.bkt)) * R;
+        const int nrows = min(R, __ldg(P.bucket_off + it.bkt + 1) - e0);
+        mbar_expect_tx(&a_full[s], (uint32_t)(nrows * G * 128));
+        for (int r = 0; r < nrows; ++r) {
+          const uint32_t ent = __ldg(P.list + e0 + r);
+          tma_load_3d(sA + s * kTileBytes + r * Gp * 128, &qmap, 0, bk.kv * G, (int)(bk.b * P.N + (ent >> 5)),
+                      &a_full[s]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: one thread drives the tensor core
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_bf16(128, 128);
+      TileIter it;
+      it.init(P.tile_off, P.nb);
+      int k = 0, nbchg = 0, prev = -1, cur = 0;
+      for (; it.valid(); it.next(), ++k) {
+        if (it.bkt != prev) {
+          if (prev >= 0) umma_commit(&b_empty[cur]);
+          cur = nbchg & 1;
+          if (!mbar_wait(&b_full[cur], (nbchg >> 1) & 1, abort)) {
+            leaf_abort(abort, P.status);
+            break;
+          }
+          ++nbchg;
+          prev = it.bkt;
+        }
+        const int s = k % kLeafStages;
+        if (!mbar_wait(&a_full[s], (k / kLeafStages) & 1, abort)) {
+          leaf_abort(abort, P.status);
+          break;
+        }
+        const int a = k % kAccBufs;
+        if (k >= kAccBufs && !mbar_wait(&acc_empty[a], ((k / kAccBufs) - 1) & 1, abort)) {
+          leaf_abort(abort, P.status);
+          break;
+        }
+        tc_fence_after();
+        const uint64_t da = umma_desc_sw128(sA + s * kTileBytes);
+        const uint64_t db = umma_desc_sw128(sB + cur * kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + a * 128, da + 2 * kk, db + 2 * kk, idesc, kk > 0);
+        umma_commit(&a_empty[s]);
+        umma_commit(&acc_full[a]);
+      }
+      // every MMA this thread issued has completed once mma_done fires
+      umma_commit(&mma_done);
+      if (!mbar_wait(&mma_done, 0, abort)) leaf_abort(abort, P.status);
+    }
+  } else {
+    // ---------------- epilogue: TMEM -> registers -> log-sum-exp -> head sum
+    const int wg = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int r = row / Gp, h = row % Gp;
+    TileIter it;
+    it.init(P.tile_off, P.nb);
+    int k = 0;
+    for (; it.valid(); it.next(), ++k) {
+      if ((k & 1) != wg) continue;
+      const int a = k % kAccBufs;
+      const bool ok = __all_sync(kFull, mbar_wait(&acc_full[a], (k / kAccBufs) & 1, abort));
+      if (!ok) {  // warp-uniform exit
+        leaf_abort(abort, P.status);
+        break;
+      }
+      tc_fence_after();
+      const Bucket bk = decode_bucket(it.bkt, P.M2, P.nchunks, P.Hkv);
+      const int e0 = __ldg(P.bucket_off + it.bkt) + (it.i - __ldg(P.tile_off + it.bkt)) * R;
+      const int nrows = min(R, __ldg(P.bucket_off + it.bkt + 1) - e0);
+      const bool qvalid = r < nrows;
+      const uint32_t ent = qvalid ? __ldg(P.list + e0 + r) : 0u;
+      const long long t = ent >> 5;
+      const int slot = ent & 31;
+      // keys of this tile that count for the query: [128p, n_eff)
+      const long long n_eff = P.causal ? (t + 1 < P.N ? t + 1 : P.N) : P.N;
+      long long lim = qvalid ? n_eff - 128LL * bk.p : 128;
+      if (lim > 128) lim = 128;
+      if (lim < 1) lim = 1;
+      const int lim0 = lim < 64 ? (int)lim : 64;
+      const int lim1 = lim > 64 ? (int)lim - 64 : 0;
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + a * 128;
+      float x[64];
+      tmem_ld32(taddr, x);
+      tmem_ld32(taddr + 32, x + 32);
+      tmem_ld_wait();
+      const bool full0 = __all_sync(kFull, lim0 == 64);
+      const float lse0 = half_lse(x, lim0, full0);
+      tmem_ld32(taddr + 64, x);
+      tmem_ld32(taddr + 96, x + 32);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&acc_empty[a]);
+      const bool any1 = __any_sync(kFull, lim1 > 0);
+      float lse1 = 0.f;
+      if (any1) {
+        const bool full1 = __all_sync(kFull, lim1 == 64);
+        lse1 = half_lse(x, lim1 > 0 ? lim1 : 1, full1);
+      }
+      const bool head = qvalid && h < G;
+      float v0 = head ? lse0 : 0.f, v1 = head ? lse1 : 0.f;
+      for (int o = Gp >> 1; o > 0; o >>= 1) {
+        v0 += __shfl_xor_sync(kFull, v0, o);
+        v1 += __shfl_xor_sync(kFull, v1, o);
+      }
+      if (qvalid && h == 0) {
+        float* out = P.leaf_scores + (((long long)bk.b * P.Hkv + bk.kv) * P.N + t) * (2 * P.K) + 2 * slot;
+        out[0] = v0;
+        out[1] = lim1 > 0 ? v1 : -INFINITY;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<kAccBufs * 128>(tmem);
+  }
+}
+
+// ------------------------------------------------------------ bucketing
+
+__device__ __forceinline__ int bucket_of(long long job, int p, long long N, int nchunks, int chunk_shift, int M2) {
+  const long long t = job % N;
+  const long long bkv = job / N;
+  return (int)((bkv * nchunks + (t >> chunk_shift)) * M2 + p);
+}
+
+__global__ void leaf_hist_kernel(const int32_t* __restrict__ surv, long long entries, int K, long long N,
+                                 int nchunks, int chunk_shift, int M2, int* __restrict__ count) {
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= entries) return;
+  const int p = surv[e];
+  if (p < 0) return;
+  atomicAdd(count + bucket_of(e / K, p, N, nchunks, chunk_shift, M2), 1);
+}
+
+__global__ void leaf_scatter_kernel(const int32_t* __restrict__ surv, long long entries, int K, long long N,
+                                    int nchunks, int chunk_shift, int M2, const int* __restrict__ bucket_off,
+                                    int* __restrict__ cursor, uint32_t* __restrict__ list) {
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= entries) return;
+  const int p = surv[e];
+  if (p < 0) return;
+  const long long job = e / K;
+  const int bkt = bucket_of(job, p, N, nchunks, chunk_shift, M2);
+  const int pos = bucket_off[bkt] + atomicAdd(cursor + bkt, 1);
+  list[pos] = ((uint32_t)(job % N) << 5) | (uint32_t)(e % K);
+}
+
+// Exclusive scans of the bucket sizes (entries) and of their tile counts
+// ceil(size / R), one CTA of 1024 threads, each owning a contiguous segment.
+__global__ void __launch_bounds__(1024) leaf_scan_kernel(const int* __restrict__ count, int nb, int R,
+                                                          int* __restrict__ bucket_off, int* __restrict__ tile_off) {
+  __shared__ int se[1024], st[1024];
+  const int tid = threadIdx.x;
+  const int per = (nb + 1023) / 1024;
+  const int lo = min(nb, tid * per), hi = min(nb, lo + per);
+  int ce = 0, ct = 0;
+  for (int i = lo; i < hi; ++i) {
+    const int c = count[i];
+    ce += c;
+    ct += (c + R - 1) / R;
+  }
+  se[tid] = ce;
+  st[tid] = ct;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {  // inclusive Hillis-Steele scan
+    const int ae = tid >= o ? se[tid - o] : 0, at = tid >= o ? st[tid - o] : 0;
+    __syncthreads();
+    se[tid] += ae;
+    st[tid] += at;
+    __syncthreads();
+  }
+  int oe = se[tid] - ce, ot = st[tid] - ct;
+  for (int i = lo; i < hi; ++i) {
+    const int c = count[i];
+    bucket_off[i] = oe;
+    tile_off[i] = ot;
+    oe += c;
+    ot += (c + R - 1) / R;
+  }
+  if (tid == 1023) {
+    bucket_off[nb] = se[1023];
+    tile_off[nb] = st[1023];
+  }
+}
+
+// Final Top-K per (b, kv, t) over the leaf candidates (children of the level-2
+// survivors, ascending); ineligible children carry -inf and are skipped.
+__global__ void leaf_final_kernel(const int32_t* __restrict__ surv, const float* __restrict__ leaf_scores,
+                                  long long jobs, int K, int32_t* __restrict__ idx, float* __restrict__ scores) {
+  const long long job = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (job >= jobs) return;
+  const int32_t* s2 = surv + job * K;
+  const float* ls = leaf_scores + job * 2 * K;
+  int cid[2 * kMaxK];
+  float csc[2 * kMaxK];
+  int nC = 0;
+  for (int j = 0; j < K; ++j) {
+    const int p = s2[j];
+    if (p < 0) break;
+    cid[nC] = 2 * p;
+    csc[nC++] = ls[2 * j];
+    const float s1 = ls[2 * j + 1];
+    if (s1 != -INFINITY) {
+      cid[nC] = 2 * p + 1;
+      csc[nC++] = s1;
+    }
+  }
+  int32_t* io = idx + job * K;
+  float* so = scores ? scores + job * K : nullptr;
+  int w = 0;
+  for (int i = 0; i < nC; ++i) {
+    bool keep = true;
+    if (nC > K) {
+      int rank = 0;
+      for (int j = 0; j < nC; ++j) rank += (csc[j] > csc[i]) || (csc[j] == csc[i] && j < i);
+      keep = rank < K;
+    }
+    if (keep) {
+      io[w] = cid[i];
+      if (so) so[w] = csc[i];
+      ++w;
+    }
+  }
+  for (; w < K; ++w) {
+    io[w] = -1;
+    if (so) so[w] = -INFINITY;
+  }
+}
+
+// ------------------------------------------------------------ host side
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 map over [rows][heads][64] with a box of {64, box_h, box_rows}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, long long rows, int heads, int box_h, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {128, (cuuint64_t)heads * 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_h, (cuuint32_t)box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int n[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (!n[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 148;
+  }
+  return n[dev];
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
+  const long long entries = (long long)L.B * L.Hkv * L.N * L.K;
+  const int G = L.Hq / L.Hkv;
+  const int Gp = G < 8 ? 8 : G;
+  const int R = 128 / Gp;
+  const unsigned eg = (unsigned)((entries + 255) / 256);
+  leaf_hist_kernel<<<eg, 256, 0, s>>>(L.surv, entries, L.K, L.N, L.nchunks, L.chunk_shift, L.M2, L.count);
+  note_launch();
+  leaf_scan_kernel<<<1, 1024, 0, s>>>(L.count, L.nb, R, L.bucket_off, L.tile_off);
+  note_launch();
+  leaf_scatter_kernel<<<eg, 256, 0, s>>>(L.surv, entries, L.K, L.N, L.nchunks, L.chunk_shift, L.M2, L.bucket_off,
+                                         L.cursor, L.list);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mark_phase(2, s);
+
+  CUtensorMap qmap, kmap;
+  if (!make_map(&qmap, L.Q, (long long)L.B * L.N, L.Hq, G, 1) ||
+      !make_map(&kmap, L.keys, (long long)L.B * L.n_cap, L.Hkv, 1, 128))
+    return cudaErrorInvalidValue;
+  static std::once_flag attr_once;
+  std::call_once(attr_once, [] {
+    cudaFuncSetAttribute(leaf_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLeafSmem);
+  });
+  LeafTcParams P;
+  P.list = L.list;
+  P.bucket_off = L.bucket_off;
+  P.tile_off = L.tile_off;
+  P.nb = L.nb;
+  P.Hkv = L.Hkv;
+  P.G = G;
+  P.Gp = Gp;
+  P.R = R;
+  P.K = L.K;
+  P.N = L.N;
+  P.n_cap = L.n_cap;
+  P.M2 = L.M2;
+  P.nchunks = L.nchunks;
+  P.causal = L.causal;
+  P.leaf_scores = L.leaf_scores;
+  P.status = L.status;
+  leaf_tc_kernel<<<sm_count(), kLeafWarps * 32, kLeafSmem, s>>>(qmap, kmap, P);
+  note_launch();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mark_phase(3, s);
+  const long long jobs = (long long)L.B * L.Hkv * L.N;
+  leaf_final_kernel<<<(unsigned)((jobs + 127) / 128), 128, 0, s>>>(L.surv, L.leaf_scores, jobs, L.K, L.idx,
+                                                                   L.scores);
+  note_launch();
+  e = cudaGetLastError();
+  mark_phase(4, s);
+  return e;
+}
+
+}  // namespace pisa

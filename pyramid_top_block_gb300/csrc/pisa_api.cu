@@ -24,7 +24,7 @@ void mark_phase(int i, cudaStream_t s) {
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kPrefillPhases = 2;
+constexpr int kPrefillPhases = 4;
 constexpr size_t kStatusBytes = 256;  // status word + reserved counters
 
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
@@ -55,7 +55,8 @@ int check_geometry(int B, long long N, int Hq, int Hkv, int d, int C, int g, int
   if (Hq % Hkv) return PISA_ERR_UNSUPPORTED;
   if (d != kD || C != kC || g != 2) return PISA_ERR_UNSUPPORTED;
   if (K > kMaxK || !pow2_group(Hq / Hkv) || Hkv > 32) return PISA_ERR_UNSUPPORTED;
-  if (N > (1LL << 30)) return PISA_ERR_UNSUPPORTED;
+  if (N > (1LL << 27)) return PISA_ERR_UNSUPPORTED;
+  if ((long long)B * Hkv * N * K >= (1LL << 31) || (long long)B * N >= (1LL << 31)) return PISA_ERR_UNSUPPORTED;
   return PISA_OK;
 }
 
@@ -68,18 +69,54 @@ int check_pyr(const pisa_pyramid* p) {
   return PISA_OK;
 }
 
-// Workspace of the prefill selection: [status 256 B][surv2: B*Hkv*N*K int32].
+// Query positions per bucketing chunk: the leaf level gathers query rows of
+// one chunk at a time, so 2^shift tokens x Hq x 128 B of Q stay in L2.  The
+// chunk grows with N so that there are at most 64 chunks.
+int chunk_shift_for(long long N) {
+  int cs = 14;
+  while ((N >> cs) > 64) ++cs;
+  return cs;
+}
+
+// Workspace of the prefill selection (every slice 256-byte aligned):
+//   [status 256 B][count nb][cursor nb]       zeroed at every call
+//   [bucket_off nb+1][tile_off nb+1]           scans of the bucket sizes
+//   [surv2: B*Hkv*N*K int32]                   level-2 survivors
+//   [list: B*Hkv*N*K uint32]                   (t << 5 | slot), bucket-sorted
+//   [leaf_scores: B*Hkv*N*2K fp32]
+// with nb = B * Hkv * nchunks * M2 buckets (chunk of queries, level-2 node).
 struct PrefillWs {
-  size_t status, surv, total;
+  size_t status, count, cursor, bucket_off, tile_off, surv, list, leaf, total, zero_bytes;
+  long long nb;
+  int nchunks, chunk_shift, M2;
 };
 
 PrefillWs prefill_layout(int B, long long N, int Hkv, int K) {
   PrefillWs w;
+  w.chunk_shift = chunk_shift_for(N);
+  w.nchunks = (int)((N + (1LL << w.chunk_shift) - 1) >> w.chunk_shift);
+  w.M2 = (int)level_size_for(N, 2);
+  w.nb = (long long)B * Hkv * w.nchunks * w.M2;
+  const size_t entries = (size_t)B * Hkv * (size_t)N * K;
   size_t o = 0;
   w.status = o;
   o += align_up(kStatusBytes);
+  w.count = o;
+  o += sizeof(int) * (size_t)w.nb;
+  w.cursor = o;
+  o += sizeof(int) * (size_t)w.nb;
+  w.zero_bytes = o;
+  o = align_up(o);
+  w.bucket_off = o;
+  o += align_up(sizeof(int) * (size_t)(w.nb + 1));
+  w.tile_off = o;
+  o += align_up(sizeof(int) * (size_t)(w.nb + 1));
   w.surv = o;
-  o += align_up(sizeof(int32_t) * (size_t)B * Hkv * (size_t)N * K);
+  o += align_up(sizeof(int32_t) * entries);
+  w.list = o;
+  o += align_up(sizeof(uint32_t) * entries);
+  w.leaf = o;
+  o += align_up(sizeof(float) * 2 * entries);
   w.total = o;
   return w;
 }
@@ -111,7 +148,7 @@ int pisa_build_pyramid(const pisa_pyramid* pyr, int64_t N, void* stream) {
   int st = check_pyr(pyr);
   if (st) return st;
   if (N < 1 || N > pyr->n_cap) return PISA_ERR_INVALID_ARG;
-  if (N > (1LL << 30) || pyr->n_cap > (1LL << 30)) return PISA_ERR_UNSUPPORTED;
+  if (N > (1LL << 27) || pyr->n_cap > (1LL << 27)) return PISA_ERR_UNSUPPORTED;
   const Levels lv = make_levels(N, pyr->n_cap);
   return cuda_status(launch_build_pyramid(static_cast<const __nv_bfloat16*>(pyr->keys), pyr->summaries, lv,
                                           N, pyr->n_cap, pyr->B, pyr->Hkv, pyr->lengths,
@@ -134,17 +171,44 @@ int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t 
   if ((reinterpret_cast<uintptr_t>(Q) & 15) || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)))
     return PISA_ERR_INVALID_ARG;
   const PrefillWs w = prefill_layout(pyr->B, N, pyr->Hkv, K);
+  if (w.nb >= (1LL << 31) || (long long)pyr->B * pyr->n_cap >= (1LL << 31)) return PISA_ERR_UNSUPPORTED;
   if (ws_bytes < w.total) return PISA_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* base = static_cast<char*>(ws);
-  cudaError_t e = cudaMemsetAsync(base + w.status, 0, kStatusBytes, s);
+  cudaError_t e = cudaMemsetAsync(base, 0, w.zero_bytes, s);
   if (e != cudaSuccess) return PISA_ERR_CUDA;
   const Levels lv = make_levels(N, pyr->n_cap);
+  int32_t* surv = reinterpret_cast<int32_t*>(base + w.surv);
   mark_phase(0, s);
-  e = launch_prefill_warp(static_cast<const __nv_bfloat16*>(Q), pyr->summaries,
-                          static_cast<const __nv_bfloat16*>(pyr->keys), lv, N, pyr->n_cap, pyr->B, Hq,
-                          pyr->Hkv, K, causal, reinterpret_cast<int32_t*>(base + w.surv), idx, scores, s);
-  return cuda_status(e);
+  e = launch_prefill_walk(static_cast<const __nv_bfloat16*>(Q), pyr->summaries, lv, N, pyr->B, Hq, pyr->Hkv, K,
+                          causal, surv, s);
+  if (e != cudaSuccess) return PISA_ERR_CUDA;
+  mark_phase(1, s);
+  LeafTcLaunch L;
+  L.Q = static_cast<const __nv_bfloat16*>(Q);
+  L.keys = static_cast<const __nv_bfloat16*>(pyr->keys);
+  L.B = pyr->B;
+  L.Hq = Hq;
+  L.Hkv = pyr->Hkv;
+  L.K = K;
+  L.causal = causal;
+  L.N = N;
+  L.n_cap = pyr->n_cap;
+  L.M2 = w.M2;
+  L.nchunks = w.nchunks;
+  L.chunk_shift = w.chunk_shift;
+  L.nb = (int)w.nb;
+  L.surv = surv;
+  L.count = reinterpret_cast<int*>(base + w.count);
+  L.cursor = reinterpret_cast<int*>(base + w.cursor);
+  L.bucket_off = reinterpret_cast<int*>(base + w.bucket_off);
+  L.tile_off = reinterpret_cast<int*>(base + w.tile_off);
+  L.list = reinterpret_cast<uint32_t*>(base + w.list);
+  L.leaf_scores = reinterpret_cast<float*>(base + w.leaf);
+  L.idx = idx;
+  L.scores = scores;
+  L.status = reinterpret_cast<int*>(base + w.status);
+  return cuda_status(launch_prefill_leaf_tc(L, s));
 }
 
 size_t pisa_decode_workspace_bytes(int B, int Hq, int Hkv, int K) {
@@ -200,7 +264,7 @@ int pisa_event_elapsed_ms(void* start, void* end, float* ms) {
 }
 
 const char* pisa_prefill_phase_name(int i) {
-  static const char* names[] = {"walk", "leaf"};
+  static const char* names[] = {"walk", "bucket", "leaf", "final"};
   return (i >= 0 && i < kPrefillPhases) ? names[i] : "";
 }
 

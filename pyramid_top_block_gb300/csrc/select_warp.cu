@@ -1,5 +1,5 @@
-// select_warp.cu -- warp-per-query selection kernels (prefill walk, prefill
-// leaf level, decode step).  Each (b, kv, t) walk is one warp; the arithmetic
+// select_warp.cu -- warp-per-query selection kernels (prefill walk over the
+// intermediate levels, decode step).  Each (b, kv, t) walk is one warp; the arithmetic
 // is fp32 on the CUDA cores with bf16 inputs, fp32 summaries and fp32
 // accumulation ("Block Sparse Attention with Log-Linear Complexity", §7.3: dot
 // products accumulated in FP32).
@@ -31,31 +31,6 @@ __global__ void __launch_bounds__(kWarps * 32) walk_kernel(
   const int nS = warp_walk_intermediate<G>(blk, lv, qs, t, K, causal != 0, scratch[warp], lane, &myS);
   int32_t* out = surv + job * K;
   if (lane < K) out[lane] = lane < nS ? myS : -1;
-}
-
-template <int G>
-__global__ void __launch_bounds__(kWarps * 32) leaf_kernel(
-    const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ keys, Levels lv,
-    long long N, long long n_cap, int Hq, int Hkv, int K, int causal, long long jobs,
-    const int32_t* __restrict__ surv, int32_t* __restrict__ idx, float* __restrict__ scores) {
-  __shared__ __align__(16) float qs_all[kWarps][G * kD];
-  __shared__ WarpScratch scratch[kWarps];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long job = (long long)blockIdx.x * kWarps + warp;
-  if (job >= jobs) return;
-  const long long t = job % N;
-  const int kv = (int)((job / N) % Hkv);
-  const long long b = job / (N * Hkv);
-  float* qs = qs_all[warp];
-  const __nv_bfloat16* qrow = Q + ((b * N + t) * Hq + (long long)kv * G) * kD;
-  for (int i = lane; i < G * kD; i += 32) qs[i] = bf2f(qrow[i]);
-  __syncwarp();
-  const int32_t* s2 = surv + job * K;
-  const int v = lane < K ? s2[lane] : -1;
-  const int nS = __popc(__ballot_sync(kFull, v >= 0));
-  const int myS = v >= 0 ? v : 0;
-  warp_leaf_select<G>(keys + b * n_cap * Hkv * kD, Hkv, kv, lv, qs, t, N, K, causal != 0, nS, myS,
-                      scratch[warp], lane, idx + job * K, scores ? scores + job * K : nullptr);
 }
 
 // One decode step for one (b, kv): append k_new at position n = lengths[b],
@@ -134,35 +109,23 @@ __global__ void bump_lengths_kernel(int32_t* lengths, int B, long long n_cap) {
 // ---------------------------------------------------------------- launchers
 
 template <int G>
-static cudaError_t launch_prefill_warp_G(const __nv_bfloat16* Q, const float* summ,
-                                         const __nv_bfloat16* keys, const Levels& lv, long long N,
-                                         long long n_cap, int B, int Hq, int Hkv, int K, int causal,
-                                         int32_t* surv, int32_t* idx, float* scores, cudaStream_t s) {
+static cudaError_t launch_prefill_walk_G(const __nv_bfloat16* Q, const float* summ, const Levels& lv, long long N,
+                                         int B, int Hq, int Hkv, int K, int causal, int32_t* surv, cudaStream_t s) {
   const long long jobs = (long long)B * Hkv * N;
   const unsigned grid = (unsigned)((jobs + kWarps - 1) / kWarps);
   walk_kernel<G><<<grid, kWarps * 32, 0, s>>>(Q, summ, lv, N, Hq, Hkv, K, causal, jobs, surv);
   note_launch();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  mark_phase(1, s);
-  leaf_kernel<G><<<grid, kWarps * 32, 0, s>>>(Q, keys, lv, N, n_cap, Hq, Hkv, K, causal, jobs, surv,
-                                              idx, scores);
-  note_launch();
-  e = cudaGetLastError();
-  mark_phase(2, s);
-  return e;
+  return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_warp(const __nv_bfloat16* Q, const float* summ, const __nv_bfloat16* keys,
-                                const Levels& lv, long long N, long long n_cap, int B, int Hq,
-                                int Hkv, int K, int causal, int32_t* surv, int32_t* idx,
-                                float* scores, cudaStream_t s) {
+cudaError_t launch_prefill_walk(const __nv_bfloat16* Q, const float* summ, const Levels& lv, long long N,
+                                int B, int Hq, int Hkv, int K, int causal, int32_t* surv, cudaStream_t s) {
   switch (Hq / Hkv) {
-    case 1: return launch_prefill_warp_G<1>(Q, summ, keys, lv, N, n_cap, B, Hq, Hkv, K, causal, surv, idx, scores, s);
-    case 2: return launch_prefill_warp_G<2>(Q, summ, keys, lv, N, n_cap, B, Hq, Hkv, K, causal, surv, idx, scores, s);
-    case 4: return launch_prefill_warp_G<4>(Q, summ, keys, lv, N, n_cap, B, Hq, Hkv, K, causal, surv, idx, scores, s);
-    case 8: return launch_prefill_warp_G<8>(Q, summ, keys, lv, N, n_cap, B, Hq, Hkv, K, causal, surv, idx, scores, s);
-    case 16: return launch_prefill_warp_G<16>(Q, summ, keys, lv, N, n_cap, B, Hq, Hkv, K, causal, surv, idx, scores, s);
+    case 1: return launch_prefill_walk_G<1>(Q, summ, lv, N, B, Hq, Hkv, K, causal, surv, s);
+    case 2: return launch_prefill_walk_G<2>(Q, summ, lv, N, B, Hq, Hkv, K, causal, surv, s);
+    case 4: return launch_prefill_walk_G<4>(Q, summ, lv, N, B, Hq, Hkv, K, causal, surv, s);
+    case 8: return launch_prefill_walk_G<8>(Q, summ, lv, N, B, Hq, Hkv, K, causal, surv, s);
+    case 16: return launch_prefill_walk_G<16>(Q, summ, lv, N, B, Hq, Hkv, K, causal, surv, s);
     default: return cudaErrorInvalidValue;
   }
 }

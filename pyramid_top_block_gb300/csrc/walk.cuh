@@ -19,8 +19,6 @@
 
 namespace pisa {
 
-constexpr unsigned kFull = 0xffffffffu;
-
 struct WarpScratch {
   int cand[2 * kMaxK];
   float score[2 * kMaxK];
