@@ -39,8 +39,21 @@ struct LeafTcLaunch {
 
 cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s);
 
-cudaError_t launch_prefill_walk(const __nv_bfloat16* Q, const float* summ, const Levels& lv, long long N,
-                                int B, int Hq, int Hkv, int K, int causal, int32_t* surv, cudaStream_t s);
+// The intermediate levels of the prefill walk (walk_mma.cu).
+struct WalkLaunch {
+  const __nv_bfloat16* Q;
+  const float* summ;
+  const Levels* lv;
+  long long N;
+  int B, Hq, Hkv, K, causal;
+  unsigned char* table;  // route table: B*Hkv*route_rows_per_bh(lv) rows of 256 bytes
+  int32_t* surv;
+  int* count;
+  int nchunks, chunk_shift, M2;
+};
+
+long long route_rows_per_bh(const Levels& lv);
+cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s);
 
 cudaError_t launch_decode_warp(const __nv_bfloat16* q_new, const __nv_bfloat16* k_new,
                                __nv_bfloat16* keys, float* summ, int32_t* lengths,

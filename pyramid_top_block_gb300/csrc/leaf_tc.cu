@@ -10,7 +10,7 @@
 // After the intermediate levels every query holds <= K level-2 survivors p; its
 // leaf candidates are the two children 2p, 2p+1 of each, i.e. the 128 keys
 // [128p, 128p+128).  Pipeline (all on one stream):
-//   leaf_hist_kernel    count (query, survivor) pairs per bucket, a bucket being
+//   (the walk kernel)   counts (query, survivor) pairs per bucket, a bucket being
 //                       (b, kv, query chunk, p); a chunk of 2^chunk_shift query
 //                       positions keeps the gathered query rows L2-resident
 //   leaf_scan_kernel    exclusive scans: entry offsets and tile offsets
@@ -345,15 +345,6 @@ __device__ __forceinline__ int bucket_of(long long job, int p, long long N, int 
   return (int)((bkv * nchunks + (t >> chunk_shift)) * M2 + p);
 }
 
-__global__ void leaf_hist_kernel(const int32_t* __restrict__ surv, long long entries, int K, long long N,
-                                 int nchunks, int chunk_shift, int M2, int* __restrict__ count) {
-  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= entries) return;
-  const int p = surv[e];
-  if (p < 0) return;
-  atomicAdd(count + bucket_of(e / K, p, N, nchunks, chunk_shift, M2), 1);
-}
-
 __global__ void leaf_scatter_kernel(const int32_t* __restrict__ surv, long long entries, int K, long long N,
                                     int nchunks, int chunk_shift, int M2, const int* __restrict__ bucket_off,
                                     int* __restrict__ cursor, uint32_t* __restrict__ list) {
@@ -501,8 +492,7 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
   const int Gp = G < 8 ? 8 : G;
   const int R = 128 / Gp;
   const unsigned eg = (unsigned)((entries + 255) / 256);
-  leaf_hist_kernel<<<eg, 256, 0, s>>>(L.surv, entries, L.K, L.N, L.nchunks, L.chunk_shift, L.M2, L.count);
-  note_launch();
+  // bucket sizes were counted by the walk kernel as it wrote the survivors
   leaf_scan_kernel<<<1, 1024, 0, s>>>(L.count, L.nb, R, L.bucket_off, L.tile_off);
   note_launch();
   leaf_scatter_kernel<<<eg, 256, 0, s>>>(L.surv, entries, L.K, L.N, L.nchunks, L.chunk_shift, L.M2, L.bucket_off,
@@ -510,7 +500,7 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mark_phase(2, s);
+  mark_phase(3, s);
 
   CUtensorMap qmap, kmap;
   if (!make_map(&qmap, L.Q, (long long)L.B * L.N, L.Hq, G, 1) ||
@@ -541,13 +531,13 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
   note_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mark_phase(3, s);
+  mark_phase(4, s);
   const long long jobs = (long long)L.B * L.Hkv * L.N;
   leaf_final_kernel<<<(unsigned)((jobs + 127) / 128), 128, 0, s>>>(L.surv, L.leaf_scores, jobs, L.K, L.idx,
                                                                    L.scores);
   note_launch();
   e = cudaGetLastError();
-  mark_phase(4, s);
+  mark_phase(5, s);
   return e;
 }
 

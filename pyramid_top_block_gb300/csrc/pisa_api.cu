@@ -24,7 +24,7 @@ void mark_phase(int i, cudaStream_t s) {
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kPrefillPhases = 4;
+constexpr int kPrefillPhases = 5;
 constexpr size_t kStatusBytes = 256;  // status word + reserved counters
 
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
@@ -84,9 +84,10 @@ int chunk_shift_for(long long N) {
 //   [surv2: B*Hkv*N*K int32]                   level-2 survivors
 //   [list: B*Hkv*N*K uint32]                   (t << 5 | slot), bucket-sorted
 //   [leaf_scores: B*Hkv*N*2K fp32]
+//   [route table: B*Hkv*rows x 256 B]          per-node logit-step rows of the walk
 // with nb = B * Hkv * nchunks * M2 buckets (chunk of queries, level-2 node).
 struct PrefillWs {
-  size_t status, count, cursor, bucket_off, tile_off, surv, list, leaf, total, zero_bytes;
+  size_t status, count, cursor, bucket_off, tile_off, surv, list, leaf, table, total, zero_bytes;
   long long nb;
   int nchunks, chunk_shift, M2;
 };
@@ -117,6 +118,8 @@ PrefillWs prefill_layout(int B, long long N, int Hkv, int K) {
   o += align_up(sizeof(uint32_t) * entries);
   w.leaf = o;
   o += align_up(sizeof(float) * 2 * entries);
+  w.table = o;
+  o += align_up((size_t)B * Hkv * (size_t)route_rows_per_bh(make_levels(N, N)) * 256);
   w.total = o;
   return w;
 }
@@ -180,10 +183,25 @@ int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t 
   const Levels lv = make_levels(N, pyr->n_cap);
   int32_t* surv = reinterpret_cast<int32_t*>(base + w.surv);
   mark_phase(0, s);
-  e = launch_prefill_walk(static_cast<const __nv_bfloat16*>(Q), pyr->summaries, lv, N, pyr->B, Hq, pyr->Hkv, K,
-                          causal, surv, s);
+  WalkLaunch W;
+  W.Q = static_cast<const __nv_bfloat16*>(Q);
+  W.summ = pyr->summaries;
+  W.lv = &lv;
+  W.N = N;
+  W.B = pyr->B;
+  W.Hq = Hq;
+  W.Hkv = pyr->Hkv;
+  W.K = K;
+  W.causal = causal;
+  W.table = reinterpret_cast<unsigned char*>(base + w.table);
+  W.surv = surv;
+  W.count = reinterpret_cast<int*>(base + w.count);
+  W.nchunks = w.nchunks;
+  W.chunk_shift = w.chunk_shift;
+  W.M2 = w.M2;
+  e = launch_prefill_walk_mma(W, s);
   if (e != cudaSuccess) return PISA_ERR_CUDA;
-  mark_phase(1, s);
+  mark_phase(2, s);
   LeafTcLaunch L;
   L.Q = static_cast<const __nv_bfloat16*>(Q);
   L.keys = static_cast<const __nv_bfloat16*>(pyr->keys);
@@ -264,7 +282,7 @@ int pisa_event_elapsed_ms(void* start, void* end, float* ms) {
 }
 
 const char* pisa_prefill_phase_name(int i) {
-  static const char* names[] = {"walk", "bucket", "leaf", "final"};
+  static const char* names[] = {"route_table", "walk", "bucket", "leaf", "final"};
   return (i >= 0 && i < kPrefillPhases) ? names[i] : "";
 }
 

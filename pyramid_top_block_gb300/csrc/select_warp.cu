@@ -1,5 +1,5 @@
-// select_warp.cu -- warp-per-query selection kernels (prefill walk over the
-// intermediate levels, decode step).  Each (b, kv, t) walk is one warp; the arithmetic
+// select_warp.cu -- the decode step: one warp walks the cached pyramid for the
+// newest query of a sequence.  Each (b, kv, t) walk is one warp; the arithmetic
 // is fp32 on the CUDA cores with bf16 inputs, fp32 summaries and fp32
 // accumulation ("Block Sparse Attention with Log-Linear Complexity", §7.3: dot
 // products accumulated in FP32).
@@ -7,31 +7,6 @@
 #include "walk.cuh"
 
 namespace pisa {
-
-constexpr int kWarps = 8;
-
-template <int G>
-__global__ void __launch_bounds__(kWarps * 32) walk_kernel(
-    const __nv_bfloat16* __restrict__ Q, const float* __restrict__ summ, Levels lv, long long N,
-    int Hq, int Hkv, int K, int causal, long long jobs, int32_t* __restrict__ surv) {
-  __shared__ __align__(16) float qs_all[kWarps][G * kD];
-  __shared__ WarpScratch scratch[kWarps];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long job = (long long)blockIdx.x * kWarps + warp;
-  if (job >= jobs) return;
-  const long long t = job % N;
-  const int kv = (int)((job / N) % Hkv);
-  const long long b = job / (N * Hkv);
-  float* qs = qs_all[warp];
-  const __nv_bfloat16* qrow = Q + ((b * N + t) * Hq + (long long)kv * G) * kD;
-  for (int i = lane; i < G * kD; i += 32) qs[i] = bf2f(qrow[i]);
-  __syncwarp();
-  const float* blk = summ + (b * Hkv + kv) * lv.total * kD;
-  int myS;
-  const int nS = warp_walk_intermediate<G>(blk, lv, qs, t, K, causal != 0, scratch[warp], lane, &myS);
-  int32_t* out = surv + job * K;
-  if (lane < K) out[lane] = lane < nS ? myS : -1;
-}
 
 // One decode step for one (b, kv): append k_new at position n = lengths[b],
 // refresh the leaf mean and its ancestor path (the decoding design keeps the
@@ -107,28 +82,6 @@ __global__ void bump_lengths_kernel(int32_t* lengths, int B, long long n_cap) {
 }
 
 // ---------------------------------------------------------------- launchers
-
-template <int G>
-static cudaError_t launch_prefill_walk_G(const __nv_bfloat16* Q, const float* summ, const Levels& lv, long long N,
-                                         int B, int Hq, int Hkv, int K, int causal, int32_t* surv, cudaStream_t s) {
-  const long long jobs = (long long)B * Hkv * N;
-  const unsigned grid = (unsigned)((jobs + kWarps - 1) / kWarps);
-  walk_kernel<G><<<grid, kWarps * 32, 0, s>>>(Q, summ, lv, N, Hq, Hkv, K, causal, jobs, surv);
-  note_launch();
-  return cudaGetLastError();
-}
-
-cudaError_t launch_prefill_walk(const __nv_bfloat16* Q, const float* summ, const Levels& lv, long long N,
-                                int B, int Hq, int Hkv, int K, int causal, int32_t* surv, cudaStream_t s) {
-  switch (Hq / Hkv) {
-    case 1: return launch_prefill_walk_G<1>(Q, summ, lv, N, B, Hq, Hkv, K, causal, surv, s);
-    case 2: return launch_prefill_walk_G<2>(Q, summ, lv, N, B, Hq, Hkv, K, causal, surv, s);
-    case 4: return launch_prefill_walk_G<4>(Q, summ, lv, N, B, Hq, Hkv, K, causal, surv, s);
-    case 8: return launch_prefill_walk_G<8>(Q, summ, lv, N, B, Hq, Hkv, K, causal, surv, s);
-    case 16: return launch_prefill_walk_G<16>(Q, summ, lv, N, B, Hq, Hkv, K, causal, surv, s);
-    default: return cudaErrorInvalidValue;
-  }
-}
 
 template <int G>
 static cudaError_t launch_decode_G(const __nv_bfloat16* q_new, const __nv_bfloat16* k_new,

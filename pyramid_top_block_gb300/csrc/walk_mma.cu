@@ -1,0 +1,368 @@
+// walk_mma.cu -- the intermediate levels of the prefill walk on tensor cores.
+//
+// "Block Sparse Attention with Log-Linear Complexity", §3.2 (coarse-to-fine:
+// each level expands the previous survivors, keeps the Top-K of at most g*K
+// candidates, keeps a level of <= K candidates unscored), "Scoring: LogSumExp"
+// (a candidate's score is log sum exp of q.kbar over its children's summaries),
+// §4.1 (summed over the query heads of the GQA group).
+//
+// Carrying the logits down the tree.  For a query head h and a node v let
+// z_v = q_h . kbar_v / sqrt(d).  A node's mean is the count-weighted mean of its
+// children's, n_v kbar_v = n_a kbar_a + n_b kbar_b, so with
+//     Delta_v = kbar_r - kbar_v          (r = the child with fewer tokens, a if equal)
+//     u_v     = q_h . Delta_v / sqrt(d)
+// the children's logits follow from the parent's:  z_r = z_v + u_v and
+// z_o = z_v - (n_r / n_o) u_v for the other child o (n_r / n_o <= 1, so the
+// error of u is never amplified).  The walk therefore needs ONE dot product per
+// candidate (with its Delta row) to get both of its children's logits, and the
+// rounding errors add up linearly along the root-to-leaf path.  The root's own
+// logit is one direct dot product with its summary.
+//
+// Precision.  Delta rows (and the root summary) are stored as a pair of bf16
+// vectors hi + lo (hi = bf16(x), lo = bf16(x - hi)), which represents the fp32
+// value to ~2^-17 relative; q is bf16 and exact.  Each dot product is two
+// bf16 mma.sync.m16n8k16 chains (hi and lo) accumulated in fp32: M = 16 query
+// heads of the group, N = 8 candidates, K = 64 features in 4 steps.
+//
+// Layout of a stored row (256 bytes): hi[64] then lo[64], each with its 32
+// bf16 pairs permuted so that lane quad position j reads its four k-steps' B
+// fragments as two 16-byte loads at byte offset 32 j.
+#include <mutex>
+
+#include "api.cuh"
+#include "tc.cuh"
+
+namespace pisa {
+
+constexpr int kWalkWarps = 8;
+
+struct RowOffsets {
+  long long o[kMaxLevels + 2];
+};
+constexpr int kRowBytes = 256;
+constexpr int kCZ = 20;  // padded stride (floats) of a candidate's 16 head logits
+constexpr int kKZ = 44;  // padded stride of a candidate's children logits (2 x 16 + pad)
+
+// Storage position (in bf16 elements, 0..63) of feature d inside a permuted half-row.
+__host__ __device__ __forceinline__ int perm_pos(int d) {
+  const int P = d >> 1, ks = P >> 3, rem = P & 7, j = rem & 3, half = rem >> 2;
+  return 2 * (8 * j + 2 * ks + half) + (d & 1);
+}
+
+// Which child a node's Delta row refers to: 1 when the second child exists and
+// holds fewer tokens (the ragged tail), else 0.
+__device__ __forceinline__ int ref_child(int l, long long v, long long Mc, long long N, int* n0, int* n1) {
+  *n0 = node_count(l - 1, 2 * v, N);
+  *n1 = (2 * v + 1 < Mc) ? node_count(l - 1, 2 * v + 1, N) : 0;
+  return (*n1 > 0 && *n1 < *n0) ? 1 : 0;
+}
+
+// Route table of one (b, kv): rows for levels 2..L (Delta rows, levels in
+// ascending order, nodes ascending) followed by the root summary row.
+// Thread per (b, kv, row, feature pair).
+__global__ void route_table_kernel(const float* __restrict__ summ, Levels lv, long long N, int BH,
+                                   long long rows_per_bh, RowOffsets ro, unsigned char* __restrict__ table) {
+  const long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long total = (long long)BH * rows_per_bh * 32;
+  if (w >= total) return;
+  const int pr = (int)(w & 31);
+  const long long row = (w >> 5) % rows_per_bh;
+  const long long bh = (w >> 5) / rows_per_bh;
+  const float* blk = summ + bh * lv.total * kD;
+  float x[2];
+  if (row == rows_per_bh - 1) {  // root summary
+    const float* r = blk + lv.off[lv.L] * kD;
+    x[0] = r[2 * pr];
+    x[1] = r[2 * pr + 1];
+  } else {
+    int l = 2;
+    while (l < lv.L && row >= ro.o[l + 1]) ++l;
+    const long long v = row - ro.o[l];
+    int n0, n1;
+    const int ref = ref_child(l, v, lv.M[l - 1], N, &n0, &n1);
+    const float* pv = blk + (lv.off[l] + v) * kD;
+    const float* pc = blk + (lv.off[l - 1] + 2 * v + ref) * kD;
+    for (int e = 0; e < 2; ++e) x[e] = pc[2 * pr + e] - pv[2 * pr + e];
+  }
+  __nv_bfloat16* hi = reinterpret_cast<__nv_bfloat16*>(table + (bh * rows_per_bh + row) * kRowBytes);
+  __nv_bfloat16* lo = hi + 64;
+  for (int e = 0; e < 2; ++e) {
+    const int d = 2 * pr + e;
+    const __nv_bfloat16 h = __float2bfloat16_rn(x[e]);
+    hi[perm_pos(d)] = h;
+    lo[perm_pos(d)] = __float2bfloat16_rn(x[e] - __bfloat162float(h));
+  }
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// d[4] = (raw) dot products of the 16 heads with the row at `row` (hi + lo):
+// thread (g, j) gets heads g, g+8 x candidates 2j, 2j+1 of the n-tile whose
+// B rows the lanes loaded (row == nullptr -> zero column).
+__device__ __forceinline__ void tile_dot(const uint32_t (*A)[4], const unsigned char* row, int j, float* d) {
+  uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0, l0 = h0, l1 = h0;
+  if (row) {
+    const uint4* p = reinterpret_cast<const uint4*>(row + 32 * j);
+    h0 = __ldg(p);
+    h1 = __ldg(p + 1);
+    l0 = __ldg(p + 8);
+    l1 = __ldg(p + 9);
+  }
+  d[0] = d[1] = d[2] = d[3] = 0.f;
+  mma_bf16_16816(d, A[0], h0.x, h0.y);
+  mma_bf16_16816(d, A[1], h0.z, h0.w);
+  mma_bf16_16816(d, A[2], h1.x, h1.y);
+  mma_bf16_16816(d, A[3], h1.z, h1.w);
+  mma_bf16_16816(d, A[0], l0.x, l0.y);
+  mma_bf16_16816(d, A[1], l0.z, l0.w);
+  mma_bf16_16816(d, A[2], l1.x, l1.y);
+  mma_bf16_16816(d, A[3], l1.z, l1.w);
+}
+
+struct WalkSmem {  // per-warp views into dynamic shared memory
+  int* cand;     // [2K] node ids of the current candidates (ascending)
+  int* src;      // [2K] (candidate index << 1 | child) each next candidate comes from
+  float* cz;     // [2K][kCZ] logits of the candidates, per head
+  float* kz;     // [2K][kKZ] logits of the candidates' two children, per head
+  float* score;  // [2K]
+  int* sel;      // [K] candidate indices of the survivors (ascending)
+};
+
+__host__ __device__ inline size_t walk_smem_per_warp(int K) {
+  const size_t c2 = 2 * (size_t)K;
+  return c2 * sizeof(int) * 2 + c2 * kCZ * 4 + c2 * kKZ * 4 + c2 * 4 + (size_t)K * 4;
+}
+
+__global__ void __launch_bounds__(kWalkWarps * 32) walk_mma_kernel(
+    const __nv_bfloat16* __restrict__ Q, const unsigned char* __restrict__ table, Levels lv,
+    RowOffsets ro, long long rows_per_bh, long long N, int Hq, int Hkv, int K,
+    int causal, long long jobs, int32_t* __restrict__ surv, int* __restrict__ count, int nchunks,
+    int chunk_shift, int M2) {
+  extern __shared__ __align__(16) unsigned char wsm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, j = lane & 3;
+  const int G = Hq / Hkv;
+  const int C2 = 2 * K;
+  unsigned char* base = wsm + (size_t)warp * walk_smem_per_warp(K);
+  WalkSmem S;
+  S.cand = reinterpret_cast<int*>(base);
+  S.src = S.cand + C2;
+  S.cz = reinterpret_cast<float*>(S.src + C2);
+  S.kz = S.cz + C2 * kCZ;
+  S.score = S.kz + C2 * kKZ;
+  S.sel = reinterpret_cast<int*>(S.score + C2);
+  constexpr float kL2e = 1.4426950408889634f;
+  constexpr float kLn2 = 0.69314718055994531f;
+
+  for (long long job = (long long)blockIdx.x * kWalkWarps + warp; job < jobs;
+       job += (long long)gridDim.x * kWalkWarps) {
+    const long long t = job % N;
+    const long long bh = job / N;
+    const int kv = (int)(bh % Hkv);
+    const long long b = bh / Hkv;
+    // A fragments: the G heads of this query's group (rows >= G are zero)
+    uint32_t A[4][4];
+    {
+      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + ((b * N + t) * Hq + (long long)kv * G) * kD);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const int w0 = 8 * ks + j;
+        A[ks][0] = g < G ? __ldg(q0 + g * 32 + w0) : 0u;
+        A[ks][1] = g + 8 < G ? __ldg(q0 + (g + 8) * 32 + w0) : 0u;
+        A[ks][2] = g < G ? __ldg(q0 + g * 32 + w0 + 4) : 0u;
+        A[ks][3] = g + 8 < G ? __ldg(q0 + (g + 8) * 32 + w0 + 4) : 0u;
+      }
+    }
+    const unsigned char* tb = table + bh * rows_per_bh * kRowBytes;
+    int nS;        // survivors of the last processed level
+    if (lv.L == 1) {
+      nS = 1;
+      if (lane == 0) S.sel[0] = 0;
+      if (lane == 0) S.cand[0] = 0;
+    } else {
+      // root logit: direct dot with the root summary row (candidate column 0)
+      float d[4];
+      tile_dot(A, g == 0 ? tb + (rows_per_bh - 1) * kRowBytes : nullptr, j, d);
+      if (j == 0) {
+        S.cz[g] = d[0] * kScale;
+        S.cz[g + 8] = d[2] * kScale;
+      }
+      if (lane == 0) S.cand[0] = 0;
+      int nC = 1;
+      __syncwarp();
+      for (int l = lv.L; l >= 2; --l) {
+        const bool scoring = nC > K;
+        const long long Mc = lv.M[l - 1];
+        const unsigned char* lrow = tb + ro.o[l] * kRowBytes;
+        for (int nt = 0; nt * 8 < nC; ++nt) {
+          const int cb = nt * 8 + g;
+          float d[4];
+          tile_dot(A, cb < nC ? lrow + (long long)S.cand[cb] * kRowBytes : nullptr, j, d);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int ci = nt * 8 + 2 * j + cc;
+            float msum = 0.f, prod = 1.f;
+            if (ci < nC) {
+              const long long c = S.cand[ci];
+              int n0, n1;
+              const int ref = ref_child(l, c, Mc, N, &n0, &n1);
+              const bool elig1 = n1 > 0 && (!causal || node_start(l - 1, 2 * c + 1) <= t);
+              const float ratio = n1 > 0 ? (ref ? (float)n1 / (float)n0 : (float)n0 / (float)n1) : 0.f;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int h = g + 8 * hh;
+                const float u = d[cc + 2 * hh] * kScale;
+                const float z = S.cz[ci * kCZ + h];
+                const float zr = z + u, zo = fmaf(-ratio, u, z);
+                const float z0 = ref ? zo : zr, z1 = ref ? zr : zo;
+                S.kz[ci * kKZ + h] = z0;
+                S.kz[ci * kKZ + 20 + h] = z1;
+                if (scoring && h < G) {
+                  if (elig1) {
+                    const float mx = fmaxf(z0, z1), mn = fminf(z0, z1);
+                    msum += mx;
+                    prod *= 1.f + ex2_approx((mn - mx) * kL2e);
+                  } else {
+                    msum += z0;
+                  }
+                }
+              }
+            }
+            if (scoring) {
+#pragma unroll
+              for (int o = 4; o < 32; o <<= 1) {
+                msum += __shfl_xor_sync(kFull, msum, o);
+                prod *= __shfl_xor_sync(kFull, prod, o);
+              }
+              if (g == 0 && ci < nC) S.score[ci] = msum + lg2_approx(prod) * kLn2;
+            }
+          }
+        }
+        __syncwarp();
+        // survivors (candidate indices, ascending)
+        if (!scoring) {
+          nS = nC;
+          if (lane < nC) S.sel[lane] = lane;
+        } else {
+          bool keep[2];
+          unsigned m[2];
+#pragma unroll
+          for (int s2 = 0; s2 < 2; ++s2) {
+            const int ci = lane + 32 * s2;
+            keep[s2] = false;
+            if (ci < nC) {
+              const float sc = S.score[ci];
+              int rank = 0;
+              for (int q = 0; q < nC; ++q) {
+                const float o = S.score[q];
+                rank += (o > sc) || (o == sc && q < ci);
+              }
+              keep[s2] = rank < K;
+            }
+            m[s2] = __ballot_sync(kFull, keep[s2]);
+          }
+          const unsigned lt = (1u << lane) - 1u;
+          if (keep[0]) S.sel[__popc(m[0] & lt)] = lane;
+          if (keep[1]) S.sel[__popc(m[0]) + __popc(m[1] & lt)] = lane + 32;
+          nS = K;
+        }
+        __syncwarp();
+        if (l == 2) break;
+        // next candidates: eligible children of the survivors, with their logits
+        const long long Mn = lv.M[l - 1];
+        int ci_s = 0;
+        long long c = 0;
+        bool v1 = false;
+        if (lane < nS) {
+          ci_s = S.sel[lane];
+          c = S.cand[ci_s];
+          v1 = 2 * c + 1 < Mn && (!causal || node_start(l - 1, 2 * c + 1) <= t);
+        }
+        const unsigned b1 = __ballot_sync(kFull, v1);
+        const int pos = lane + __popc(b1 & ((1u << lane) - 1u));
+        const int nN = nS + __popc(b1);
+        __syncwarp();
+        if (lane < nS) {
+          S.cand[pos] = (int)(2 * c);
+          S.src[pos] = ci_s << 1;
+          if (v1) {
+            S.cand[pos + 1] = (int)(2 * c + 1);
+            S.src[pos + 1] = (ci_s << 1) | 1;
+          }
+        }
+        __syncwarp();
+        for (int e = lane; e < nN * 16; e += 32) {
+          const int ci = e >> 4, h = e & 15;
+          const int sr = S.src[ci];
+          S.cz[ci * kCZ + h] = S.kz[(sr >> 1) * kKZ + 20 * (sr & 1) + h];
+        }
+        nC = nN;
+        __syncwarp();
+      }
+    }
+    // level-2 survivors (node ids, ascending) -> workspace, and bucket counts
+    int32_t* out = surv + job * K;
+    if (lane < K) {
+      int p = -1;
+      if (lane < nS) p = S.cand[S.sel[lane]];
+      out[lane] = p;
+      if (p >= 0) atomicAdd(count + ((bh * nchunks + (t >> chunk_shift)) * M2 + p), 1);
+    }
+    __syncwarp();
+  }
+}
+
+// Host side: table size and launches.
+long long route_rows_per_bh(const Levels& lv) {
+  long long r = 1;  // root summary row
+  for (int l = 2; l <= lv.L; ++l) r += lv.M[l];
+  return r;
+}
+
+cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
+  const Levels& lv = *W.lv;
+  const long long rows = route_rows_per_bh(lv);
+  const int BH = W.B * W.Hkv;
+  RowOffsets ro;  // row offset of each level inside a (b, kv) table (levels 2..L ascending)
+  long long o = 0;
+  for (int l = 0; l < kMaxLevels + 2; ++l) ro.o[l] = 0;
+  for (int l = 2; l <= lv.L; ++l) {
+    ro.o[l] = o;
+    o += lv.M[l];
+  }
+  ro.o[lv.L + 1] = o;
+  const long long thr = (long long)BH * rows * 32;
+  route_table_kernel<<<(unsigned)((thr + 255) / 256), 256, 0, s>>>(W.summ, lv, W.N, BH, rows, ro, W.table);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mark_phase(1, s);
+  const size_t smem = walk_smem_per_warp(W.K) * kWalkWarps;
+  {  // per-warp scratch grows with K (K = 32: 17 KB per warp)
+    static std::mutex mu;
+    static size_t attr = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (smem > attr) {
+      e = cudaFuncSetAttribute(walk_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      attr = smem;
+    }
+  }
+  const long long jobs = (long long)BH * W.N;
+  long long blocks = (jobs + kWalkWarps - 1) / kWalkWarps;
+  const long long cap = 152LL * 32;
+  if (blocks > cap) blocks = cap;
+  walk_mma_kernel<<<(unsigned)blocks, kWalkWarps * 32, smem, s>>>(W.Q, W.table, lv, ro, rows, W.N, W.Hq, W.Hkv, W.K,
+                                                                   W.causal, jobs, W.surv, W.count, W.nchunks,
+                                                                   W.chunk_shift, W.M2);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace pisa
