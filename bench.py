@@ -268,6 +268,7 @@ def run_ours(args):
         ev_e[i].record(stream)
     torch.cuda.synchronize()
     launches = pisa.kernel_launches() - launches0
+    device_status = pisa.check_device_status(ws)
     pisa.set_phase_events(None)
     if dist:
         dist.barrier()
@@ -348,6 +349,7 @@ def run_ours(args):
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg(w, args),
                 "roofline": roof, "roofline_pass": pass_roof, "phases_ms": phase_ms,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+                "device_status": device_status,
                 "decode": decode}
         print(json.dumps(line), flush=True)
     if dist:

@@ -30,6 +30,8 @@ struct LeafTcLaunch {
   int* cursor;
   int* bucket_off;
   int* tile_off;
+  int* tile_bkt;        // [max_tiles] bucket of each tile
+  long long max_tiles;  // upper bound on the number of tiles
   uint32_t* list;
   float* leaf_scores;
   int32_t* idx;

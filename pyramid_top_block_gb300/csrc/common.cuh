@@ -10,7 +10,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/pisa.h"
+#include "pisa.h"
 
 namespace pisa {
 

@@ -32,17 +32,20 @@ namespace pisa {
 
 constexpr int kLeafStages = 6;    // query-row tiles in flight (16 KB each)
 constexpr int kAccBufs = 4;       // TMEM accumulators of 128 fp32 columns
-constexpr int kLeafWarps = 10;    // producer, MMA, 2 epilogue warpgroups
-constexpr int kTileBlock = 8;     // consecutive tiles handled by one CTA in a row
+constexpr int kLeafWarps = 12;    // metadata, MMA, 2 epilogue warpgroups, 2 query-row warps
+constexpr int kTileBlock = 32;    // consecutive tiles handled by one CTA in a row
+constexpr int kInfo = 16;         // tile descriptors in flight (producer -> MMA / epilogue)
 constexpr int kTileBytes = 128 * 128;  // 128 rows of 64 bf16
 constexpr size_t kLeafSmem = (size_t)(kLeafStages + 2) * kTileBytes + 1024;
 
 struct LeafTcParams {
+  const __nv_bfloat16* Q;
   const uint32_t* list;
   const int* bucket_off;
   const int* tile_off;
+  const int* tile_bkt;
   int nb;
-  int Hkv, G, Gp, R, K;
+  int Hq, Hkv, G, Gp, R, K;
   long long N, n_cap;
   int M2, nchunks;
   int causal;
@@ -52,6 +55,12 @@ struct LeafTcParams {
 
 struct Bucket {
   int b, kv, p;
+};
+
+// What the producer tells the MMA and epilogue warps about tile k.
+struct TileInfo {
+  int bkt, nrows;
+  uint32_t ent[16];  // (t << 5 | slot) of each query row of the tile
 };
 
 __device__ __forceinline__ Bucket decode_bucket(int bkt, int M2, int nchunks, int Hkv) {
@@ -75,37 +84,6 @@ __device__ __forceinline__ int find_bucket(const int* tile_off, int nb, int tile
   }
   return lo;
 }
-
-// Iterates the tiles of this CTA in order: blocks of kTileBlock consecutive
-// tiles, block j handled by CTA j % gridDim.x.  Every warp role walks the
-// same sequence, so they agree on tile k's stage, buffers and bucket.
-struct TileIter {
-  int total, blk, i, i1, bkt;
-  const int* tile_off;
-  int nb;
-  __device__ void init(const int* to, int n_b) {
-    tile_off = to;
-    nb = n_b;
-    total = __ldg(to + n_b);
-    blk = blockIdx.x;
-    start_block();
-  }
-  __device__ void start_block() {
-    i = blk * kTileBlock;
-    i1 = min(i + kTileBlock, total);
-    if (i < total) bkt = find_bucket(tile_off, nb, i);
-  }
-  __device__ bool valid() const { return i < total; }
-  __device__ void next() {
-    ++i;
-    if (i >= i1) {
-      blk += gridDim.x;
-      start_block();
-    } else {
-      while (__ldg(tile_off + bkt + 1) <= i) ++bkt;
-    }
-  }
-};
 
 __device__ __forceinline__ void leaf_abort(volatile int* abort, int* status) {
   *abort = 1;
@@ -164,7 +142,8 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
   unsigned char* sA = sm;
   unsigned char* sB = sm + kLeafStages * kTileBytes;
   __shared__ uint64_t a_full[kLeafStages], a_empty[kLeafStages], b_full[2], b_empty[2];
-  __shared__ uint64_t acc_full[kAccBufs], acc_empty[kAccBufs], mma_done;
+  __shared__ uint64_t acc_full[kAccBufs], acc_empty[kAccBufs], info_full[kInfo], info_empty[kInfo], mma_done;
+  __shared__ TileInfo info[kInfo];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   volatile int* abort = &abort_flag;
@@ -183,6 +162,10 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
       mbar_init(&acc_full[s], 1);
       mbar_init(&acc_empty[s], 128);
     }
+    for (int s = 0; s < kInfo; ++s) {
+      mbar_init(&info_full[s], 1);
+      mbar_init(&info_empty[s], 128 + 32);  // the epilogue warpgroup + the query-row warp
+    }
     mbar_init(&mma_done, 1);
     abort_flag = 0;
     mbar_fence_init();
@@ -192,50 +175,109 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   const int R = P.R, Gp = P.Gp, G = P.G;
+  const int total = __ldg(P.tile_off + P.nb);
+  // this CTA's tiles: blocks of kTileBlock consecutive tiles, block j on CTA j % gridDim.x
+  int my_tiles = 0;
+  for (int blk = blockIdx.x; blk * kTileBlock < total; blk += gridDim.x) my_tiles += min(kTileBlock, total - blk * kTileBlock);
 
   if (warp == 0) {
-    // ---------------- producer: TMA loads of key blocks and query rows
-    if (lane == 0) {
-      TileIter it;
-      it.init(P.tile_off, P.nb);
-      int k = 0, nbchg = 0, prev = -1;
-      for (; it.valid(); it.next(), ++k) {
-        const Bucket bk = decode_bucket(it.bkt, P.M2, P.nchunks, P.Hkv);
-        if (it.bkt != prev) {
-          const int bb = nbchg & 1;
-          if (nbchg >= 2 && !mbar_wait(&b_empty[bb], ((nbchg >> 1) - 1) & 1, abort)) {
-            leaf_abort(abort, P.status);
-            break;
+    // ---------------- metadata warp: resolves tiles (lane-parallel, one block of kTileBlock
+    // tiles at a time), waits for a free stage, loads key blocks by TMA, arms a_full with
+    // the tile's byte count and publishes the tile descriptor (info ring).
+    int k = 0, nbchg = 0, prev = -1;
+    bool ok = true;
+    for (int blk = blockIdx.x; ok && blk * kTileBlock < total; blk += gridDim.x) {
+      const int i0 = blk * kTileBlock;
+      const int n = min(kTileBlock, total - i0);
+      int mb = 0, me0 = 0, mn = 0;
+      if (lane < n) {
+        mb = __ldg(P.tile_bkt + i0 + lane);
+        const int to = __ldg(P.tile_off + mb);
+        me0 = __ldg(P.bucket_off + mb) + (i0 + lane - to) * R;
+        mn = min(R, __ldg(P.bucket_off + mb + 1) - me0);
+      }
+      uint32_t ents[kTileBlock];  // lane r holds entry r of every tile of the block
+#pragma unroll
+      for (int m = 0; m < kTileBlock; ++m) {
+        const int e0 = __shfl_sync(kFull, me0, m), nr = __shfl_sync(kFull, mn, m);
+        ents[m] = (m < n && lane < nr) ? __ldg(P.list + e0 + lane) : 0u;
+      }
+#pragma unroll 1
+      for (int m = 0; m < n && ok; ++m, ++k) {
+        const int bkt = __shfl_sync(kFull, mb, m), nrows = __shfl_sync(kFull, mn, m);
+        const int slot = k % kInfo, s = k % kLeafStages;
+        bool w = true;
+        if (lane == 0) {
+          if (k >= kInfo) w = mbar_wait(&info_empty[slot], ((k / kInfo) - 1) & 1, abort);
+          if (w && bkt != prev) {
+            const Bucket bk = decode_bucket(bkt, P.M2, P.nchunks, P.Hkv);
+            const int bb = nbchg & 1;
+            if (nbchg >= 2) w = mbar_wait(&b_empty[bb], ((nbchg >> 1) - 1) & 1, abort);
+            if (w) {
+              mbar_expect_tx(&b_full[bb], kTileBytes);
+              tma_load_3d(sB + bb * kTileBytes, &kmap, 0, bk.kv, (int)(bk.b * P.n_cap + 128LL * bk.p), &b_full[bb]);
+            }
           }
-          mbar_expect_tx(&b_full[bb], kTileBytes);
-          tma_load_3d(sB + bb * kTileBytes, &kmap, 0, bk.kv, (int)(bk.b * P.n_cap + 128LL * bk.p), &b_full[bb]);
-          ++nbchg;
-          prev = it.bkt;
+          if (w && k >= kLeafStages) w = mbar_wait(&a_empty[s], ((k / kLeafStages) - 1) & 1, abort);
+          if (w) mbar_expect_tx(&a_full[s], (uint32_t)(nrows * G * 128));
         }
-        const int s = k % kLeafStages;
-        if (k >= kLeafStages && !mbar_wait(&a_empty[s], ((k / kLeafStages) - 1) & 1, abort)) {
-          leaf_abort(abort, P.status);
+        ok = __shfl_sync(kFull, w, 0);
+        if (!ok) {
+          if (lane == 0) leaf_abort(abort, P.status);
           break;
         }
-        const int e0 = __ldg(P.bucket_off + it.bkt) + (it.i - __ldg(P.tile_off + it.bkt)) * R;
-        const int nrows = min(R, __ldg(P.bucket_off + it.bkt + 1) - e0);
-        mbar_expect_tx(&a_full[s], (uint32_t)(nrows * G * 128));
-        for (int r = 0; r < nrows; ++r) {
-          const uint32_t ent = __ldg(P.list + e0 + r);
-          tma_load_3d(sA + s * kTileBytes + r * Gp * 128, &qmap, 0, bk.kv * G, (int)(bk.b * P.N + (ent >> 5)),
-                      &a_full[s]);
+        if (bkt != prev) {
+          ++nbchg;
+          prev = bkt;
         }
+        uint32_t e = 0;
+#pragma unroll
+        for (int mm = 0; mm < kTileBlock; ++mm)
+          if (mm == m) e = ents[mm];
+        if (lane < nrows) info[slot].ent[lane] = e;
+        if (lane == 0) {
+          info[slot].bkt = bkt;
+          info[slot].nrows = nrows;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&info_full[slot]);
       }
+      __syncwarp();
+    }
+  } else if (warp >= kLeafWarps - 2) {
+    // ---------------- query-row warps: tile k's rows are loaded by warp (k & 1), one
+    // TMA box {64 features, G heads, 1 token} per query, completing on a_full
+    const int tw = warp - (kLeafWarps - 2);
+    for (int k = tw; k < my_tiles; k += 2) {
+      const int slot = k % kInfo, s = k % kLeafStages;
+      const bool ok = __all_sync(kFull, mbar_wait(&info_full[slot], (k / kInfo) & 1, abort));
+      if (!ok) {
+        if (lane == 0) leaf_abort(abort, P.status);
+        break;
+      }
+      const Bucket bk = decode_bucket(info[slot].bkt, P.M2, P.nchunks, P.Hkv);
+      const int nrows = info[slot].nrows;
+      if (lane < nrows) {
+        const uint32_t ent = info[slot].ent[lane];
+        tma_load_3d(sA + s * kTileBytes + lane * Gp * 128, &qmap, 0, bk.kv * G, (int)(bk.b * P.N + (ent >> 5)),
+                    &a_full[s]);
+      }
+      __syncwarp();
+      mbar_arrive(&info_empty[slot]);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: one thread drives the tensor core
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_bf16(128, 128);
-      TileIter it;
-      it.init(P.tile_off, P.nb);
-      int k = 0, nbchg = 0, prev = -1, cur = 0;
-      for (; it.valid(); it.next(), ++k) {
-        if (it.bkt != prev) {
+      int nbchg = 0, prev = -1, cur = 0;
+      for (int k = 0; k < my_tiles; ++k) {
+        const int slot = k % kInfo, s = k % kLeafStages, a = k % kAccBufs;
+        if (!mbar_wait(&info_full[slot], (k / kInfo) & 1, abort)) {
+          leaf_abort(abort, P.status);
+          break;
+        }
+        const int bkt = info[slot].bkt;
+        if (bkt != prev) {
           if (prev >= 0) umma_commit(&b_empty[cur]);
           cur = nbchg & 1;
           if (!mbar_wait(&b_full[cur], (nbchg >> 1) & 1, abort)) {
@@ -243,14 +285,12 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
             break;
           }
           ++nbchg;
-          prev = it.bkt;
+          prev = bkt;
         }
-        const int s = k % kLeafStages;
         if (!mbar_wait(&a_full[s], (k / kLeafStages) & 1, abort)) {
           leaf_abort(abort, P.status);
           break;
         }
-        const int a = k % kAccBufs;
         if (k >= kAccBufs && !mbar_wait(&acc_empty[a], ((k / kAccBufs) - 1) & 1, abort)) {
           leaf_abort(abort, P.status);
           break;
@@ -268,30 +308,27 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
       if (!mbar_wait(&mma_done, 0, abort)) leaf_abort(abort, P.status);
     }
   } else {
-    // ---------------- epilogue: TMEM -> registers -> log-sum-exp -> head sum
+    // ---------------- epilogue (warps 2..9): TMEM -> registers -> log-sum-exp -> head sum
     const int wg = (warp - 2) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const int r = row / Gp, h = row % Gp;
-    TileIter it;
-    it.init(P.tile_off, P.nb);
-    int k = 0;
-    for (; it.valid(); it.next(), ++k) {
-      if ((k & 1) != wg) continue;
-      const int a = k % kAccBufs;
-      const bool ok = __all_sync(kFull, mbar_wait(&acc_full[a], (k / kAccBufs) & 1, abort));
+    for (int k = wg; k < my_tiles; k += 2) {
+      const int a = k % kAccBufs, slot = k % kInfo;
+      const bool ok = __all_sync(kFull, mbar_wait(&acc_full[a], (k / kAccBufs) & 1, abort) &&
+                                            mbar_wait(&info_full[slot], (k / kInfo) & 1, abort));
       if (!ok) {  // warp-uniform exit
         leaf_abort(abort, P.status);
         break;
       }
       tc_fence_after();
-      const Bucket bk = decode_bucket(it.bkt, P.M2, P.nchunks, P.Hkv);
-      const int e0 = __ldg(P.bucket_off + it.bkt) + (it.i - __ldg(P.tile_off + it.bkt)) * R;
-      const int nrows = min(R, __ldg(P.bucket_off + it.bkt + 1) - e0);
+      const Bucket bk = decode_bucket(info[slot].bkt, P.M2, P.nchunks, P.Hkv);
+      const int nrows = info[slot].nrows;
       const bool qvalid = r < nrows;
-      const uint32_t ent = qvalid ? __ldg(P.list + e0 + r) : 0u;
+      const uint32_t ent = qvalid ? info[slot].ent[r] : 0u;
+      mbar_arrive(&info_empty[slot]);
       const long long t = ent >> 5;
-      const int slot = ent & 31;
+      const int qslot = ent & 31;
       // keys of this tile that count for the query: [128p, n_eff)
       const long long n_eff = P.causal ? (t + 1 < P.N ? t + 1 : P.N) : P.N;
       long long lim = qvalid ? n_eff - 128LL * bk.p : 128;
@@ -324,7 +361,7 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
         v1 += __shfl_xor_sync(kFull, v1, o);
       }
       if (qvalid && h == 0) {
-        float* out = P.leaf_scores + (((long long)bk.b * P.Hkv + bk.kv) * P.N + t) * (2 * P.K) + 2 * slot;
+        float* out = P.leaf_scores + (((long long)bk.b * P.Hkv + bk.kv) * P.N + t) * (2 * P.K) + 2 * qslot;
         out[0] = v0;
         out[1] = lim1 > 0 ? v1 : -INFINITY;
       }
@@ -394,6 +431,14 @@ __global__ void __launch_bounds__(1024) leaf_scan_kernel(const int* __restrict__
     bucket_off[nb] = se[1023];
     tile_off[nb] = st[1023];
   }
+}
+
+// tile_bkt[i] = bucket of tile i (the largest bucket whose first tile is <= i).
+__global__ void leaf_tile_map_kernel(const int* __restrict__ tile_off, int nb, long long max_tiles,
+                                     int* __restrict__ tile_bkt) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= max_tiles || i >= tile_off[nb]) return;
+  tile_bkt[i] = find_bucket(tile_off, nb, (int)i);
 }
 
 // Final Top-K per (b, kv, t) over the leaf candidates (children of the level-2
@@ -498,6 +543,9 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
   leaf_scatter_kernel<<<eg, 256, 0, s>>>(L.surv, entries, L.K, L.N, L.nchunks, L.chunk_shift, L.M2, L.bucket_off,
                                          L.cursor, L.list);
   note_launch();
+  leaf_tile_map_kernel<<<(unsigned)((L.max_tiles + 255) / 256), 256, 0, s>>>(L.tile_off, L.nb, L.max_tiles,
+                                                                              L.tile_bkt);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   mark_phase(3, s);
@@ -511,9 +559,12 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
     cudaFuncSetAttribute(leaf_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLeafSmem);
   });
   LeafTcParams P;
+  P.Q = L.Q;
+  P.Hq = L.Hq;
   P.list = L.list;
   P.bucket_off = L.bucket_off;
   P.tile_off = L.tile_off;
+  P.tile_bkt = L.tile_bkt;
   P.nb = L.nb;
   P.Hkv = L.Hkv;
   P.G = G;

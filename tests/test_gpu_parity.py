@@ -21,8 +21,10 @@ def _f32(x: torch.Tensor) -> np.ndarray:
 def _run_prefill(q, k, K, causal=True):
     qd, kd = q.to(DEV), k.to(DEV)
     pyr = pisa.build_pyramid(kd)
-    idx, sc = pisa.select_prefill(qd, pyr, K, causal=causal)
-    torch.cuda.synchronize()
+    B, N, Hq, _ = q.shape
+    ws = torch.empty(pisa.select_workspace_bytes(B, N, Hq, k.shape[2], K), dtype=torch.uint8, device=DEV)
+    idx, sc = pisa.select_prefill(qd, pyr, K, causal=causal, workspace=ws)
+    assert pisa.check_device_status(ws) == 0, "a kernel reported a device-side error"
     return pyr, idx.cpu().numpy(), sc.cpu().numpy()
 
 
