@@ -8,21 +8,29 @@
 //
 // Carrying the logits down the tree.  For a query head h and a node v let
 // z_v = q_h . kbar_v / sqrt(d).  A node's mean is the count-weighted mean of its
-// children's, n_v kbar_v = n_a kbar_a + n_b kbar_b, so with
-//     Delta_v = kbar_r - kbar_v          (r = the child with fewer tokens, a if equal)
+// children's, n_v kbar_v = n_a kbar_a + n_b kbar_b.  With
+//     Delta_v = kbar_ref - kbar_v     (ref = the child with fewer tokens, a if equal)
 //     u_v     = q_h . Delta_v / sqrt(d)
-// the children's logits follow from the parent's:  z_r = z_v + u_v and
-// z_o = z_v - (n_r / n_o) u_v for the other child o (n_r / n_o <= 1, so the
-// error of u is never amplified).  The walk therefore needs ONE dot product per
-// candidate (with its Delta row) to get both of its children's logits, and the
-// rounding errors add up linearly along the root-to-leaf path.  The root's own
-// logit is one direct dot product with its summary.
+// the children's logits are z_ref = z_v + u_v and z_oth = z_v - r u_v with
+// r = n_ref / n_oth <= 1 (r = 1 for every node but the last of a level).  So
+// the LSE over the two children is
+//     log(e^{z_v + u} + e^{z_v - r u}) = z_v + max(u, -r u) + log(1 + e^{-(1+r)|u|}),
+// i.e. z_v + log(2 cosh u) for equal children.  Summed over the heads of the
+// group, a candidate's score is Z_v + sum_h [max(u_h, -r u_h) + log(1 + e^{-(1+r)|u_h|})]
+// with Z_v = sum_h z_{v,h}, and its children's head sums are Z_v + sum_h u_h and
+// Z_v - r sum_h u_h.  The walk therefore carries ONE scalar per candidate and
+// needs one 16-head dot product per candidate (with its Delta row) per level;
+// rounding errors add up linearly down the path.  A child that starts after
+// the query (causal) leaves the single-child score Z_child.
 //
-// Precision.  Delta rows (and the root summary) are stored as a pair of bf16
-// vectors hi + lo (hi = bf16(x), lo = bf16(x - hi)), which represents the fp32
-// value to ~2^-17 relative; q is bf16 and exact.  Each dot product is two
-// bf16 mma.sync.m16n8k16 chains (hi and lo) accumulated in fp32: M = 16 query
-// heads of the group, N = 8 candidates, K = 64 features in 4 steps.
+// The walk starts at the highest level with more than K nodes (all levels
+// above it are kept whole, without scoring): its eligible nodes are the first
+// candidates, and their Z = (sum_h q_h) . kbar / sqrt(d) is one fp32 dot product.
+//
+// Precision.  Delta rows are stored as a pair of bf16 vectors hi + lo
+// (hi = bf16(x), lo = bf16(x - hi)), ~2^-17 relative; q is bf16 and exact.
+// Each dot product is two bf16 mma.sync.m16n8k16 chains (hi and lo)
+// accumulated in fp32: M = 16 query heads, N = 8 candidates, K = 64 features.
 //
 // Layout of a stored row (256 bytes): hi[64] then lo[64], each with its 32
 // bf16 pairs permuted so that lane quad position j reads its four k-steps' B
@@ -40,8 +48,6 @@ struct RowOffsets {
   long long o[kMaxLevels + 2];
 };
 constexpr int kRowBytes = 256;
-constexpr int kCZ = 20;  // padded stride (floats) of a candidate's 16 head logits
-constexpr int kKZ = 44;  // padded stride of a candidate's children logits (2 x 16 + pad)
 
 // Storage position (in bf16 elements, 0..63) of feature d inside a permuted half-row.
 __host__ __device__ __forceinline__ int perm_pos(int d) {
@@ -57,8 +63,8 @@ __device__ __forceinline__ int ref_child(int l, long long v, long long Mc, long 
   return (*n1 > 0 && *n1 < *n0) ? 1 : 0;
 }
 
-// Route table of one (b, kv): rows for levels 2..L (Delta rows, levels in
-// ascending order, nodes ascending) followed by the root summary row.
+// Route table of one (b, kv): Delta rows of the nodes of levels 2..L (levels
+// ascending, nodes ascending).
 // Thread per (b, kv, row, feature pair).
 __global__ void route_table_kernel(const float* __restrict__ summ, Levels lv, long long N, int BH,
                                    long long rows_per_bh, RowOffsets ro, unsigned char* __restrict__ table) {
@@ -69,12 +75,8 @@ __global__ void route_table_kernel(const float* __restrict__ summ, Levels lv, lo
   const long long row = (w >> 5) % rows_per_bh;
   const long long bh = (w >> 5) / rows_per_bh;
   const float* blk = summ + bh * lv.total * kD;
-  float x[2];
-  if (row == rows_per_bh - 1) {  // root summary
-    const float* r = blk + lv.off[lv.L] * kD;
-    x[0] = r[2 * pr];
-    x[1] = r[2 * pr + 1];
-  } else {
+  float x[2] = {0.f, 0.f};
+  if (lv.L >= 2 && row < ro.o[lv.L + 1]) {  // (the table's spare last row stays zero)
     int l = 2;
     while (l < lv.L && row >= ro.o[l + 1]) ++l;
     const long long v = row - ro.o[l];
@@ -127,23 +129,50 @@ __device__ __forceinline__ void tile_dot(const uint32_t (*A)[4], const unsigned 
 
 struct WalkSmem {  // per-warp views into dynamic shared memory
   int* cand;     // [2K] node ids of the current candidates (ascending)
-  int* src;      // [2K] (candidate index << 1 | child) each next candidate comes from
-  float* cz;     // [2K][kCZ] logits of the candidates, per head
-  float* kz;     // [2K][kKZ] logits of the candidates' two children, per head
+  float* zs;     // [2K] head-summed logit Z of each candidate
+  float* su;     // [2K] head-summed u of each candidate (for its children's Z)
   float* score;  // [2K]
   int* sel;      // [K] candidate indices of the survivors (ascending)
+  float* qsum;   // [64] sum over the group's heads of q (fp32)
 };
 
+// [qsum 64 floats][cand 2K][zs 2K][su 2K][score 2K][sel K], rounded up to 16 bytes so
+// that every warp's qsum (read as float4) stays 16-byte aligned.
 __host__ __device__ inline size_t walk_smem_per_warp(int K) {
-  const size_t c2 = 2 * (size_t)K;
-  return c2 * sizeof(int) * 2 + c2 * kCZ * 4 + c2 * kKZ * 4 + c2 * 4 + (size_t)K * 4;
+  return ((size_t)64 * 4 + (size_t)2 * K * 16 + (size_t)K * 4 + 15) & ~(size_t)15;
+}
+
+// Children of candidate c (level l) in a sequence of n tokens: whether the
+// second child exists and is eligible, which child the Delta row refers to
+// and the ratio r = n_ref / n_oth.  Only the last node of a level can have
+// unequal children.
+struct Kids {
+  bool two;    // the second child exists and is eligible
+  bool ref1;   // Delta refers to the second child
+  float r;
+};
+
+__device__ __forceinline__ Kids kids_of(int l, int c, int Mc, int n, int t, bool causal) {
+  Kids k;
+  const int c1 = 2 * c + 1;
+  const bool exists = c1 < Mc;
+  k.two = exists && (!causal || (c1 << (kLog2C + l - 2)) <= t);
+  k.ref1 = false;
+  k.r = 1.f;
+  if (exists && c1 == Mc - 1) {  // possibly ragged last pair
+    const int n0 = node_count(l - 1, 2 * c, n), n1 = node_count(l - 1, c1, n);
+    if (n1 < n0) {
+      k.ref1 = true;
+      k.r = (float)n1 / (float)n0;
+    }
+  }
+  return k;
 }
 
 __global__ void __launch_bounds__(kWalkWarps * 32) walk_mma_kernel(
-    const __nv_bfloat16* __restrict__ Q, const unsigned char* __restrict__ table, Levels lv,
-    RowOffsets ro, long long rows_per_bh, long long N, int Hq, int Hkv, int K,
-    int causal, long long jobs, int32_t* __restrict__ surv, int* __restrict__ count, int nchunks,
-    int chunk_shift, int M2) {
+    const __nv_bfloat16* __restrict__ Q, const float* __restrict__ summ, const unsigned char* __restrict__ table,
+    Levels lv, RowOffsets ro, long long rows_per_bh, int N, int Hq, int Hkv, int K, int causal, int l_start,
+    long long jobs, int32_t* __restrict__ surv, int* __restrict__ count, int nchunks, int chunk_shift, int M2) {
   extern __shared__ __align__(16) unsigned char wsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, j = lane & 3;
@@ -151,25 +180,46 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_mma_kernel(
   const int C2 = 2 * K;
   unsigned char* base = wsm + (size_t)warp * walk_smem_per_warp(K);
   WalkSmem S;
-  S.cand = reinterpret_cast<int*>(base);
-  S.src = S.cand + C2;
-  S.cz = reinterpret_cast<float*>(S.src + C2);
-  S.kz = S.cz + C2 * kCZ;
-  S.score = S.kz + C2 * kKZ;
+  S.qsum = reinterpret_cast<float*>(base);
+  S.cand = reinterpret_cast<int*>(S.qsum + 64);
+  S.zs = reinterpret_cast<float*>(S.cand + C2);
+  S.su = S.zs + C2;
+  S.score = S.su + C2;
   S.sel = reinterpret_cast<int*>(S.score + C2);
   constexpr float kL2e = 1.4426950408889634f;
   constexpr float kLn2 = 0.69314718055994531f;
 
   for (long long job = (long long)blockIdx.x * kWalkWarps + warp; job < jobs;
        job += (long long)gridDim.x * kWalkWarps) {
-    const long long t = job % N;
+    const int t = (int)(job % N);
     const long long bh = job / N;
     const int kv = (int)(bh % Hkv);
     const long long b = bh / Hkv;
-    // A fragments: the G heads of this query's group (rows >= G are zero)
-    uint32_t A[4][4];
-    {
-      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + ((b * N + t) * Hq + (long long)kv * G) * kD);
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + ((b * N + t) * Hq + (long long)kv * G) * kD);
+    int nS;  // survivors (candidate indices in S.sel) at the last processed level
+    if (l_start < 2) {
+      // at most K nodes at level 2: every eligible level-2 node survives unscored
+      const int m2 = lv.L >= 2 ? lv.M[2] : 1;
+      const int el = causal ? min(m2, (t >> (kLog2C + 1)) + 1) : m2;
+      nS = el;
+      if (lane < el) {
+        S.cand[lane] = lane;
+        S.sel[lane] = lane;
+      }
+    } else {
+      // head-summed query (fp32), lane owns features 2*lane, 2*lane+1
+      {
+        float a0 = 0.f, a1 = 0.f;
+        for (int h = 0; h < G; ++h) {
+          const uint32_t w = __ldg(q0 + h * 32 + lane);
+          a0 += __uint_as_float(w << 16);
+          a1 += __uint_as_float(w & 0xffff0000u);
+        }
+        S.qsum[2 * lane] = a0;
+        S.qsum[2 * lane + 1] = a1;
+      }
+      // A fragments: the G heads of this query's group (rows >= G are zero)
+      uint32_t A[4][4];
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         const int w0 = 8 * ks + j;
@@ -178,27 +228,30 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_mma_kernel(
         A[ks][2] = g < G ? __ldg(q0 + g * 32 + w0 + 4) : 0u;
         A[ks][3] = g + 8 < G ? __ldg(q0 + (g + 8) * 32 + w0 + 4) : 0u;
       }
-    }
-    const unsigned char* tb = table + bh * rows_per_bh * kRowBytes;
-    int nS;        // survivors of the last processed level
-    if (lv.L == 1) {
-      nS = 1;
-      if (lane == 0) S.sel[0] = 0;
-      if (lane == 0) S.cand[0] = 0;
-    } else {
-      // root logit: direct dot with the root summary row (candidate column 0)
-      float d[4];
-      tile_dot(A, g == 0 ? tb + (rows_per_bh - 1) * kRowBytes : nullptr, j, d);
-      if (j == 0) {
-        S.cz[g] = d[0] * kScale;
-        S.cz[g + 8] = d[2] * kScale;
-      }
-      if (lane == 0) S.cand[0] = 0;
-      int nC = 1;
       __syncwarp();
-      for (int l = lv.L; l >= 2; --l) {
+      // first candidates: the eligible nodes of level l_start, Z by a direct fp32 dot
+      int nC;
+      {
+        const int ml = lv.M[l_start];
+        nC = causal ? min(ml, (t >> (kLog2C + l_start - 1)) + 1) : ml;
+        for (int ci = lane; ci < nC; ci += 32) {
+          const float4* kr = reinterpret_cast<const float4*>(summ + (bh * lv.total + lv.off[l_start] + ci) * kD);
+          const float4* qs = reinterpret_cast<const float4*>(S.qsum);
+          float acc = 0.f;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float4 kk = __ldg(kr + e), qq = qs[e];
+            acc = fmaf(qq.x, kk.x, fmaf(qq.y, kk.y, fmaf(qq.z, kk.z, fmaf(qq.w, kk.w, acc))));
+          }
+          S.cand[ci] = ci;
+          S.zs[ci] = acc * kScale;
+        }
+      }
+      __syncwarp();
+      const unsigned char* tb = table + bh * rows_per_bh * kRowBytes;
+      for (int l = l_start;; --l) {
         const bool scoring = nC > K;
-        const long long Mc = lv.M[l - 1];
+        const int Mc = lv.M[l - 1];
         const unsigned char* lrow = tb + ro.o[l] * kRowBytes;
         for (int nt = 0; nt * 8 < nC; ++nt) {
           const int cb = nt * 8 + g;
@@ -207,40 +260,39 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_mma_kernel(
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const int ci = nt * 8 + 2 * j + cc;
-            float msum = 0.f, prod = 1.f;
+            float su = 0.f, am = 0.f, pr = 1.f;
+            Kids kd;
+            kd.two = false;
+            kd.ref1 = false;
+            kd.r = 1.f;
             if (ci < nC) {
-              const long long c = S.cand[ci];
-              int n0, n1;
-              const int ref = ref_child(l, c, Mc, N, &n0, &n1);
-              const bool elig1 = n1 > 0 && (!causal || node_start(l - 1, 2 * c + 1) <= t);
-              const float ratio = n1 > 0 ? (ref ? (float)n1 / (float)n0 : (float)n0 / (float)n1) : 0.f;
+              kd = kids_of(l, S.cand[ci], Mc, N, t, causal != 0);
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
-                const int h = g + 8 * hh;
-                const float u = d[cc + 2 * hh] * kScale;
-                const float z = S.cz[ci * kCZ + h];
-                const float zr = z + u, zo = fmaf(-ratio, u, z);
-                const float z0 = ref ? zo : zr, z1 = ref ? zr : zo;
-                S.kz[ci * kKZ + h] = z0;
-                S.kz[ci * kKZ + 20 + h] = z1;
-                if (scoring && h < G) {
-                  if (elig1) {
-                    const float mx = fmaxf(z0, z1), mn = fminf(z0, z1);
-                    msum += mx;
-                    prod *= 1.f + ex2_approx((mn - mx) * kL2e);
-                  } else {
-                    msum += z0;
+                if (g + 8 * hh < G) {
+                  const float u = d[cc + 2 * hh] * kScale;
+                  su += u;
+                  if (scoring && kd.two) {
+                    am += u >= 0.f ? u : -kd.r * u;
+                    pr *= 1.f + ex2_approx(-(1.f + kd.r) * fabsf(u) * kL2e);
                   }
                 }
               }
             }
-            if (scoring) {
 #pragma unroll
-              for (int o = 4; o < 32; o <<= 1) {
-                msum += __shfl_xor_sync(kFull, msum, o);
-                prod *= __shfl_xor_sync(kFull, prod, o);
+            for (int o = 4; o < 32; o <<= 1) {
+              su += __shfl_xor_sync(kFull, su, o);
+              if (scoring) {
+                am += __shfl_xor_sync(kFull, am, o);
+                pr *= __shfl_xor_sync(kFull, pr, o);
               }
-              if (g == 0 && ci < nC) S.score[ci] = msum + lg2_approx(prod) * kLn2;
+            }
+            if (g == 0 && ci < nC) {
+              S.su[ci] = su;
+              if (scoring) {
+                const float z = S.zs[ci];
+                S.score[ci] = kd.two ? z + am + lg2_approx(pr) * kLn2 : z + (kd.ref1 ? -kd.r : 1.f) * su;
+              }
             }
           }
         }
@@ -274,33 +326,31 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_mma_kernel(
         }
         __syncwarp();
         if (l == 2) break;
-        // next candidates: eligible children of the survivors, with their logits
-        const long long Mn = lv.M[l - 1];
-        int ci_s = 0;
-        long long c = 0;
+        // next candidates: eligible children of the survivors, with their head-summed Z
+        int c = 0, ci_s = 0;
         bool v1 = false;
+        float z0 = 0.f, z1 = 0.f;
         if (lane < nS) {
           ci_s = S.sel[lane];
           c = S.cand[ci_s];
-          v1 = 2 * c + 1 < Mn && (!causal || node_start(l - 1, 2 * c + 1) <= t);
+          const Kids kd = kids_of(l, c, Mc, N, t, causal != 0);
+          v1 = kd.two;
+          const float z = S.zs[ci_s], su = S.su[ci_s];
+          const float zr = z + su, zo = fmaf(-kd.r, su, z);
+          z0 = kd.ref1 ? zo : zr;
+          z1 = kd.ref1 ? zr : zo;
         }
         const unsigned b1 = __ballot_sync(kFull, v1);
         const int pos = lane + __popc(b1 & ((1u << lane) - 1u));
         const int nN = nS + __popc(b1);
         __syncwarp();
         if (lane < nS) {
-          S.cand[pos] = (int)(2 * c);
-          S.src[pos] = ci_s << 1;
+          S.cand[pos] = 2 * c;
+          S.zs[pos] = z0;
           if (v1) {
-            S.cand[pos + 1] = (int)(2 * c + 1);
-            S.src[pos + 1] = (ci_s << 1) | 1;
+            S.cand[pos + 1] = 2 * c + 1;
+            S.zs[pos + 1] = z1;
           }
-        }
-        __syncwarp();
-        for (int e = lane; e < nN * 16; e += 32) {
-          const int ci = e >> 4, h = e & 15;
-          const int sr = S.src[ci];
-          S.cz[ci * kCZ + h] = S.kz[(sr >> 1) * kKZ + 20 * (sr & 1) + h];
         }
         nC = nN;
         __syncwarp();
@@ -320,7 +370,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_mma_kernel(
 
 // Host side: table size and launches.
 long long route_rows_per_bh(const Levels& lv) {
-  long long r = 1;  // root summary row
+  long long r = 1;  // (at least one row, so that the table is never empty)
   for (int l = 2; l <= lv.L; ++l) r += lv.M[l];
   return r;
 }
@@ -358,9 +408,16 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
   long long blocks = (jobs + kWalkWarps - 1) / kWalkWarps;
   const long long cap = 152LL * 32;
   if (blocks > cap) blocks = cap;
-  walk_mma_kernel<<<(unsigned)blocks, kWalkWarps * 32, smem, s>>>(W.Q, W.table, lv, ro, rows, W.N, W.Hq, W.Hkv, W.K,
-                                                                   W.causal, jobs, W.surv, W.count, W.nchunks,
-                                                                   W.chunk_shift, W.M2);
+  // first scored level: the highest level holding more than K nodes (0: none)
+  int l_start = 0;
+  for (int l = lv.L; l >= 2; --l)
+    if (lv.M[l] > W.K) {
+      l_start = l;
+      break;
+    }
+  walk_mma_kernel<<<(unsigned)blocks, kWalkWarps * 32, smem, s>>>(W.Q, W.summ, W.table, lv, ro, rows, (int)W.N, W.Hq,
+                                                                   W.Hkv, W.K, W.causal, l_start, jobs, W.surv,
+                                                                   W.count, W.nchunks, W.chunk_shift, W.M2);
   note_launch();
   return cudaGetLastError();
 }
