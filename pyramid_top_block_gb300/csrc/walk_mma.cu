@@ -29,12 +29,14 @@
 //
 // Precision.  Delta rows are stored as a pair of bf16 vectors hi + lo
 // (hi = bf16(x), lo = bf16(x - hi)), ~2^-17 relative; q is bf16 and exact.
-// Each dot product is two bf16 mma.sync.m16n8k16 chains (hi and lo)
-// accumulated in fp32: M = 16 query heads, N = 8 candidates, K = 64 features.
+// The dot products are bf16 mma.sync.m16n8k16 in fp32: M = 16 candidates
+// (their Delta rows, hi and lo), N = 8 query heads (two tiles for 16 heads),
+// K = 64 features.  Thread (g, j) of the warp then holds candidates g and g+8
+// for heads 2j, 2j+1 (+8), so a head sum is two shuffles inside a lane quad.
 //
 // Layout of a stored row (256 bytes): hi[64] then lo[64], each with its 32
-// bf16 pairs permuted so that lane quad position j reads its four k-steps' B
-// fragments as two 16-byte loads at byte offset 32 j.
+// bf16 pairs permuted so that lane quad position j reads its four k-steps'
+// A-fragment words as two 16-byte loads at byte offset 32 j.
 #include <mutex>
 
 #include "api.cuh"
@@ -104,29 +106,6 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// d[4] = (raw) dot products of the 16 heads with the row at `row` (hi + lo):
-// thread (g, j) gets heads g, g+8 x candidates 2j, 2j+1 of the n-tile whose
-// B rows the lanes loaded (row == nullptr -> zero column).
-__device__ __forceinline__ void tile_dot(const uint32_t (*A)[4], const unsigned char* row, int j, float* d) {
-  uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0, l0 = h0, l1 = h0;
-  if (row) {
-    const uint4* p = reinterpret_cast<const uint4*>(row + 32 * j);
-    h0 = __ldg(p);
-    h1 = __ldg(p + 1);
-    l0 = __ldg(p + 8);
-    l1 = __ldg(p + 9);
-  }
-  d[0] = d[1] = d[2] = d[3] = 0.f;
-  mma_bf16_16816(d, A[0], h0.x, h0.y);
-  mma_bf16_16816(d, A[1], h0.z, h0.w);
-  mma_bf16_16816(d, A[2], h1.x, h1.y);
-  mma_bf16_16816(d, A[3], h1.z, h1.w);
-  mma_bf16_16816(d, A[0], l0.x, l0.y);
-  mma_bf16_16816(d, A[1], l0.z, l0.w);
-  mma_bf16_16816(d, A[2], l1.x, l1.y);
-  mma_bf16_16816(d, A[3], l1.z, l1.w);
-}
-
 struct WalkSmem {  // per-warp views into dynamic shared memory
   int* cand;     // [2K] node ids of the current candidates (ascending)
   float* zs;     // [2K] head-summed logit Z of each candidate
@@ -136,10 +115,12 @@ struct WalkSmem {  // per-warp views into dynamic shared memory
   float* qsum;   // [64] sum over the group's heads of q (fp32)
 };
 
-// [qsum 64 floats][cand 2K][zs 2K][su 2K][score 2K][sel K], rounded up to 16 bytes so
-// that every warp's qsum (read as float4) stays 16-byte aligned.
+// [qsum 64][score S4][cand 2K][zs 2K][su 2K][sel K] (4-byte words, S4 = 2K rounded up
+// to a multiple of 4), rounded up to 16 bytes: qsum and score are read as float4 and
+// stay 16-byte aligned in every warp's slice.
+__host__ __device__ inline int score_slots(int K) { return (2 * K + 3) & ~3; }
 __host__ __device__ inline size_t walk_smem_per_warp(int K) {
-  return ((size_t)64 * 4 + (size_t)2 * K * 16 + (size_t)K * 4 + 15) & ~(size_t)15;
+  return ((size_t)(64 + score_slots(K) + 6 * K + K) * 4 + 15) & ~(size_t)15;
 }
 
 // Children of candidate c (level l) in a sequence of n tokens: whether the
@@ -169,7 +150,7 @@ __device__ __forceinline__ Kids kids_of(int l, int c, int Mc, int n, int t, bool
   return k;
 }
 
-__global__ void __launch_bounds__(kWalkWarps * 32) walk_mma_kernel(
+__global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
     const __nv_bfloat16* __restrict__ Q, const float* __restrict__ summ, const unsigned char* __restrict__ table,
     Levels lv, RowOffsets ro, long long rows_per_bh, int N, int Hq, int Hkv, int K, int causal, int l_start,
     long long jobs, int32_t* __restrict__ surv, int* __restrict__ count, int nchunks, int chunk_shift, int M2) {
@@ -181,11 +162,11 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_mma_kernel(
   unsigned char* base = wsm + (size_t)warp * walk_smem_per_warp(K);
   WalkSmem S;
   S.qsum = reinterpret_cast<float*>(base);
-  S.cand = reinterpret_cast<int*>(S.qsum + 64);
+  S.score = S.qsum + 64;
+  S.cand = reinterpret_cast<int*>(S.score + score_slots(K));
   S.zs = reinterpret_cast<float*>(S.cand + C2);
   S.su = S.zs + C2;
-  S.score = S.su + C2;
-  S.sel = reinterpret_cast<int*>(S.score + C2);
+  S.sel = reinterpret_cast<int*>(S.su + C2);
   constexpr float kL2e = 1.4426950408889634f;
   constexpr float kLn2 = 0.69314718055994531f;
 
@@ -218,7 +199,8 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_mma_kernel(
         S.qsum[2 * lane] = a0;
         S.qsum[2 * lane + 1] = a1;
       }
-      // A fragments: the G heads of this query's group (rows >= G are zero)
+      // Q^T fragments (the MMA's B operand), per k-step: [0] / [2] = words (2j, 2j+8) of
+      // head g (head tile 0), [1] / [3] the same for head g + 8 (head tile 1); heads >= G are zero
       uint32_t A[4][4];
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
@@ -253,13 +235,48 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_mma_kernel(
         const bool scoring = nC > K;
         const int Mc = lv.M[l - 1];
         const unsigned char* lrow = tb + ro.o[l] * kRowBytes;
-        for (int nt = 0; nt * 8 < nC; ++nt) {
-          const int cb = nt * 8 + g;
-          float d[4];
-          tile_dot(A, cb < nC ? lrow + (long long)S.cand[cb] * kRowBytes : nullptr, j, d);
+        for (int mt = 0; mt * 16 < nC; ++mt) {
+          // A fragments: Delta rows (hi, lo) of candidates 16mt + g and 16mt + g + 8
+          const int c0i = mt * 16 + g, c1i = c0i + 8;
+          uint4 h0[2], l0[2], h1[2], l1[2];
+          {
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            h0[0] = h0[1] = l0[0] = l0[1] = h1[0] = h1[1] = l1[0] = l1[1] = z;
+            if (c0i < nC) {
+              const uint4* p = reinterpret_cast<const uint4*>(lrow + (long long)S.cand[c0i] * kRowBytes + 32 * j);
+              h0[0] = __ldg(p);
+              h0[1] = __ldg(p + 1);
+              l0[0] = __ldg(p + 8);
+              l0[1] = __ldg(p + 9);
+            }
+            if (c1i < nC) {
+              const uint4* p = reinterpret_cast<const uint4*>(lrow + (long long)S.cand[c1i] * kRowBytes + 32 * j);
+              h1[0] = __ldg(p);
+              h1[1] = __ldg(p + 1);
+              l1[0] = __ldg(p + 8);
+              l1[1] = __ldg(p + 9);
+            }
+          }
+          // four independent accumulation chains: (head tile 0/1) x (hi/lo)
+          float dh[2][4] = {}, dl[2][4] = {};
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint4& H0 = h0[ks >> 1];
+            const uint4& H1 = h1[ks >> 1];
+            const uint4& L0 = l0[ks >> 1];
+            const uint4& L1 = l1[ks >> 1];
+            const bool hiw = ks & 1;
+            const uint32_t ah[4] = {hiw ? H0.z : H0.x, hiw ? H1.z : H1.x, hiw ? H0.w : H0.y, hiw ? H1.w : H1.y};
+            const uint32_t al[4] = {hiw ? L0.z : L0.x, hiw ? L1.z : L1.x, hiw ? L0.w : L0.y, hiw ? L1.w : L1.y};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              mma_bf16_16816(dh[nt], ah, A[ks][nt], A[ks][nt + 2]);
+              mma_bf16_16816(dl[nt], al, A[ks][nt], A[ks][nt + 2]);
+            }
+          }
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
-            const int ci = nt * 8 + 2 * j + cc;
+            const int ci = cc ? c1i : c0i;
             float su = 0.f, am = 0.f, pr = 1.f;
             Kids kd;
             kd.two = false;
@@ -268,26 +285,29 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_mma_kernel(
             if (ci < nC) {
               kd = kids_of(l, S.cand[ci], Mc, N, t, causal != 0);
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                if (g + 8 * hh < G) {
-                  const float u = d[cc + 2 * hh] * kScale;
-                  su += u;
-                  if (scoring && kd.two) {
-                    am += u >= 0.f ? u : -kd.r * u;
-                    pr *= 1.f + ex2_approx(-(1.f + kd.r) * fabsf(u) * kL2e);
+              for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  if (8 * nt + 2 * j + e < G) {
+                    const float u = (dh[nt][2 * cc + e] + dl[nt][2 * cc + e]) * kScale;
+                    su += u;
+                    if (scoring && kd.two) {
+                      am += u >= 0.f ? u : -kd.r * u;
+                      pr *= 1.f + ex2_approx(-(1.f + kd.r) * fabsf(u) * kL2e);
+                    }
                   }
                 }
               }
             }
 #pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
+            for (int o = 1; o < 4; o <<= 1) {
               su += __shfl_xor_sync(kFull, su, o);
               if (scoring) {
                 am += __shfl_xor_sync(kFull, am, o);
                 pr *= __shfl_xor_sync(kFull, pr, o);
               }
             }
-            if (g == 0 && ci < nC) {
+            if (j == 0 && ci < nC) {
               S.su[ci] = su;
               if (scoring) {
                 const float z = S.zs[ci];
@@ -311,9 +331,14 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_mma_kernel(
             if (ci < nC) {
               const float sc = S.score[ci];
               int rank = 0;
-              for (int q = 0; q < nC; ++q) {
-                const float o = S.score[q];
-                rank += (o > sc) || (o == sc && q < ci);
+              const float4* s4 = reinterpret_cast<const float4*>(S.score);
+              for (int q4 = 0; q4 * 4 < nC; ++q4) {
+                const float4 o = s4[q4];
+                const int q = 4 * q4;
+                rank += (q < nC && (o.x > sc || (o.x == sc && q < ci)));
+                rank += (q + 1 < nC && (o.y > sc || (o.y == sc && q + 1 < ci)));
+                rank += (q + 2 < nC && (o.z > sc || (o.z == sc && q + 2 < ci)));
+                rank += (q + 3 < nC && (o.w > sc || (o.w == sc && q + 3 < ci)));
               }
               keep[s2] = rank < K;
             }
