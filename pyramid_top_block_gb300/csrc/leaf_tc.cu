@@ -101,13 +101,24 @@ __device__ __forceinline__ float half_lse(const float* x, int lim, bool full) {
   const float nb = -ref * kL2e8;
   float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
   if (full) {
+    // packed pairs: one fma.f32x2 and one add.f32x2 per two keys, four pair accumulators
+    const unsigned long long k2 = f2_pack(kL2e8, kL2e8), n2 = f2_pack(nb, nb);
+    unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-    for (int c = 0; c < 64; c += 4) {
-      s0 += ex2_approx(fmaf(x[c], kL2e8, nb));
-      s1 += ex2_approx(fmaf(x[c + 1], kL2e8, nb));
-      s2 += ex2_approx(fmaf(x[c + 2], kL2e8, nb));
-      s3 += ex2_approx(fmaf(x[c + 3], kL2e8, nb));
+    for (int c = 0; c < 64; c += 2) {
+      float a, b;
+      f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), k2, n2), a, b);
+      acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(ex2_approx(a), ex2_approx(b)));
     }
+    float p0, p1, p2, p3, p4, p5, p6, p7;
+    f2_unpack(acc[0], p0, p1);
+    f2_unpack(acc[1], p2, p3);
+    f2_unpack(acc[2], p4, p5);
+    f2_unpack(acc[3], p6, p7);
+    s0 = p0 + p1;
+    s1 = p2 + p3;
+    s2 = p4 + p5;
+    s3 = p6 + p7;
   } else {
 #pragma unroll
     for (int c = 0; c < 64; c += 4) {

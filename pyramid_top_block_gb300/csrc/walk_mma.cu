@@ -50,6 +50,8 @@ struct RowOffsets {
   long long o[kMaxLevels + 2];
 };
 constexpr int kRowBytes = 256;
+constexpr int kCacheRowBytes = 272;  // shared-memory row stride (16-byte pad against bank conflicts)
+constexpr int kCacheRows = 240;      // Delta rows of the top scored levels kept in shared memory
 
 // Storage position (in bf16 elements, 0..63) of feature d inside a permuted half-row.
 __host__ __device__ __forceinline__ int perm_pos(int d) {
@@ -150,15 +152,30 @@ __device__ __forceinline__ Kids kids_of(int l, int c, int Mc, int n, int t, bool
   return k;
 }
 
+// Grid: blockIdx.y = (b, kv); the CTAs of one (b, kv) take its query positions
+// interleaved (t = blockIdx.x + gridDim.x * i) so causal work stays balanced.
+// Each CTA first copies the Delta rows of levels [l_lo, l_start] of its (b, kv)
+// (contiguous in the table) into shared memory.
 __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
     const __nv_bfloat16* __restrict__ Q, const float* __restrict__ summ, const unsigned char* __restrict__ table,
     Levels lv, RowOffsets ro, long long rows_per_bh, int N, int Hq, int Hkv, int K, int causal, int l_start,
-    long long jobs, int32_t* __restrict__ surv, int* __restrict__ count, int nchunks, int chunk_shift, int M2) {
+    int l_lo, int32_t* __restrict__ surv, int* __restrict__ count, int nchunks, int chunk_shift, int M2) {
   extern __shared__ __align__(16) unsigned char wsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, j = lane & 3;
   const int G = Hq / Hkv;
   const int C2 = 2 * K;
+  const long long bh = blockIdx.y;
+  // shared cache of the top levels' rows
+  const int crow0 = (l_start >= 2) ? (int)ro.o[l_lo] : 0;
+  const int ncache = (l_start >= 2) ? (int)(ro.o[l_start + 1] - ro.o[l_lo]) : 0;
+  unsigned char* cache = wsm + (size_t)kWalkWarps * walk_smem_per_warp(K);
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(table + (bh * rows_per_bh + crow0) * kRowBytes);
+    for (int e = threadIdx.x; e < ncache * 16; e += blockDim.x)
+      *reinterpret_cast<uint4*>(cache + (e >> 4) * kCacheRowBytes + (e & 15) * 16) = __ldg(src + e);
+  }
+  __syncthreads();
   unsigned char* base = wsm + (size_t)warp * walk_smem_per_warp(K);
   WalkSmem S;
   S.qsum = reinterpret_cast<float*>(base);
@@ -170,10 +187,8 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
   constexpr float kL2e = 1.4426950408889634f;
   constexpr float kLn2 = 0.69314718055994531f;
 
-  for (long long job = (long long)blockIdx.x * kWalkWarps + warp; job < jobs;
-       job += (long long)gridDim.x * kWalkWarps) {
-    const int t = (int)(job % N);
-    const long long bh = job / N;
+  for (int t = blockIdx.x + gridDim.x * warp; t < N; t += gridDim.x * kWalkWarps) {
+    const long long job = bh * N + t;
     const int kv = (int)(bh % Hkv);
     const long long b = bh / Hkv;
     const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + ((b * N + t) * Hq + (long long)kv * G) * kD);
@@ -235,6 +250,8 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
         const bool scoring = nC > K;
         const int Mc = lv.M[l - 1];
         const unsigned char* lrow = tb + ro.o[l] * kRowBytes;
+        const bool cached = l >= l_lo;
+        const unsigned char* crow = cache + (ro.o[l] - crow0) * kCacheRowBytes;
         for (int mt = 0; mt * 16 < nC; ++mt) {
           // A fragments: Delta rows (hi, lo) of candidates 16mt + g and 16mt + g + 8
           const int c0i = mt * 16 + g, c1i = c0i + 8;
@@ -242,19 +259,36 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
           {
             const uint4 z = make_uint4(0, 0, 0, 0);
             h0[0] = h0[1] = l0[0] = l0[1] = h1[0] = h1[1] = l1[0] = l1[1] = z;
-            if (c0i < nC) {
-              const uint4* p = reinterpret_cast<const uint4*>(lrow + (long long)S.cand[c0i] * kRowBytes + 32 * j);
-              h0[0] = __ldg(p);
-              h0[1] = __ldg(p + 1);
-              l0[0] = __ldg(p + 8);
-              l0[1] = __ldg(p + 9);
-            }
-            if (c1i < nC) {
-              const uint4* p = reinterpret_cast<const uint4*>(lrow + (long long)S.cand[c1i] * kRowBytes + 32 * j);
-              h1[0] = __ldg(p);
-              h1[1] = __ldg(p + 1);
-              l1[0] = __ldg(p + 8);
-              l1[1] = __ldg(p + 9);
+            if (cached) {
+              if (c0i < nC) {
+                const uint4* p = reinterpret_cast<const uint4*>(crow + S.cand[c0i] * kCacheRowBytes + 32 * j);
+                h0[0] = p[0];
+                h0[1] = p[1];
+                l0[0] = p[8];
+                l0[1] = p[9];
+              }
+              if (c1i < nC) {
+                const uint4* p = reinterpret_cast<const uint4*>(crow + S.cand[c1i] * kCacheRowBytes + 32 * j);
+                h1[0] = p[0];
+                h1[1] = p[1];
+                l1[0] = p[8];
+                l1[1] = p[9];
+              }
+            } else {
+              if (c0i < nC) {
+                const uint4* p = reinterpret_cast<const uint4*>(lrow + (long long)S.cand[c0i] * kRowBytes + 32 * j);
+                h0[0] = __ldg(p);
+                h0[1] = __ldg(p + 1);
+                l0[0] = __ldg(p + 8);
+                l0[1] = __ldg(p + 9);
+              }
+              if (c1i < nC) {
+                const uint4* p = reinterpret_cast<const uint4*>(lrow + (long long)S.cand[c1i] * kRowBytes + 32 * j);
+                h1[0] = __ldg(p);
+                h1[1] = __ldg(p + 1);
+                l1[0] = __ldg(p + 8);
+                l1[1] = __ldg(p + 9);
+              }
             }
           }
           // four independent accumulation chains: (head tile 0/1) x (hi/lo)
@@ -418,8 +452,21 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   mark_phase(1, s);
-  const size_t smem = walk_smem_per_warp(W.K) * kWalkWarps;
-  {  // per-warp scratch grows with K (K = 32: 17 KB per warp)
+  // first scored level: the highest level holding more than K nodes (0: none); the
+  // rows of levels [l_lo, l_start] (at most kCacheRows) are cached in shared memory
+  int l_start = 0;
+  for (int l = lv.L; l >= 2; --l)
+    if (lv.M[l] > W.K) {
+      l_start = l;
+      break;
+    }
+  int l_lo = l_start + 1, crows = 0;
+  while (l_start >= 2 && l_lo - 1 >= 2 && crows + lv.M[l_lo - 1] <= kCacheRows) {
+    --l_lo;
+    crows += lv.M[l_lo];
+  }
+  const size_t smem = walk_smem_per_warp(W.K) * kWalkWarps + (size_t)crows * kCacheRowBytes;
+  {  // per-warp scratch grows with K, the row cache with the tree
     static std::mutex mu;
     static size_t attr = 0;
     std::lock_guard<std::mutex> lock(mu);
@@ -429,20 +476,14 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
       attr = smem;
     }
   }
-  const long long jobs = (long long)BH * W.N;
-  long long blocks = (jobs + kWalkWarps - 1) / kWalkWarps;
-  const long long cap = 152LL * 32;
-  if (blocks > cap) blocks = cap;
-  // first scored level: the highest level holding more than K nodes (0: none)
-  int l_start = 0;
-  for (int l = lv.L; l >= 2; --l)
-    if (lv.M[l] > W.K) {
-      l_start = l;
-      break;
-    }
-  walk_mma_kernel<<<(unsigned)blocks, kWalkWarps * 32, smem, s>>>(W.Q, W.summ, W.table, lv, ro, rows, (int)W.N, W.Hq,
-                                                                   W.Hkv, W.K, W.causal, l_start, jobs, W.surv,
-                                                                   W.count, W.nchunks, W.chunk_shift, W.M2);
+  // CTAs per (b, kv): about 3 resident CTAs per SM over the whole grid
+  int per_bh = (int)((3LL * 152 + BH - 1) / BH);
+  if (per_bh > W.N) per_bh = (int)W.N;
+  if (per_bh < 1) per_bh = 1;
+  dim3 grid((unsigned)per_bh, (unsigned)BH);
+  walk_mma_kernel<<<grid, kWalkWarps * 32, smem, s>>>(W.Q, W.summ, W.table, lv, ro, rows, (int)W.N, W.Hq, W.Hkv, W.K,
+                                                       W.causal, l_start, l_lo, W.surv, W.count, W.nchunks,
+                                                       W.chunk_shift, W.M2);
   note_launch();
   return cudaGetLastError();
 }
