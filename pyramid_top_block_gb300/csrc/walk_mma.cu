@@ -36,7 +36,13 @@
 //
 // Layout of a stored row (256 bytes): hi[64] then lo[64], each with its 32
 // bf16 pairs permuted so that lane quad position j reads its four k-steps'
-// A-fragment words as two 16-byte loads at byte offset 32 j.
+// A-fragment words as two 16-byte loads at byte offset 32 j.  Rows are stored
+// pre-multiplied by log2(e)/sqrt(d), so q . row is a logit in base-2 units.
+//
+// Table of one (b, kv): the Delta rows of levels 2..L (levels ascending, nodes
+// ascending), one zero row, then kZRows "mean rows" kbar of the nodes of the
+// first scored level (zero beyond its size): q_h . kbar for every head is one
+// MMA tile, which gives that level's head-summed Z.
 #include <mutex>
 
 #include "api.cuh"
@@ -50,6 +56,8 @@ struct RowOffsets {
   long long o[kMaxLevels + 2];
 };
 constexpr int kRowBytes = 256;
+constexpr int kZRows = 2 * kMaxK;    // mean rows of the first scored level (at most 2K nodes)
+constexpr float kRowScale = 0.18033688011112042f;  // log2(e) / sqrt(64)
 constexpr int kCacheRowBytes = 272;  // shared-memory row stride (16-byte pad against bank conflicts)
 constexpr int kCacheRows = 240;      // Delta rows of the top scored levels kept in shared memory
 
@@ -67,11 +75,10 @@ __device__ __forceinline__ int ref_child(int l, long long v, long long Mc, long 
   return (*n1 > 0 && *n1 < *n0) ? 1 : 0;
 }
 
-// Route table of one (b, kv): Delta rows of the nodes of levels 2..L (levels
-// ascending, nodes ascending).
-// Thread per (b, kv, row, feature pair).
+// Route table: thread per (b, kv, row, feature pair).
 __global__ void route_table_kernel(const float* __restrict__ summ, Levels lv, long long N, int BH,
-                                   long long rows_per_bh, RowOffsets ro, unsigned char* __restrict__ table) {
+                                   long long rows_per_bh, RowOffsets ro, int l_start,
+                                   unsigned char* __restrict__ table) {
   const long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long total = (long long)BH * rows_per_bh * 32;
   if (w >= total) return;
@@ -79,8 +86,9 @@ __global__ void route_table_kernel(const float* __restrict__ summ, Levels lv, lo
   const long long row = (w >> 5) % rows_per_bh;
   const long long bh = (w >> 5) / rows_per_bh;
   const float* blk = summ + bh * lv.total * kD;
+  const long long zrow0 = ro.o[lv.L + 1] + 1;
   float x[2] = {0.f, 0.f};
-  if (lv.L >= 2 && row < ro.o[lv.L + 1]) {  // (the table's spare last row stays zero)
+  if (lv.L >= 2 && row < ro.o[lv.L + 1]) {  // Delta row (the spare row after them stays zero)
     int l = 2;
     while (l < lv.L && row >= ro.o[l + 1]) ++l;
     const long long v = row - ro.o[l];
@@ -88,7 +96,10 @@ __global__ void route_table_kernel(const float* __restrict__ summ, Levels lv, lo
     const int ref = ref_child(l, v, lv.M[l - 1], N, &n0, &n1);
     const float* pv = blk + (lv.off[l] + v) * kD;
     const float* pc = blk + (lv.off[l - 1] + 2 * v + ref) * kD;
-    for (int e = 0; e < 2; ++e) x[e] = pc[2 * pr + e] - pv[2 * pr + e];
+    for (int e = 0; e < 2; ++e) x[e] = (pc[2 * pr + e] - pv[2 * pr + e]) * kRowScale;
+  } else if (l_start >= 2 && row >= zrow0 && row - zrow0 < lv.M[l_start]) {  // mean row
+    const float* pv = blk + (lv.off[l_start] + (row - zrow0)) * kD;
+    for (int e = 0; e < 2; ++e) x[e] = pv[2 * pr + e] * kRowScale;
   }
   __nv_bfloat16* hi = reinterpret_cast<__nv_bfloat16*>(table + (bh * rows_per_bh + row) * kRowBytes);
   __nv_bfloat16* lo = hi + 64;
@@ -323,7 +334,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                   if (8 * nt + 2 * j + e < G) {
-                    const float u = (dh[nt][2 * cc + e] + dl[nt][2 * cc + e]) * kScale;
+                    const float u = (dh[nt][2 * cc + e] + dl[nt][2 * cc + e]) * kLn2;
                     su += u;
                     if (scoring && kd.two) {
                       am += u >= 0.f ? u : -kd.r * u;
@@ -427,9 +438,304 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// Walk for K <= 8: every level has at most 16 candidates, one MMA tile, and the
+// whole walk stays in registers.  MMA row g holds candidate 2g and row g + 8
+// candidate 2g + 1; after the head sums lane (g, j) owns candidate 2g + (j & 1)
+// (lanes j and j ^ 2 hold identical copies), so the candidates of a level sit in
+// lane order 0, 1, 4, 5, 8, 9, ... and survivor positions are popcounts of
+// ballots.  Scores are base-2 logits (the rows carry log2(e)/sqrt(d)).
+
+// The ragged last pair of children, per level l (children at level l - 1).
+struct LevelTail {
+  int node[kMaxLevels + 2];  // parent whose second child holds fewer tokens than its first (-1: none)
+  float nr[kMaxLevels + 2];  // -(n_second / n_first) for that parent
+};
+
+constexpr int kCandBuf = 64;  // per-warp 32-bit words: two buffers of 16 node ids + 16 Z
+
+__device__ __forceinline__ void ld_row(const unsigned char* p, bool shared_src, bool valid, uint4& h0, uint4& h1,
+                                       uint4& l0, uint4& l1) {
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  h0 = h1 = l0 = l1 = z;
+  if (!valid) return;
+  const uint4* v = reinterpret_cast<const uint4*>(p);
+  if (shared_src) {
+    h0 = v[0];
+    h1 = v[1];
+    l0 = v[8];
+    l1 = v[9];
+  } else {
+    h0 = __ldg(v);
+    h1 = __ldg(v + 1);
+    l0 = __ldg(v + 8);
+    l1 = __ldg(v + 9);
+  }
+}
+
+// q . row for the two MMA-row candidates (a: row g, b: row g + 8) and the
+// lane's heads: u[nt][0..1] = candidate a, heads 8 nt + 2j + {0, 1};
+// u[nt][2..3] = candidate b.
+template <int NT>
+__device__ __forceinline__ void tile_dots(const uint32_t (&A)[4][4], const uint4 (&ra)[4], const uint4 (&rb)[4],
+                                          float (&u)[NT][4]) {
+  float dh[NT][4], dl[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dh[nt][i] = dl[nt][i] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) {
+    const uint4& Ha = ra[ks >> 1];
+    const uint4& La = ra[2 + (ks >> 1)];
+    const uint4& Hb = rb[ks >> 1];
+    const uint4& Lb = rb[2 + (ks >> 1)];
+    const bool hw = ks & 1;
+    const uint32_t ah[4] = {hw ? Ha.z : Ha.x, hw ? Hb.z : Hb.x, hw ? Ha.w : Ha.y, hw ? Hb.w : Hb.y};
+    const uint32_t al[4] = {hw ? La.z : La.x, hw ? Lb.z : Lb.x, hw ? La.w : La.y, hw ? Lb.w : Lb.y};
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      mma_bf16_16816(dh[nt], ah, A[ks][nt], A[ks][nt + 2]);
+      mma_bf16_16816(dl[nt], al, A[ks][nt], A[ks][nt + 2]);
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[nt][i] = dh[nt][i] + dl[nt][i];
+}
+
+// Lane keeps candidate s of the pair (a, b) it computed partial sums for: its
+// own partial plus the partner lane's (lane ^ 1 holds the other candidate).
+__device__ __forceinline__ float keep_add(float pa, float pb, int s) {
+  const float send = s ? pa : pb, mine = s ? pb : pa;
+  return mine + __shfl_xor_sync(kFull, send, 1);
+}
+__device__ __forceinline__ float keep_mul(float pa, float pb, int s) {
+  const float send = s ? pa : pb, mine = s ? pb : pa;
+  return mine * __shfl_xor_sync(kFull, send, 1);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
+    const __nv_bfloat16* __restrict__ Q, const unsigned char* __restrict__ table, Levels lv, RowOffsets ro,
+    LevelTail tail, long long rows_per_bh, int N, int Hq, int Hkv, int K, int causal, int l_start, int l_lo,
+    int32_t* __restrict__ surv, int* __restrict__ count, int nchunks, int chunk_shift, int M2) {
+  extern __shared__ __align__(16) unsigned char wsm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, j = lane & 3, s = j & 1;
+  const int oc = 2 * g + s;  // the candidate this lane owns after the head sums
+  const int G = Hq / Hkv;
+  const long long bh = blockIdx.y;
+  const int kv = (int)(bh % Hkv);
+  const long long b = bh / Hkv;
+  const long long zrow0 = ro.o[lv.L + 1] + 1;
+  // shared memory: [mean rows 16][Delta rows of levels l_lo..l_start][per-warp candidate buffers]
+  const int crow0 = (l_start >= 2) ? (int)ro.o[l_lo] : 0;
+  const int ncache = (l_start >= 2) ? (int)(ro.o[l_start + 1] - ro.o[l_lo]) : 0;
+  unsigned char* czr = wsm;
+  unsigned char* cdr = wsm + 16 * kCacheRowBytes;
+  int* cbuf = reinterpret_cast<int*>(cdr + (size_t)ncache * kCacheRowBytes) + warp * kCandBuf;
+  if (l_start >= 2) {
+    const unsigned char* src0 = table + bh * rows_per_bh * kRowBytes;
+    for (int e = threadIdx.x; e < 16 * 16; e += blockDim.x)
+      *reinterpret_cast<uint4*>(czr + (e >> 4) * kCacheRowBytes + (e & 15) * 16) =
+          __ldg(reinterpret_cast<const uint4*>(src0 + zrow0 * kRowBytes) + e);
+    for (int e = threadIdx.x; e < ncache * 16; e += blockDim.x)
+      *reinterpret_cast<uint4*>(cdr + (e >> 4) * kCacheRowBytes + (e & 15) * 16) =
+          __ldg(reinterpret_cast<const uint4*>(src0 + (long long)crow0 * kRowBytes) + e);
+  }
+  __syncthreads();
+  // padded heads (>= G) get an exponent of -inf: their factor 1 + 2^arg stays 1
+  float2 pad[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    pad[nt].x = (8 * nt + 2 * j < G) ? 0.f : -INFINITY;
+    pad[nt].y = (8 * nt + 2 * j + 1 < G) ? 0.f : -INFINITY;
+  }
+  const unsigned lt = (1u << lane) - 1u;
+  constexpr unsigned kPrimary = 0x33333333u;  // lanes with j < 2: one copy of each candidate
+
+  for (int t = blockIdx.x + gridDim.x * warp; t < N; t += gridDim.x * kWalkWarps) {
+    __syncwarp();  // the previous query's reads of the candidate buffers are done
+    const long long job = bh * N + t;
+    int32_t* out = surv + job * K;
+    int* cnt = count + (bh * nchunks + (t >> chunk_shift)) * M2;
+    if (l_start < 2) {
+      // at most K nodes at level 2: every eligible level-2 node survives unscored
+      const int m2 = lv.L >= 2 ? lv.M[2] : 1;
+      const int el = causal ? min(m2, (t >> (kLog2C + 1)) + 1) : m2;
+      if (lane < K) {
+        const int p = lane < el ? lane : -1;
+        out[lane] = p;
+        if (p >= 0) atomicAdd(cnt + p, 1);
+      }
+      continue;
+    }
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + ((b * N + t) * Hq + (long long)kv * G) * kD);
+    // Q^T fragments (the MMA's B operand): [ks][nt] / [ks][nt + 2] = words (8ks + j, 8ks + j + 4)
+    // of head g + 8 nt; heads >= G are zero
+    uint32_t A[4][4];
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const int w0 = 8 * ks + j;
+      A[ks][0] = g < G ? __ldg(q0 + g * 32 + w0) : 0u;
+      A[ks][2] = g < G ? __ldg(q0 + g * 32 + w0 + 4) : 0u;
+      A[ks][1] = (NT > 1 && g + 8 < G) ? __ldg(q0 + (g + 8) * 32 + w0) : 0u;
+      A[ks][3] = (NT > 1 && g + 8 < G) ? __ldg(q0 + (g + 8) * 32 + w0 + 4) : 0u;
+    }
+    // first candidates: the eligible nodes of level l_start; Z from the mean rows
+    int nC;
+    {
+      const int ml = lv.M[l_start];
+      nC = causal ? min(ml, (t >> (kLog2C + l_start - 1)) + 1) : ml;
+    }
+    int c = oc;  // node id of the owned candidate
+    float Z;
+    {
+      uint4 ra[4], rb[4];
+      ld_row(czr + (2 * g) * kCacheRowBytes + 32 * j, true, 2 * g < nC, ra[0], ra[1], ra[2], ra[3]);
+      ld_row(czr + (2 * g + 1) * kCacheRowBytes + 32 * j, true, 2 * g + 1 < nC, rb[0], rb[1], rb[2], rb[3]);
+      float u[NT][4];
+      tile_dots<NT>(A, ra, rb, u);
+      float sa = 0.f, sb = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        sa += u[nt][0] + u[nt][1];
+        sb += u[nt][2] + u[nt][3];
+      }
+      Z = keep_add(sa, sb, s);
+      Z += __shfl_xor_sync(kFull, Z, 2);
+    }
+    for (int l = l_start;; --l) {
+      const bool scoring = nC > K;
+      const int Mc = lv.M[l - 1];
+      const int lim = causal ? min(Mc - 1, t >> (l + 4)) : Mc - 1;  // last eligible second child
+      const int rag = tail.node[l];
+      const float rnr = tail.nr[l];
+      // rows of the two MMA-row candidates
+      const int c_oth = __shfl_xor_sync(kFull, c, 1);
+      const int na = s ? c_oth : c, nb = s ? c : c_oth;
+      const bool va = 2 * g < nC, vb = 2 * g + 1 < nC;
+      uint4 ra[4], rb[4];
+      if (l >= l_lo) {
+        const unsigned char* base = cdr + (ro.o[l] - crow0) * kCacheRowBytes + 32 * j;
+        ld_row(base + na * kCacheRowBytes, true, va, ra[0], ra[1], ra[2], ra[3]);
+        ld_row(base + nb * kCacheRowBytes, true, vb, rb[0], rb[1], rb[2], rb[3]);
+      } else {
+        const unsigned char* base = table + (bh * rows_per_bh + ro.o[l]) * kRowBytes + 32 * j;
+        ld_row(base + (long long)na * kRowBytes, false, va, ra[0], ra[1], ra[2], ra[3]);
+        ld_row(base + (long long)nb * kRowBytes, false, vb, rb[0], rb[1], rb[2], rb[3]);
+      }
+      float u[NT][4];
+      tile_dots<NT>(A, ra, rb, u);
+      // per candidate of the pair: sum of u, sum of max(u, -r u), prod of (1 + 2^{-(1+r)|u|})
+      float su[2], am[2], pr[2];
+      const bool any_rag = __any_sync(kFull, (va && na == rag) || (vb && nb == rag));
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        unsigned long long s2 = f2_pack(0.f, 0.f), m2 = s2, p2 = f2_pack(1.f, 1.f);
+        if (!any_rag) {  // r = 1: max(u, -u) = |u|, exponent -2|u|
+          const unsigned long long m2c = f2_pack(-2.f, -2.f);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const float ux = u[nt][2 * cc], uy = u[nt][2 * cc + 1];
+            const unsigned long long u2 = f2_pack(ux, uy), a2 = f2_pack(fabsf(ux), fabsf(uy));
+            s2 = f2_add(s2, u2);
+            m2 = f2_add(m2, a2);
+            const unsigned long long x2 = f2_fma(a2, m2c, f2_pack(pad[nt].x, pad[nt].y));
+            float xx, xy;
+            f2_unpack(x2, xx, xy);
+            p2 = f2_fma(p2, f2_pack(ex2_approx(xx), ex2_approx(xy)), p2);
+          }
+        } else {
+          const int nd = cc ? nb : na;
+          const float nr = nd == rag ? rnr : -1.f;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const float ux = u[nt][2 * cc], uy = u[nt][2 * cc + 1];
+            const float tx = nr * ux, ty = nr * uy;
+            const float mx = fmaxf(ux, tx), my = fmaxf(uy, ty);
+            s2 = f2_add(s2, f2_pack(ux, uy));
+            m2 = f2_add(m2, f2_pack(mx, my));
+            const float ex = ex2_approx(fminf(ux, tx) - mx + pad[nt].x);
+            const float ey = ex2_approx(fminf(uy, ty) - my + pad[nt].y);
+            p2 = f2_fma(p2, f2_pack(ex, ey), p2);
+          }
+        }
+        float a, bb;
+        f2_unpack(s2, a, bb);
+        su[cc] = a + bb;
+        f2_unpack(m2, a, bb);
+        am[cc] = a + bb;
+        f2_unpack(p2, a, bb);
+        pr[cc] = a * bb;
+      }
+      // head sums for the owned candidate
+      float sum_u = keep_add(su[0], su[1], s);
+      float part = keep_add(am[0], am[1], s) + lg2_approx(keep_mul(pr[0], pr[1], s));
+      sum_u += __shfl_xor_sync(kFull, sum_u, 2);
+      part += __shfl_xor_sync(kFull, part, 2);
+      const bool valid = oc < nC;
+      const bool two = 2 * c + 1 <= lim;
+      const bool ref1 = c == rag;
+      const float nr = ref1 ? rnr : -1.f;
+      bool keep = valid;
+      if (scoring) {
+        const float sc = Z + (two ? part : (ref1 ? nr : 1.f) * sum_u);
+        // order-preserving integer key; the low 4 bits hold 15 - candidate (lower index wins a tie)
+        const unsigned fb = __float_as_uint(sc);
+        unsigned key = fb ^ ((unsigned)((int)fb >> 31) | 0x80000000u);
+        key = valid ? ((key & ~15u) | (unsigned)(15 - oc)) : 0u;
+        int rank = 0;
+        const int half = 16 * (j >> 1);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const unsigned o = __shfl_sync(kFull, key, half + 4 * (k >> 1) + (k & 1));
+          rank += o > key;
+        }
+        rank += __shfl_xor_sync(kFull, rank, 2);
+        keep = valid && rank < K;
+      }
+      const unsigned bk = __ballot_sync(kFull, keep) & kPrimary;
+      const unsigned b2 = __ballot_sync(kFull, keep && two) & kPrimary;
+      const int before = __popc(bk & lt);
+      if (l == 2) {
+        if (j < 2 && keep) {
+          out[before] = c;
+          atomicAdd(cnt + c, 1);
+        }
+        const int nS = __popc(bk);
+        if (lane < K && lane >= nS) out[lane] = -1;
+        break;
+      }
+      // next candidates: the survivors' eligible children, ascending, with their Z
+      {
+        const float zr = Z + sum_u, zo = fmaf(nr, sum_u, Z);
+        int* buf = cbuf + ((l & 1) << 5);
+        if (j < 2 && keep) {
+          const int pos = before + __popc(b2 & lt);
+          buf[pos] = 2 * c;
+          buf[16 + pos] = __float_as_int(ref1 ? zo : zr);
+          if (two) {
+            buf[pos + 1] = 2 * c + 1;
+            buf[16 + pos + 1] = __float_as_int(ref1 ? zr : zo);
+          }
+        }
+        nC = __popc(bk) + __popc(b2);
+        __syncwarp();
+        if (oc < nC) {
+          c = buf[oc];
+          Z = __int_as_float(buf[16 + oc]);
+        }
+      }
+    }
+  }
+}
+
 // Host side: table size and launches.
 long long route_rows_per_bh(const Levels& lv) {
-  long long r = 1;  // (at least one row, so that the table is never empty)
+  long long r = 1 + kZRows;  // the zero row and the mean rows
   for (int l = 2; l <= lv.L; ++l) r += lv.M[l];
   return r;
 }
@@ -446,24 +752,63 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
     o += lv.M[l];
   }
   ro.o[lv.L + 1] = o;
-  const long long thr = (long long)BH * rows * 32;
-  route_table_kernel<<<(unsigned)((thr + 255) / 256), 256, 0, s>>>(W.summ, lv, W.N, BH, rows, ro, W.table);
-  note_launch();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  mark_phase(1, s);
-  // first scored level: the highest level holding more than K nodes (0: none); the
-  // rows of levels [l_lo, l_start] (at most kCacheRows) are cached in shared memory
+  // first scored level: the highest level holding more than K nodes (0: none)
   int l_start = 0;
   for (int l = lv.L; l >= 2; --l)
     if (lv.M[l] > W.K) {
       l_start = l;
       break;
     }
+  const long long thr = (long long)BH * rows * 32;
+  route_table_kernel<<<(unsigned)((thr + 255) / 256), 256, 0, s>>>(W.summ, lv, W.N, BH, rows, ro, l_start, W.table);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mark_phase(1, s);
+  // the rows of levels [l_lo, l_start] (at most kCacheRows) are cached in shared memory
   int l_lo = l_start + 1, crows = 0;
   while (l_start >= 2 && l_lo - 1 >= 2 && crows + lv.M[l_lo - 1] <= kCacheRows) {
     --l_lo;
     crows += lv.M[l_lo];
+  }
+  // CTAs per (b, kv): about 3 resident CTAs per SM over the whole grid
+  int per_bh = (int)((3LL * 152 + BH - 1) / BH);
+  if (per_bh > W.N) per_bh = (int)W.N;
+  if (per_bh < 1) per_bh = 1;
+  dim3 grid((unsigned)per_bh, (unsigned)BH);
+  const int G = W.Hq / W.Hkv;
+  if (W.K <= 8) {
+    LevelTail tail;
+    for (int l = 0; l < kMaxLevels + 2; ++l) {
+      tail.node[l] = -1;
+      tail.nr[l] = -1.f;
+    }
+    for (int l = 2; l <= lv.L; ++l) {
+      const int Mc = lv.M[l - 1];
+      if (Mc >= 2 && (Mc & 1) == 0) {
+        const int n0 = node_count(l - 1, Mc - 2, W.N), n1 = node_count(l - 1, Mc - 1, W.N);
+        if (n1 < n0) {
+          tail.node[l] = Mc / 2 - 1;
+          tail.nr[l] = -((float)n1 / (float)n0);
+        }
+      }
+    }
+    const size_t smem = (size_t)(16 + crows) * kCacheRowBytes + (size_t)kWalkWarps * kCandBuf * 4;
+    auto kern = G > 8 ? walk_k8_kernel<2> : walk_k8_kernel<1>;
+    {
+      static std::mutex mu;
+      static size_t attr[2] = {0, 0};
+      std::lock_guard<std::mutex> lock(mu);
+      if (smem > attr[G > 8]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr[G > 8] = smem;
+      }
+    }
+    kern<<<grid, kWalkWarps * 32, smem, s>>>(W.Q, W.table, lv, ro, tail, rows, (int)W.N, W.Hq, W.Hkv, W.K, W.causal,
+                                              l_start, l_lo, W.surv, W.count, W.nchunks, W.chunk_shift, W.M2);
+    note_launch();
+    return cudaGetLastError();
   }
   const size_t smem = walk_smem_per_warp(W.K) * kWalkWarps + (size_t)crows * kCacheRowBytes;
   {  // per-warp scratch grows with K, the row cache with the tree
@@ -476,11 +821,6 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
       attr = smem;
     }
   }
-  // CTAs per (b, kv): about 3 resident CTAs per SM over the whole grid
-  int per_bh = (int)((3LL * 152 + BH - 1) / BH);
-  if (per_bh > W.N) per_bh = (int)W.N;
-  if (per_bh < 1) per_bh = 1;
-  dim3 grid((unsigned)per_bh, (unsigned)BH);
   walk_mma_kernel<<<grid, kWalkWarps * 32, smem, s>>>(W.Q, W.summ, W.table, lv, ro, rows, (int)W.N, W.Hq, W.Hkv, W.K,
                                                        W.causal, l_start, l_lo, W.surv, W.count, W.nchunks,
                                                        W.chunk_shift, W.M2);
