@@ -30,7 +30,7 @@ struct LeafTcLaunch {
   int* cursor;
   int* bucket_off;
   int* tile_off;
-  int* tile_bkt;        // [max_tiles] bucket of each tile
+  int4* tile_desc;      // [max_tiles] {first entry, rows, level-2 survivor p, b * Hkv + kv}
   long long max_tiles;  // upper bound on the number of tiles
   uint32_t* list;
   float* leaf_scores;

@@ -32,9 +32,17 @@ namespace pisa {
 
 constexpr int kLeafStages = 6;    // query-row tiles in flight (16 KB each)
 constexpr int kAccBufs = 4;       // TMEM accumulators of 128 fp32 columns
-constexpr int kLeafWarps = 12;    // metadata, MMA, 2 epilogue warpgroups, 2 query-row warps
+constexpr int kLeafWarps = 16;    // key-block loader, MMA, 2 query-row warps, 3 epilogue warpgroups
+constexpr int kEpiGroups = 3;     // epilogue warpgroups (warps 4..15)
+// A warpgroup waits for tile k only after finishing tile k - kEpiGroups, so with
+// kEpiGroups <= kAccBufs the accumulator barrier it waits on is never more than
+// one phase behind (the MMA warp commits tiles in order).
+static_assert(kEpiGroups <= kAccBufs, "an epilogue warpgroup could run two accumulator phases ahead");
 constexpr int kTileBlock = 32;    // consecutive tiles handled by one CTA in a row
-constexpr int kInfo = 16;         // tile descriptors in flight (producer -> MMA / epilogue)
+// Query-row warp w loads tiles k = w (mod 2); with an even stage count the stage it
+// refills last held one of its own tiles, so its wait on a_empty is never two
+// phases ahead.
+static_assert(kLeafStages % 2 == 0, "query-row warps alternate tiles");
 constexpr int kTileBytes = 128 * 128;  // 128 rows of 64 bf16
 constexpr size_t kLeafSmem = (size_t)(kLeafStages + 2) * kTileBytes + 1024;
 
@@ -43,7 +51,7 @@ struct LeafTcParams {
   const uint32_t* list;
   const int* bucket_off;
   const int* tile_off;
-  const int* tile_bkt;
+  const int4* tile_desc;  // per tile: first entry, rows, level-2 survivor p, b * Hkv + kv
   int nb;
   int Hq, Hkv, G, Gp, R, K;
   long long N, n_cap;
@@ -53,23 +61,10 @@ struct LeafTcParams {
   int* status;
 };
 
-struct Bucket {
-  int b, kv, p;
-};
-
-// What the producer tells the MMA and epilogue warps about tile k.
-struct TileInfo {
-  int bkt, nrows;
-  uint32_t ent[16];  // (t << 5 | slot) of each query row of the tile
-};
-
-__device__ __forceinline__ Bucket decode_bucket(int bkt, int M2, int nchunks, int Hkv) {
-  Bucket r;
-  r.p = bkt % M2;
-  const int bkv = bkt / M2 / nchunks;
-  r.kv = bkv % Hkv;
-  r.b = bkv / Hkv;
-  return r;
+// Global index of this CTA's k-th tile: blocks of kTileBlock consecutive tiles,
+// block j on CTA j % gridDim.x.
+__device__ __forceinline__ int tile_of(int k) {
+  return (blockIdx.x + gridDim.x * (k / kTileBlock)) * kTileBlock + (k % kTileBlock);
 }
 
 // Largest bucket whose first tile is <= tile (tile_off is non-decreasing).
@@ -90,22 +85,18 @@ __device__ __forceinline__ void leaf_abort(volatile int* abort, int* status) {
   set_status(status, PISA_ERR_DEVICE_TIMEOUT);
 }
 
-// Masked log-sum-exp of one 64-key half: x holds the raw q.k dot products,
-// lim the number of leading keys that count (1..64).  Exponents are taken
-// relative to the first key's logit (exp2 of (x - x0) * log2(e)/8); if that
-// overflows, the sum is redone relative to the true maximum.
-__device__ __forceinline__ float half_lse(const float* x, int lim, bool full) {
-  constexpr float kL2e8 = 0.18033688011112042f;  // log2(e) / sqrt(64)
-  constexpr float kLn2 = 0.69314718055994531f;
-  const float ref = x[0];
-  const float nb = -ref * kL2e8;
-  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+constexpr float kL2e8 = 0.18033688011112042f;  // log2(e) / sqrt(64)
+
+// sum_{i < cnt} 2^(x_i * log2(e)/8 + nb) over one 32-column chunk of raw q.k dot
+// products (nb = -ref * log2(e)/8 for the half's reference logit ref).  `full`
+// (warp-uniform) means every lane has cnt == 32: packed f32x2 arithmetic, one
+// fma.f32x2 and one add.f32x2 per two keys into four pair accumulators.
+__device__ __forceinline__ float chunk_exp_sum(const float (&x)[32], int cnt, bool full, float nb) {
   if (full) {
-    // packed pairs: one fma.f32x2 and one add.f32x2 per two keys, four pair accumulators
     const unsigned long long k2 = f2_pack(kL2e8, kL2e8), n2 = f2_pack(nb, nb);
     unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-    for (int c = 0; c < 64; c += 2) {
+    for (int c = 0; c < 32; c += 2) {
       float a, b;
       f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), k2, n2), a, b);
       acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(ex2_approx(a), ex2_approx(b)));
@@ -115,34 +106,59 @@ __device__ __forceinline__ float half_lse(const float* x, int lim, bool full) {
     f2_unpack(acc[1], p2, p3);
     f2_unpack(acc[2], p4, p5);
     f2_unpack(acc[3], p6, p7);
-    s0 = p0 + p1;
-    s1 = p2 + p3;
-    s2 = p4 + p5;
-    s3 = p6 + p7;
-  } else {
+    return ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7));
+  }
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-    for (int c = 0; c < 64; c += 4) {
-      s0 += c < lim ? ex2_approx(fmaf(x[c], kL2e8, nb)) : 0.f;
-      s1 += c + 1 < lim ? ex2_approx(fmaf(x[c + 1], kL2e8, nb)) : 0.f;
-      s2 += c + 2 < lim ? ex2_approx(fmaf(x[c + 2], kL2e8, nb)) : 0.f;
-      s3 += c + 3 < lim ? ex2_approx(fmaf(x[c + 3], kL2e8, nb)) : 0.f;
+  for (int c = 0; c < 32; c += 4) {
+    s0 += c < cnt ? ex2_approx(fmaf(x[c], kL2e8, nb)) : 0.f;
+    s1 += c + 1 < cnt ? ex2_approx(fmaf(x[c + 1], kL2e8, nb)) : 0.f;
+    s2 += c + 2 < cnt ? ex2_approx(fmaf(x[c + 2], kL2e8, nb)) : 0.f;
+    s3 += c + 3 < cnt ? ex2_approx(fmaf(x[c + 3], kL2e8, nb)) : 0.f;
+  }
+  return (s0 + s1) + (s2 + s3);
+}
+
+// Running masked log-sum-exp of one 64-key half, fed 32 columns at a time.
+// Exponents are taken relative to the half's first key (no max pass); if a
+// chunk would overflow the running sum, the reference moves up to that chunk's
+// maximum and the sum so far is rescaled.
+struct HalfLse {
+  float ref, s;
+  __device__ __forceinline__ void first(const float (&x)[32], int cnt, bool full) {
+    ref = x[0];
+    s = 0.f;
+    add(x, cnt, full);
+  }
+  __device__ __forceinline__ void add(const float (&x)[32], int cnt, bool full) {
+    const float t = s + chunk_exp_sum(x, cnt, full, -ref * kL2e8);
+    if (__any_sync(kFull, !(t <= 3.0e38f))) {  // rare: rescale against the chunk maximum
+      if (!(t <= 3.0e38f)) {
+        float m = ref;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c < cnt) m = fmaxf(m, x[c]);
+        s = s * ex2_approx((ref - m) * kL2e8) + chunk_exp_sum(x, cnt, false, -m * kL2e8);
+        ref = m;
+      } else {
+        s = t;
+      }
+    } else {
+      s = t;
     }
   }
-  float s = (s0 + s1) + (s2 + s3);
-  float r = ref;
-  if (!(s <= 3.0e38f)) {  // overflow (or NaN input): redo against the maximum
-    float m = x[0];
-#pragma unroll
-    for (int c = 1; c < 64; ++c)
-      if (c < lim) m = fmaxf(m, x[c]);
-    const float nm = -m * kL2e8;
-    s = 0.f;
-#pragma unroll
-    for (int c = 0; c < 64; ++c)
-      if (c < lim) s += ex2_approx(fmaf(x[c], kL2e8, nm));
-    r = m;
+  __device__ __forceinline__ float value() const {  // natural-log units
+    return ref * 0.125f + lg2_approx(s) * 0.69314718055994531f;
   }
-  return r * 0.125f + lg2_approx(s) * kLn2;
+};
+
+// Orders the uses of registers written by tcgen05.ld after the wait::ld that
+// completes them.
+__device__ __forceinline__ void reg_fence32(float (&x)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 8)
+    asm volatile("" : "+f"(x[i]), "+f"(x[i + 1]), "+f"(x[i + 2]), "+f"(x[i + 3]), "+f"(x[i + 4]), "+f"(x[i + 5]),
+                 "+f"(x[i + 6]), "+f"(x[i + 7]));
 }
 
 __global__ void __launch_bounds__(kLeafWarps * 32, 1)
@@ -153,8 +169,7 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
   unsigned char* sA = sm;
   unsigned char* sB = sm + kLeafStages * kTileBytes;
   __shared__ uint64_t a_full[kLeafStages], a_empty[kLeafStages], b_full[2], b_empty[2];
-  __shared__ uint64_t acc_full[kAccBufs], acc_empty[kAccBufs], info_full[kInfo], info_empty[kInfo], mma_done;
-  __shared__ TileInfo info[kInfo];
+  __shared__ uint64_t acc_full[kAccBufs], acc_empty[kAccBufs], mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   volatile int* abort = &abort_flag;
@@ -173,10 +188,6 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
       mbar_init(&acc_full[s], 1);
       mbar_init(&acc_empty[s], 128);
     }
-    for (int s = 0; s < kInfo; ++s) {
-      mbar_init(&info_full[s], 1);
-      mbar_init(&info_empty[s], 128 + 32);  // the epilogue warpgroup + the query-row warp
-    }
     mbar_init(&mma_done, 1);
     abort_flag = 0;
     mbar_fence_init();
@@ -185,197 +196,183 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const int R = P.R, Gp = P.Gp, G = P.G;
+  const int Gp = P.Gp, G = P.G;
   const int total = __ldg(P.tile_off + P.nb);
-  // this CTA's tiles: blocks of kTileBlock consecutive tiles, block j on CTA j % gridDim.x
   int my_tiles = 0;
   for (int blk = blockIdx.x; blk * kTileBlock < total; blk += gridDim.x) my_tiles += min(kTileBlock, total - blk * kTileBlock);
 
-  if (warp == 0) {
-    // ---------------- metadata warp: resolves tiles (lane-parallel, one block of kTileBlock
-    // tiles at a time), waits for a free stage, loads key blocks by TMA, arms a_full with
-    // the tile's byte count and publishes the tile descriptor (info ring).
-    int k = 0, nbchg = 0, prev = -1;
+  if (warp <= 1) {
+    // ---------------- warp 0 loads the key block (two sibling leaves, 128 keys) of every
+    // run of tiles with the same (b, kv, p) into a double buffer; warp 1 drives the tensor
+    // core.  Both read this CTA's tile descriptors 32 at a time and find the key-block
+    // changes with a ballot.
+    const bool mma = warp == 1;
+    const uint32_t idesc = umma_idesc_bf16(128, 128);
+    int nchg = 0, cur = 0, prev_p = -1, prev_bh = -1, k = 0;
     bool ok = true;
     for (int blk = blockIdx.x; ok && blk * kTileBlock < total; blk += gridDim.x) {
       const int i0 = blk * kTileBlock;
       const int n = min(kTileBlock, total - i0);
-      int mb = 0, me0 = 0, mn = 0;
-      if (lane < n) {
-        mb = __ldg(P.tile_bkt + i0 + lane);
-        const int to = __ldg(P.tile_off + mb);
-        me0 = __ldg(P.bucket_off + mb) + (i0 + lane - to) * R;
-        mn = min(R, __ldg(P.bucket_off + mb + 1) - me0);
+      const int4 d = lane < n ? __ldg(P.tile_desc + i0 + lane) : make_int4(0, 0, -1, -1);
+      int pp = __shfl_up_sync(kFull, d.z, 1), pb = __shfl_up_sync(kFull, d.w, 1);
+      if (lane == 0) {
+        pp = prev_p;
+        pb = prev_bh;
       }
-      uint32_t ents[kTileBlock];  // lane r holds entry r of every tile of the block
-#pragma unroll
-      for (int m = 0; m < kTileBlock; ++m) {
-        const int e0 = __shfl_sync(kFull, me0, m), nr = __shfl_sync(kFull, mn, m);
-        ents[m] = (m < n && lane < nr) ? __ldg(P.list + e0 + lane) : 0u;
-      }
-#pragma unroll 1
-      for (int m = 0; m < n && ok; ++m, ++k) {
-        const int bkt = __shfl_sync(kFull, mb, m), nrows = __shfl_sync(kFull, mn, m);
-        const int slot = k % kInfo, s = k % kLeafStages;
-        bool w = true;
-        if (lane == 0) {
-          if (k >= kInfo) w = mbar_wait(&info_empty[slot], ((k / kInfo) - 1) & 1, abort);
-          if (w && bkt != prev) {
-            const Bucket bk = decode_bucket(bkt, P.M2, P.nchunks, P.Hkv);
-            const int bb = nbchg & 1;
-            if (nbchg >= 2) w = mbar_wait(&b_empty[bb], ((nbchg >> 1) - 1) & 1, abort);
+      const unsigned chg = __ballot_sync(kFull, lane < n && (d.z != pp || d.w != pb));
+      prev_p = __shfl_sync(kFull, d.z, n - 1);
+      prev_bh = __shfl_sync(kFull, d.w, n - 1);
+      if (!mma) {
+        for (unsigned m = chg; m && ok; m &= m - 1) {
+          const int src = __ffs(m) - 1;
+          const int p = __shfl_sync(kFull, d.z, src), bh = __shfl_sync(kFull, d.w, src);
+          bool w = true;
+          if (lane == 0) {
+            const int bb = nchg & 1;
+            if (nchg >= 2) w = mbar_wait(&b_empty[bb], ((nchg >> 1) - 1) & 1, abort);
             if (w) {
               mbar_expect_tx(&b_full[bb], kTileBytes);
-              tma_load_3d(sB + bb * kTileBytes, &kmap, 0, bk.kv, (int)(bk.b * P.n_cap + 128LL * bk.p), &b_full[bb]);
+              tma_load_3d(sB + bb * kTileBytes, &kmap, 0, bh % P.Hkv, (int)((bh / P.Hkv) * P.n_cap + 128LL * p),
+                          &b_full[bb]);
             }
           }
-          if (w && k >= kLeafStages) w = mbar_wait(&a_empty[s], ((k / kLeafStages) - 1) & 1, abort);
-          if (w) mbar_expect_tx(&a_full[s], (uint32_t)(nrows * G * 128));
+          ok = __shfl_sync(kFull, w, 0);
+          ++nchg;
         }
-        ok = __shfl_sync(kFull, w, 0);
-        if (!ok) {
-          if (lane == 0) leaf_abort(abort, P.status);
-          break;
-        }
-        if (bkt != prev) {
-          ++nbchg;
-          prev = bkt;
-        }
-        uint32_t e = 0;
+      } else {
+        for (int m = 0; m < n && ok; ++m, ++k) {
+          const int s = k % kLeafStages, a = k % kAccBufs;
+          bool w = true;
+          if (lane == 0) {
+            if ((chg >> m) & 1) {
+              if (nchg > 0) umma_commit(&b_empty[cur]);  // fires once the previous block's MMAs are done
+              cur = nchg & 1;
+              w = mbar_wait(&b_full[cur], (nchg >> 1) & 1, abort);
+              ++nchg;
+            }
+            w = w && mbar_wait(&a_full[s], (k / kLeafStages) & 1, abort);
+            w = w && (k < kAccBufs || mbar_wait(&acc_empty[a], ((k / kAccBufs) - 1) & 1, abort));
+            if (w) {
+              tc_fence_after();
+              const uint64_t da = umma_desc_sw128(sA + s * kTileBytes);
+              const uint64_t db = umma_desc_sw128(sB + cur * kTileBytes);
 #pragma unroll
-        for (int mm = 0; mm < kTileBlock; ++mm)
-          if (mm == m) e = ents[mm];
-        if (lane < nrows) info[slot].ent[lane] = e;
-        if (lane == 0) {
-          info[slot].bkt = bkt;
-          info[slot].nrows = nrows;
+              for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + a * 128, da + 2 * kk, db + 2 * kk, idesc, kk > 0);
+              umma_commit(&a_empty[s]);
+              umma_commit(&acc_full[a]);
+            }
+          }
+          ok = __shfl_sync(kFull, w, 0);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&info_full[slot]);
       }
-      __syncwarp();
     }
-  } else if (warp >= kLeafWarps - 2) {
-    // ---------------- query-row warps: tile k's rows are loaded by warp (k & 1), one
-    // TMA box {64 features, G heads, 1 token} per query, completing on a_full
-    const int tw = warp - (kLeafWarps - 2);
+    if (!ok && lane == 0) leaf_abort(abort, P.status);
+    if (mma && lane == 0) {
+      // every MMA this thread issued has completed once mma_done fires (waited for even
+      // after an abort, with a poll limit, so that TMEM is never freed under an MMA)
+      umma_commit(&mma_done);
+      if (!mbar_wait(&mma_done, 0, nullptr)) leaf_abort(abort, P.status);
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ---------------- query-row warps: tile k's rows are loaded by warp 2 + (k & 1), one
+    // TMA box {64 features, G heads, 1 token} per query, completing on a_full.  The
+    // descriptors are read two tiles ahead and the entries one tile ahead.
+    const int tw = warp - 2;
+    int4 d1 = make_int4(0, 0, 0, 0), d2 = make_int4(0, 0, 0, 0);
+    if (tw < my_tiles) d1 = __ldg(P.tile_desc + tile_of(tw));
+    if (tw + 2 < my_tiles) d2 = __ldg(P.tile_desc + tile_of(tw + 2));
+    uint32_t e1 = lane < d1.y ? __ldg(P.list + d1.x + lane) : 0u;
     for (int k = tw; k < my_tiles; k += 2) {
-      const int slot = k % kInfo, s = k % kLeafStages;
-      const bool ok = __all_sync(kFull, mbar_wait(&info_full[slot], (k / kInfo) & 1, abort));
-      if (!ok) {
+      const int4 d = d1;
+      const uint32_t ent = e1;
+      d1 = d2;
+      e1 = (k + 2 < my_tiles && lane < d1.y) ? __ldg(P.list + d1.x + lane) : 0u;
+      if (k + 4 < my_tiles) d2 = __ldg(P.tile_desc + tile_of(k + 4));
+      const int s = k % kLeafStages;
+      bool w = true;
+      if (lane == 0) {
+        if (k >= kLeafStages) w = mbar_wait(&a_empty[s], ((k / kLeafStages) - 1) & 1, abort);
+        if (w) mbar_expect_tx(&a_full[s], (uint32_t)(d.y * G * 128));
+      }
+      if (!__shfl_sync(kFull, w, 0)) {
         if (lane == 0) leaf_abort(abort, P.status);
         break;
       }
-      const Bucket bk = decode_bucket(info[slot].bkt, P.M2, P.nchunks, P.Hkv);
-      const int nrows = info[slot].nrows;
-      if (lane < nrows) {
-        const uint32_t ent = info[slot].ent[lane];
-        tma_load_3d(sA + s * kTileBytes + lane * Gp * 128, &qmap, 0, bk.kv * G, (int)(bk.b * P.N + (ent >> 5)),
-                    &a_full[s]);
-      }
       __syncwarp();
-      mbar_arrive(&info_empty[slot]);
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer: one thread drives the tensor core
-    if (lane == 0) {
-      const uint32_t idesc = umma_idesc_bf16(128, 128);
-      int nbchg = 0, prev = -1, cur = 0;
-      for (int k = 0; k < my_tiles; ++k) {
-        const int slot = k % kInfo, s = k % kLeafStages, a = k % kAccBufs;
-        if (!mbar_wait(&info_full[slot], (k / kInfo) & 1, abort)) {
-          leaf_abort(abort, P.status);
-          break;
-        }
-        const int bkt = info[slot].bkt;
-        if (bkt != prev) {
-          if (prev >= 0) umma_commit(&b_empty[cur]);
-          cur = nbchg & 1;
-          if (!mbar_wait(&b_full[cur], (nbchg >> 1) & 1, abort)) {
-            leaf_abort(abort, P.status);
-            break;
-          }
-          ++nbchg;
-          prev = bkt;
-        }
-        if (!mbar_wait(&a_full[s], (k / kLeafStages) & 1, abort)) {
-          leaf_abort(abort, P.status);
-          break;
-        }
-        if (k >= kAccBufs && !mbar_wait(&acc_empty[a], ((k / kAccBufs) - 1) & 1, abort)) {
-          leaf_abort(abort, P.status);
-          break;
-        }
-        tc_fence_after();
-        const uint64_t da = umma_desc_sw128(sA + s * kTileBytes);
-        const uint64_t db = umma_desc_sw128(sB + cur * kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + a * 128, da + 2 * kk, db + 2 * kk, idesc, kk > 0);
-        umma_commit(&a_empty[s]);
-        umma_commit(&acc_full[a]);
-      }
-      // every MMA this thread issued has completed once mma_done fires
-      umma_commit(&mma_done);
-      if (!mbar_wait(&mma_done, 0, abort)) leaf_abort(abort, P.status);
+      if (lane < d.y)
+        tma_load_3d(sA + s * kTileBytes + lane * Gp * 128, &qmap, 0, (d.w % P.Hkv) * G,
+                    (int)((d.w / P.Hkv) * P.N + (ent >> 5)), &a_full[s]);
     }
   } else {
-    // ---------------- epilogue (warps 2..9): TMEM -> registers -> log-sum-exp -> head sum
-    const int wg = (warp - 2) >> 2;
+    // ---------------- epilogue (warps 4..15): warpgroup wg takes tiles wg, wg + 3, ...;
+    // TMEM -> registers 32 columns at a time -> log-sum-exp per key half -> head sum
+    const int wg = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const int r = row / Gp, h = row % Gp;
-    for (int k = wg; k < my_tiles; k += 2) {
-      const int a = k % kAccBufs, slot = k % kInfo;
-      const bool ok = __all_sync(kFull, mbar_wait(&acc_full[a], (k / kAccBufs) & 1, abort) &&
-                                            mbar_wait(&info_full[slot], (k / kInfo) & 1, abort));
+    int4 dn = wg < my_tiles ? __ldg(P.tile_desc + tile_of(wg)) : make_int4(0, 0, 0, 0);
+    for (int k = wg; k < my_tiles; k += kEpiGroups) {
+      const int a = k % kAccBufs;
+      const int4 d = dn;  // this tile's descriptor (read one tile ahead)
+      const bool qvalid = r < d.y;
+      const uint32_t ent = qvalid ? __ldg(P.list + d.x + r) : 0u;
+      if (k + kEpiGroups < my_tiles) dn = __ldg(P.tile_desc + tile_of(k + kEpiGroups));
+      const bool ok = __all_sync(kFull, mbar_wait(&acc_full[a], (k / kAccBufs) & 1, abort));
       if (!ok) {  // warp-uniform exit
         leaf_abort(abort, P.status);
         break;
       }
       tc_fence_after();
-      const Bucket bk = decode_bucket(info[slot].bkt, P.M2, P.nchunks, P.Hkv);
-      const int nrows = info[slot].nrows;
-      const bool qvalid = r < nrows;
-      const uint32_t ent = qvalid ? info[slot].ent[r] : 0u;
-      mbar_arrive(&info_empty[slot]);
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + a * 128;
+      float xa[32], xb[32];
+      tmem_ld32(taddr, xa);
+      const int tp = d.z, tbh = d.w;
       const long long t = ent >> 5;
       const int qslot = ent & 31;
       // keys of this tile that count for the query: [128p, n_eff)
       const long long n_eff = P.causal ? (t + 1 < P.N ? t + 1 : P.N) : P.N;
-      long long lim = qvalid ? n_eff - 128LL * bk.p : 128;
+      long long lim = qvalid ? n_eff - 128LL * tp : 128;
       if (lim > 128) lim = 128;
       if (lim < 1) lim = 1;
-      const int lim0 = lim < 64 ? (int)lim : 64;
-      const int lim1 = lim > 64 ? (int)lim - 64 : 0;
-      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + a * 128;
-      float x[64];
-      tmem_ld32(taddr, x);
-      tmem_ld32(taddr + 32, x + 32);
+      const int l = (int)lim;  // columns [0, l) count; chunk c holds columns [32c, 32c + 32)
+      const int c0 = min(l, 32), c1 = min(max(l - 32, 0), 32), c2 = min(max(l - 64, 0), 32),
+                c3 = max(l - 96, 0);
+      HalfLse h0, h1;
       tmem_ld_wait();
-      const bool full0 = __all_sync(kFull, lim0 == 64);
-      const float lse0 = half_lse(x, lim0, full0);
-      tmem_ld32(taddr + 64, x);
-      tmem_ld32(taddr + 96, x + 32);
+      reg_fence32(xa);
+      tmem_ld32(taddr + 32, xb);
+      h0.first(xa, c0, __all_sync(kFull, c0 == 32));
       tmem_ld_wait();
+      reg_fence32(xb);
+      tmem_ld32(taddr + 64, xa);
+      if (__any_sync(kFull, c1 > 0)) h0.add(xb, c1, __all_sync(kFull, c1 == 32));
+      tmem_ld_wait();
+      reg_fence32(xa);
+      tmem_ld32(taddr + 96, xb);
+      const bool any1 = __any_sync(kFull, c2 > 0);
+      if (any1) h1.first(xa, c2 > 0 ? c2 : 1, __all_sync(kFull, c2 == 32));
+      tmem_ld_wait();
+      reg_fence32(xb);
       tc_fence_before();
       mbar_arrive(&acc_empty[a]);
-      const bool any1 = __any_sync(kFull, lim1 > 0);
-      float lse1 = 0.f;
-      if (any1) {
-        const bool full1 = __all_sync(kFull, lim1 == 64);
-        lse1 = half_lse(x, lim1 > 0 ? lim1 : 1, full1);
-      }
+      if (any1 && __any_sync(kFull, c3 > 0)) h1.add(xb, c3, __all_sync(kFull, c3 == 32));
       const bool head = qvalid && h < G;
-      float v0 = head ? lse0 : 0.f, v1 = head ? lse1 : 0.f;
+      float v0 = head ? h0.value() : 0.f, v1 = (head && any1) ? h1.value() : 0.f;
       for (int o = Gp >> 1; o > 0; o >>= 1) {
         v0 += __shfl_xor_sync(kFull, v0, o);
         v1 += __shfl_xor_sync(kFull, v1, o);
       }
       if (qvalid && h == 0) {
-        float* out = P.leaf_scores + (((long long)bk.b * P.Hkv + bk.kv) * P.N + t) * (2 * P.K) + 2 * qslot;
+        float* out = P.leaf_scores + ((long long)tbh * P.N + t) * (2 * P.K) + 2 * qslot;
         out[0] = v0;
-        out[1] = lim1 > 0 ? v1 : -INFINITY;
+        out[1] = l > 64 ? v1 : -INFINITY;
       }
+    }
+  }
+  if (threadIdx.x == 0 && *abort) {
+    // after an abort, give copies still in flight into this CTA's shared memory time to land
+    const long long t0 = clock64();
+    while (clock64() - t0 < 4000000) {
     }
   }
   __syncthreads();
@@ -444,12 +441,16 @@ __global__ void __launch_bounds__(1024) leaf_scan_kernel(const int* __restrict__
   }
 }
 
-// tile_bkt[i] = bucket of tile i (the largest bucket whose first tile is <= i).
-__global__ void leaf_tile_map_kernel(const int* __restrict__ tile_off, int nb, long long max_tiles,
-                                     int* __restrict__ tile_bkt) {
+// Descriptor of leaf tile i: its bucket is the largest bucket whose first tile is
+// <= i; {first entry, rows, level-2 survivor p, b * Hkv + kv}.
+__global__ void leaf_tile_desc_kernel(const int* __restrict__ tile_off, const int* __restrict__ bucket_off, int nb,
+                                      long long max_tiles, int R, int M2, int nchunks, int4* __restrict__ desc) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= max_tiles || i >= tile_off[nb]) return;
-  tile_bkt[i] = find_bucket(tile_off, nb, (int)i);
+  const int bkt = find_bucket(tile_off, nb, (int)i);
+  const int e0 = bucket_off[bkt] + ((int)i - tile_off[bkt]) * R;
+  const int nrows = min(R, bucket_off[bkt + 1] - e0);
+  desc[i] = make_int4(e0, nrows, bkt % M2, bkt / M2 / nchunks);
 }
 
 // Final Top-K per (b, kv, t) over the leaf candidates (children of the level-2
@@ -554,8 +555,9 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
   leaf_scatter_kernel<<<eg, 256, 0, s>>>(L.surv, entries, L.K, L.N, L.nchunks, L.chunk_shift, L.M2, L.bucket_off,
                                          L.cursor, L.list);
   note_launch();
-  leaf_tile_map_kernel<<<(unsigned)((L.max_tiles + 255) / 256), 256, 0, s>>>(L.tile_off, L.nb, L.max_tiles,
-                                                                              L.tile_bkt);
+  leaf_tile_desc_kernel<<<(unsigned)((L.max_tiles + 255) / 256), 256, 0, s>>>(L.tile_off, L.bucket_off, L.nb,
+                                                                               L.max_tiles, R, L.M2, L.nchunks,
+                                                                               L.tile_desc);
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -575,7 +577,7 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
   P.list = L.list;
   P.bucket_off = L.bucket_off;
   P.tile_off = L.tile_off;
-  P.tile_bkt = L.tile_bkt;
+  P.tile_desc = L.tile_desc;
   P.nb = L.nb;
   P.Hkv = L.Hkv;
   P.G = G;

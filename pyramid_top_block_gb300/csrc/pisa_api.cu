@@ -81,14 +81,14 @@ int chunk_shift_for(long long N) {
 // Workspace of the prefill selection (every slice 256-byte aligned):
 //   [status 256 B][count nb][cursor nb]       zeroed at every call
 //   [bucket_off nb+1][tile_off nb+1]           scans of the bucket sizes
-//   [tile_bkt: max_tiles int32]                bucket of each leaf tile
+//   [tile_desc: max_tiles int4]                first entry, rows, p, b*Hkv+kv of each leaf tile
 //   [surv2: B*Hkv*N*K int32]                   level-2 survivors
 //   [list: B*Hkv*N*K uint32]                   (t << 5 | slot), bucket-sorted
 //   [leaf_scores: B*Hkv*N*2K fp32]
 //   [route table: B*Hkv*rows x 256 B]          per-node logit-step rows of the walk
 // with nb = B * Hkv * nchunks * M2 buckets (chunk of queries, level-2 node).
 struct PrefillWs {
-  size_t status, count, cursor, bucket_off, tile_off, tile_bkt, surv, list, leaf, table, total, zero_bytes;
+  size_t status, count, cursor, bucket_off, tile_off, tile_desc, surv, list, leaf, table, total, zero_bytes;
   long long max_tiles;
   long long nb;
   int nchunks, chunk_shift, M2;
@@ -116,8 +116,8 @@ PrefillWs prefill_layout(int B, long long N, int Hkv, int K) {
   o += align_up(sizeof(int) * (size_t)(w.nb + 1));
   // a tile holds R = 128 / max(G, 8) >= 8 queries: at most entries / 8 + nb tiles
   w.max_tiles = (long long)(entries / 8) + w.nb + 1;
-  w.tile_bkt = o;
-  o += align_up(sizeof(int) * (size_t)w.max_tiles);
+  w.tile_desc = o;
+  o += align_up(sizeof(int4) * (size_t)w.max_tiles);
   w.surv = o;
   o += align_up(sizeof(int32_t) * entries);
   w.list = o;
@@ -227,7 +227,7 @@ int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t 
   L.cursor = reinterpret_cast<int*>(base + w.cursor);
   L.bucket_off = reinterpret_cast<int*>(base + w.bucket_off);
   L.tile_off = reinterpret_cast<int*>(base + w.tile_off);
-  L.tile_bkt = reinterpret_cast<int*>(base + w.tile_bkt);
+  L.tile_desc = reinterpret_cast<int4*>(base + w.tile_desc);
   L.max_tiles = w.max_tiles;
   L.list = reinterpret_cast<uint32_t*>(base + w.list);
   L.leaf_scores = reinterpret_cast<float*>(base + w.leaf);

@@ -49,7 +49,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   for (int i = 0; i < kWaitPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 63 && *abort) return false;
+    if ((i & 63) == 63 && abort && *abort) return false;
   }
   return false;
 }

@@ -119,6 +119,15 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The same with a zero accumulator in.
+__device__ __forceinline__ void mma_bf16_16816_z(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 struct WalkSmem {  // per-warp views into dynamic shared memory
   int* cand;     // [2K] node ids of the current candidates (ascending)
   float* zs;     // [2K] head-summed logit Z of each candidate
@@ -440,11 +449,12 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
 
 // ---------------------------------------------------------------------------
 // Walk for K <= 8: every level has at most 16 candidates, one MMA tile, and the
-// whole walk stays in registers.  MMA row g holds candidate 2g and row g + 8
-// candidate 2g + 1; after the head sums lane (g, j) owns candidate 2g + (j & 1)
-// (lanes j and j ^ 2 hold identical copies), so the candidates of a level sit in
-// lane order 0, 1, 4, 5, 8, 9, ... and survivor positions are popcounts of
-// ballots.  Scores are base-2 logits (the rows carry log2(e)/sqrt(d)).
+// whole walk stays in registers.  MMA row m holds candidate m; after the head
+// sums lane (g, j) owns candidate g + 8 (j & 1) (lanes j and j ^ 2 hold
+// identical copies), and survivor positions are popcounts of ballots.  Rows g
+// and g + 1 of a quarter-warp's shared-memory loads are then usually two
+// siblings, adjacent rows, which the 272-byte row stride puts in disjoint
+// banks.  Scores are base-2 logits (the rows carry log2(e)/sqrt(d)).
 
 // The ragged last pair of children, per level l (children at level l - 1).
 struct LevelTail {
@@ -452,13 +462,10 @@ struct LevelTail {
   float nr[kMaxLevels + 2];  // -(n_second / n_first) for that parent
 };
 
-constexpr int kCandBuf = 64;  // per-warp 32-bit words: two buffers of 16 node ids + 16 Z
+constexpr int kCandBuf = 80;  // per-warp 32-bit words: two buffers of 16 node ids + 16 Z, 16 rank keys
 
-__device__ __forceinline__ void ld_row(const unsigned char* p, bool shared_src, bool valid, uint4& h0, uint4& h1,
-                                       uint4& l0, uint4& l1) {
-  const uint4 z = make_uint4(0, 0, 0, 0);
-  h0 = h1 = l0 = l1 = z;
-  if (!valid) return;
+__device__ __forceinline__ void ld_row(const unsigned char* p, bool shared_src, uint4& h0, uint4& h1, uint4& l0,
+                                       uint4& l1) {
   const uint4* v = reinterpret_cast<const uint4*>(p);
   if (shared_src) {
     h0 = v[0];
@@ -481,10 +488,6 @@ __device__ __forceinline__ void tile_dots(const uint32_t (&A)[4][4], const uint4
                                           float (&u)[NT][4]) {
   float dh[NT][4], dl[NT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) dh[nt][i] = dl[nt][i] = 0.f;
-#pragma unroll
   for (int ks = 0; ks < 4; ++ks) {
     const uint4& Ha = ra[ks >> 1];
     const uint4& La = ra[2 + (ks >> 1)];
@@ -495,8 +498,13 @@ __device__ __forceinline__ void tile_dots(const uint32_t (&A)[4][4], const uint4
     const uint32_t al[4] = {hw ? La.z : La.x, hw ? Lb.z : Lb.x, hw ? La.w : La.y, hw ? Lb.w : Lb.y};
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      mma_bf16_16816(dh[nt], ah, A[ks][nt], A[ks][nt + 2]);
-      mma_bf16_16816(dl[nt], al, A[ks][nt], A[ks][nt + 2]);
+      if (ks == 0) {
+        mma_bf16_16816_z(dh[nt], ah, A[ks][nt], A[ks][nt + 2]);
+        mma_bf16_16816_z(dl[nt], al, A[ks][nt], A[ks][nt + 2]);
+      } else {
+        mma_bf16_16816(dh[nt], ah, A[ks][nt], A[ks][nt + 2]);
+        mma_bf16_16816(dl[nt], al, A[ks][nt], A[ks][nt + 2]);
+      }
     }
   }
 #pragma unroll
@@ -524,7 +532,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
   extern __shared__ __align__(16) unsigned char wsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, j = lane & 3, s = j & 1;
-  const int oc = 2 * g + s;  // the candidate this lane owns after the head sums
+  const int oc = g + 8 * s;  // the candidate this lane owns after the head sums
   const int G = Hq / Hkv;
   const long long bh = blockIdx.y;
   const int kv = (int)(bh % Hkv);
@@ -554,7 +562,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
     pad[nt].y = (8 * nt + 2 * j + 1 < G) ? 0.f : -INFINITY;
   }
   const unsigned lt = (1u << lane) - 1u;
-  constexpr unsigned kPrimary = 0x33333333u;  // lanes with j < 2: one copy of each candidate
+  constexpr unsigned kLo = 0x11111111u, kHi = 0x22222222u;  // lanes owning candidates 0..7 / 8..15 (j = 0 / 1)
 
   for (int t = blockIdx.x + gridDim.x * warp; t < N; t += gridDim.x * kWalkWarps) {
     __syncwarp();  // the previous query's reads of the candidate buffers are done
@@ -594,8 +602,9 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
     float Z;
     {
       uint4 ra[4], rb[4];
-      ld_row(czr + (2 * g) * kCacheRowBytes + 32 * j, true, 2 * g < nC, ra[0], ra[1], ra[2], ra[3]);
-      ld_row(czr + (2 * g + 1) * kCacheRowBytes + 32 * j, true, 2 * g + 1 < nC, rb[0], rb[1], rb[2], rb[3]);
+      // (rows of candidates >= nC are loaded too; their results are never kept)
+      ld_row(czr + g * kCacheRowBytes + 32 * j, true, ra[0], ra[1], ra[2], ra[3]);
+      ld_row(czr + (g + 8) * kCacheRowBytes + 32 * j, true, rb[0], rb[1], rb[2], rb[3]);
       float u[NT][4];
       tile_dots<NT>(A, ra, rb, u);
       float sa = 0.f, sb = 0.f;
@@ -616,16 +625,18 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
       // rows of the two MMA-row candidates
       const int c_oth = __shfl_xor_sync(kFull, c, 1);
       const int na = s ? c_oth : c, nb = s ? c : c_oth;
-      const bool va = 2 * g < nC, vb = 2 * g + 1 < nC;
+      const bool va = g < nC, vb = g + 8 < nC;
+      // candidates >= nC read row 0 of the level (their results are never kept)
+      const int ra_row = va ? na : 0, rb_row = vb ? nb : 0;
       uint4 ra[4], rb[4];
       if (l >= l_lo) {
         const unsigned char* base = cdr + (ro.o[l] - crow0) * kCacheRowBytes + 32 * j;
-        ld_row(base + na * kCacheRowBytes, true, va, ra[0], ra[1], ra[2], ra[3]);
-        ld_row(base + nb * kCacheRowBytes, true, vb, rb[0], rb[1], rb[2], rb[3]);
+        ld_row(base + ra_row * kCacheRowBytes, true, ra[0], ra[1], ra[2], ra[3]);
+        ld_row(base + rb_row * kCacheRowBytes, true, rb[0], rb[1], rb[2], rb[3]);
       } else {
         const unsigned char* base = table + (bh * rows_per_bh + ro.o[l]) * kRowBytes + 32 * j;
-        ld_row(base + (long long)na * kRowBytes, false, va, ra[0], ra[1], ra[2], ra[3]);
-        ld_row(base + (long long)nb * kRowBytes, false, vb, rb[0], rb[1], rb[2], rb[3]);
+        ld_row(base + ra_row * kRowBytes, false, ra[0], ra[1], ra[2], ra[3]);
+        ld_row(base + rb_row * kRowBytes, false, rb[0], rb[1], rb[2], rb[3]);
       }
       float u[NT][4];
       tile_dots<NT>(A, ra, rb, u);
@@ -687,25 +698,26 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
         const unsigned fb = __float_as_uint(sc);
         unsigned key = fb ^ ((unsigned)((int)fb >> 31) | 0x80000000u);
         key = valid ? ((key & ~15u) | (unsigned)(15 - oc)) : 0u;
-        int rank = 0;
-        const int half = 16 * (j >> 1);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const unsigned o = __shfl_sync(kFull, key, half + 4 * (k >> 1) + (k & 1));
-          rank += o > key;
-        }
+        // rank = number of larger keys: lanes j < 2 count among candidates 0..7, j >= 2 among 8..15
+        unsigned* keys = reinterpret_cast<unsigned*>(cbuf) + 64;
+        if (j < 2) keys[oc] = key;
+        __syncwarp();
+        const uint4* kq = reinterpret_cast<const uint4*>(keys + 8 * (j >> 1));
+        const uint4 k0 = kq[0], k1 = kq[1];
+        int rank = (k0.x > key) + (k0.y > key) + (k0.z > key) + (k0.w > key) + (k1.x > key) + (k1.y > key) +
+                   (k1.z > key) + (k1.w > key);
         rank += __shfl_xor_sync(kFull, rank, 2);
         keep = valid && rank < K;
       }
-      const unsigned bk = __ballot_sync(kFull, keep) & kPrimary;
-      const unsigned b2 = __ballot_sync(kFull, keep && two) & kPrimary;
-      const int before = __popc(bk & lt);
+      // survivors before this candidate (in candidate order), and those with two children
+      const unsigned bk = __ballot_sync(kFull, keep), b2 = __ballot_sync(kFull, keep && two);
+      const int before = s ? __popc(bk & kLo) + __popc(bk & kHi & lt) : __popc(bk & kLo & lt);
       if (l == 2) {
         if (j < 2 && keep) {
           out[before] = c;
           atomicAdd(cnt + c, 1);
         }
-        const int nS = __popc(bk);
+        const int nS = __popc(bk & (kLo | kHi));
         if (lane < K && lane >= nS) out[lane] = -1;
         break;
       }
@@ -714,7 +726,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
         const float zr = Z + sum_u, zo = fmaf(nr, sum_u, Z);
         int* buf = cbuf + ((l & 1) << 5);
         if (j < 2 && keep) {
-          const int pos = before + __popc(b2 & lt);
+          const int pos = before + (s ? __popc(b2 & kLo) + __popc(b2 & kHi & lt) : __popc(b2 & kLo & lt));
           buf[pos] = 2 * c;
           buf[16 + pos] = __float_as_int(ref1 ? zo : zr);
           if (two) {
@@ -722,7 +734,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
             buf[16 + pos + 1] = __float_as_int(ref1 ? zr : zo);
           }
         }
-        nC = __popc(bk) + __popc(b2);
+        nC = __popc(bk & (kLo | kHi)) + __popc(b2 & (kLo | kHi));
         __syncwarp();
         if (oc < nC) {
           c = buf[oc];
