@@ -30,8 +30,10 @@
 
 namespace pisa {
 
-constexpr int kLeafStages = 6;    // query-row tiles in flight (16 KB each)
 constexpr int kAccBufs = 4;       // TMEM accumulators of 128 fp32 columns
+// Query-row stages (16 KB each), one per accumulator: the stage of tile k is free again
+// once tile k's MMAs have completed, which acc_full already signals.
+constexpr int kLeafStages = kAccBufs;
 constexpr int kLeafWarps = 16;    // key-block loader, MMA, 2 query-row warps, 3 epilogue warpgroups
 constexpr int kEpiGroups = 3;     // epilogue warpgroups (warps 4..15)
 // A warpgroup waits for tile k only after finishing tile k - kEpiGroups, so with
@@ -39,12 +41,14 @@ constexpr int kEpiGroups = 3;     // epilogue warpgroups (warps 4..15)
 // one phase behind (the MMA warp commits tiles in order).
 static_assert(kEpiGroups <= kAccBufs, "an epilogue warpgroup could run two accumulator phases ahead");
 constexpr int kTileBlock = 32;    // consecutive tiles handled by one CTA in a row
-// Query-row warp w loads tiles k = w (mod 2); with an even stage count the stage it
-// refills last held one of its own tiles, so its wait on a_empty is never two
+// Query-row warp w loads tiles k = w (mod 2) and, before refilling the stage of tile
+// k, waits on acc_full for tile k - kLeafStages; with an even stage count that tile
+// was its own, loaded after the previous phase completed, so the wait is never two
 // phases ahead.
 static_assert(kLeafStages % 2 == 0, "query-row warps alternate tiles");
 constexpr int kTileBytes = 128 * 128;  // 128 rows of 64 bf16
-constexpr size_t kLeafSmem = (size_t)(kLeafStages + 2) * kTileBytes + 1024;
+constexpr int kKeyBufs = 4;       // key blocks in flight (the loader runs up to 3 blocks ahead)
+constexpr size_t kLeafSmem = (size_t)(kLeafStages + kKeyBufs) * kTileBytes + 1024;
 
 struct LeafTcParams {
   const __nv_bfloat16* Q;
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   unsigned char* sA = sm;
   unsigned char* sB = sm + kLeafStages * kTileBytes;
-  __shared__ uint64_t a_full[kLeafStages], a_empty[kLeafStages], b_full[2], b_empty[2];
+  __shared__ uint64_t a_full[kLeafStages], b_full[kKeyBufs], b_empty[kKeyBufs];
   __shared__ uint64_t acc_full[kAccBufs], acc_empty[kAccBufs], mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -178,9 +182,8 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kLeafStages; ++s) {
       mbar_init(&a_full[s], 1);
-      mbar_init(&a_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kKeyBufs; ++s) {
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
     }
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
 
   if (warp <= 1) {
     // ---------------- warp 0 loads the key block (two sibling leaves, 128 keys) of every
-    // run of tiles with the same (b, kv, p) into a double buffer; warp 1 drives the tensor
+    // run of tiles with the same (b, kv, p) into a ring of kKeyBufs buffers; warp 1 drives the tensor
     // core.  Both read this CTA's tile descriptors 32 at a time and find the key-block
     // changes with a ballot.
     const bool mma = warp == 1;
@@ -228,8 +231,8 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
           const int p = __shfl_sync(kFull, d.z, src), bh = __shfl_sync(kFull, d.w, src);
           bool w = true;
           if (lane == 0) {
-            const int bb = nchg & 1;
-            if (nchg >= 2) w = mbar_wait(&b_empty[bb], ((nchg >> 1) - 1) & 1, abort);
+            const int bb = nchg % kKeyBufs;
+            if (nchg >= kKeyBufs) w = mbar_wait(&b_empty[bb], ((nchg / kKeyBufs) - 1) & 1, abort);
             if (w) {
               mbar_expect_tx(&b_full[bb], kTileBytes);
               tma_load_3d(sB + bb * kTileBytes, &kmap, 0, bh % P.Hkv, (int)((bh / P.Hkv) * P.n_cap + 128LL * p),
@@ -240,30 +243,32 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
           ++nchg;
         }
       } else {
-        for (int m = 0; m < n && ok; ++m, ++k) {
-          const int s = k % kLeafStages, a = k % kAccBufs;
-          bool w = true;
-          if (lane == 0) {
+        // lane 0 issues the block's tiles; the warp learns of an abort once per block
+        bool w = true;
+        if (lane == 0) {
+          for (int m = 0; m < n && w; ++m) {
+            const int kt = k + m;
+            const int s = kt % kLeafStages, a = kt % kAccBufs;
             if ((chg >> m) & 1) {
               if (nchg > 0) umma_commit(&b_empty[cur]);  // fires once the previous block's MMAs are done
-              cur = nchg & 1;
-              w = mbar_wait(&b_full[cur], (nchg >> 1) & 1, abort);
+              cur = nchg % kKeyBufs;
+              w = mbar_wait(&b_full[cur], (nchg / kKeyBufs) & 1, abort);
               ++nchg;
             }
-            w = w && mbar_wait(&a_full[s], (k / kLeafStages) & 1, abort);
-            w = w && (k < kAccBufs || mbar_wait(&acc_empty[a], ((k / kAccBufs) - 1) & 1, abort));
+            w = w && mbar_wait(&a_full[s], (kt / kLeafStages) & 1, abort);
+            w = w && (kt < kAccBufs || mbar_wait(&acc_empty[a], ((kt / kAccBufs) - 1) & 1, abort));
             if (w) {
               tc_fence_after();
               const uint64_t da = umma_desc_sw128(sA + s * kTileBytes);
               const uint64_t db = umma_desc_sw128(sB + cur * kTileBytes);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + a * 128, da + 2 * kk, db + 2 * kk, idesc, kk > 0);
-              umma_commit(&a_empty[s]);
-              umma_commit(&acc_full[a]);
+              umma_commit(&acc_full[a]);  // also frees the tile's query-row stage
             }
           }
-          ok = __shfl_sync(kFull, w, 0);
         }
+        k += n;
+        ok = __shfl_sync(kFull, w, 0);
       }
     }
     if (!ok && lane == 0) leaf_abort(abort, P.status);
@@ -291,7 +296,7 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
       const int s = k % kLeafStages;
       bool w = true;
       if (lane == 0) {
-        if (k >= kLeafStages) w = mbar_wait(&a_empty[s], ((k / kLeafStages) - 1) & 1, abort);
+        if (k >= kLeafStages) w = mbar_wait(&acc_full[s], ((k / kLeafStages) - 1) & 1, abort);
         if (w) mbar_expect_tx(&a_full[s], (uint32_t)(d.y * G * 128));
       }
       if (!__shfl_sync(kFull, w, 0)) {
