@@ -27,7 +27,7 @@ struct LeafTcLaunch {
   int M2, nchunks, chunk_shift, nb;
   const int32_t* surv;
   int* count;
-  int* cursor;
+  const int32_t* srank;  // rank of each survivor inside its bucket (from the walk)
   int* bucket_off;
   int* tile_off;
   int4* tile_desc;      // [max_tiles] {first entry, rows, level-2 survivor p, b * Hkv + kv}
@@ -50,6 +50,7 @@ struct WalkLaunch {
   int B, Hq, Hkv, K, causal;
   unsigned char* table;  // route table: B*Hkv*route_rows_per_bh(lv) rows of 256 bytes
   int32_t* surv;
+  int32_t* srank;  // rank of each survivor inside its bucket (the bucket count before it)
   int* count;
   int nchunks, chunk_shift, M2;
 };

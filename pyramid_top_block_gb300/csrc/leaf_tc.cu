@@ -397,52 +397,88 @@ __device__ __forceinline__ int bucket_of(long long job, int p, long long N, int 
 
 __global__ void leaf_scatter_kernel(const int32_t* __restrict__ surv, long long entries, int K, long long N,
                                     int nchunks, int chunk_shift, int M2, const int* __restrict__ bucket_off,
-                                    int* __restrict__ cursor, uint32_t* __restrict__ list) {
+                                    const int32_t* __restrict__ srank, uint32_t* __restrict__ list) {
   const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= entries) return;
   const int p = surv[e];
   if (p < 0) return;
   const long long job = e / K;
   const int bkt = bucket_of(job, p, N, nchunks, chunk_shift, M2);
-  const int pos = bucket_off[bkt] + atomicAdd(cursor + bkt, 1);
+  const int pos = bucket_off[bkt] + srank[e];
   list[pos] = ((uint32_t)(job % N) << 5) | (uint32_t)(e % K);
 }
 
 // Exclusive scans of the bucket sizes (entries) and of their tile counts
-// ceil(size / R), one CTA of 1024 threads, each owning a contiguous segment.
+// ceil(size / R).  One CTA of 1024 threads sweeps the buckets in tiles of 4096,
+// each thread four consecutive buckets (coalesced), warp shuffles and one shared
+// array for the in-tile scan, a running carry between tiles.
 __global__ void __launch_bounds__(1024) leaf_scan_kernel(const int* __restrict__ count, int nb, int R,
                                                           int* __restrict__ bucket_off, int* __restrict__ tile_off) {
-  __shared__ int se[1024], st[1024];
-  const int tid = threadIdx.x;
-  const int per = (nb + 1023) / 1024;
-  const int lo = min(nb, tid * per), hi = min(nb, lo + per);
-  int ce = 0, ct = 0;
-  for (int i = lo; i < hi; ++i) {
-    const int c = count[i];
-    ce += c;
-    ct += (c + R - 1) / R;
-  }
-  se[tid] = ce;
-  st[tid] = ct;
+  __shared__ int we[32], wt[32];
+  __shared__ int carry[2];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry[0] = carry[1] = 0;
   __syncthreads();
-  for (int o = 1; o < 1024; o <<= 1) {  // inclusive Hillis-Steele scan
-    const int ae = tid >= o ? se[tid - o] : 0, at = tid >= o ? st[tid - o] : 0;
+  for (int base = 0; base < nb; base += 4096) {
+    const int i = base + 4 * tid;
+    int c[4], t[4];
+    int se = 0, st = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      c[q] = i + q < nb ? count[i + q] : 0;
+      t[q] = (c[q] + R - 1) / R;
+      se += c[q];
+      st += t[q];
+    }
+    int ie = se, it = st;  // inclusive scan over the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int ve = __shfl_up_sync(kFull, ie, o), vt = __shfl_up_sync(kFull, it, o);
+      if (lane >= o) {
+        ie += ve;
+        it += vt;
+      }
+    }
+    if (lane == 31) {
+      we[warp] = ie;
+      wt[warp] = it;
+    }
     __syncthreads();
-    se[tid] += ae;
-    st[tid] += at;
+    if (warp == 0) {  // scan of the 32 warp totals
+      int xe = we[lane], xt = wt[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int ve = __shfl_up_sync(kFull, xe, o), vt = __shfl_up_sync(kFull, xt, o);
+        if (lane >= o) {
+          xe += ve;
+          xt += vt;
+        }
+      }
+      we[lane] = xe;
+      wt[lane] = xt;
+    }
+    __syncthreads();
+    int oe = carry[0] + (warp ? we[warp - 1] : 0) + ie - se;
+    int ot = carry[1] + (warp ? wt[warp - 1] : 0) + it - st;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (i + q < nb) {
+        bucket_off[i + q] = oe;
+        tile_off[i + q] = ot;
+      }
+      oe += c[q];
+      ot += t[q];
+    }
+    __syncthreads();
+    if (tid == 0) {
+      carry[0] += we[31];
+      carry[1] += wt[31];
+    }
     __syncthreads();
   }
-  int oe = se[tid] - ce, ot = st[tid] - ct;
-  for (int i = lo; i < hi; ++i) {
-    const int c = count[i];
-    bucket_off[i] = oe;
-    tile_off[i] = ot;
-    oe += c;
-    ot += (c + R - 1) / R;
-  }
-  if (tid == 1023) {
-    bucket_off[nb] = se[1023];
-    tile_off[nb] = st[1023];
+  if (tid == 0) {
+    bucket_off[nb] = carry[0];
+    tile_off[nb] = carry[1];
   }
 }
 
@@ -558,7 +594,7 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
   leaf_scan_kernel<<<1, 1024, 0, s>>>(L.count, L.nb, R, L.bucket_off, L.tile_off);
   note_launch();
   leaf_scatter_kernel<<<eg, 256, 0, s>>>(L.surv, entries, L.K, L.N, L.nchunks, L.chunk_shift, L.M2, L.bucket_off,
-                                         L.cursor, L.list);
+                                         L.srank, L.list);
   note_launch();
   leaf_tile_desc_kernel<<<(unsigned)((L.max_tiles + 255) / 256), 256, 0, s>>>(L.tile_off, L.bucket_off, L.nb,
                                                                                L.max_tiles, R, L.M2, L.nchunks,

@@ -79,16 +79,17 @@ int chunk_shift_for(long long N) {
 }
 
 // Workspace of the prefill selection (every slice 256-byte aligned):
-//   [status 256 B][count nb][cursor nb]       zeroed at every call
+//   [status 256 B][count nb]                  zeroed at every call
 //   [bucket_off nb+1][tile_off nb+1]           scans of the bucket sizes
 //   [tile_desc: max_tiles int4]                first entry, rows, p, b*Hkv+kv of each leaf tile
 //   [surv2: B*Hkv*N*K int32]                   level-2 survivors
+//   [srank: B*Hkv*N*K int32]                   rank of each survivor inside its bucket
 //   [list: B*Hkv*N*K uint32]                   (t << 5 | slot), bucket-sorted
 //   [leaf_scores: B*Hkv*N*2K fp32]
 //   [route table: B*Hkv*rows x 256 B]          per-node logit-step rows of the walk
 // with nb = B * Hkv * nchunks * M2 buckets (chunk of queries, level-2 node).
 struct PrefillWs {
-  size_t status, count, cursor, bucket_off, tile_off, tile_desc, surv, list, leaf, table, total, zero_bytes;
+  size_t status, count, srank, bucket_off, tile_off, tile_desc, surv, list, leaf, table, total, zero_bytes;
   long long max_tiles;
   long long nb;
   int nchunks, chunk_shift, M2;
@@ -106,8 +107,6 @@ PrefillWs prefill_layout(int B, long long N, int Hkv, int K) {
   o += align_up(kStatusBytes);
   w.count = o;
   o += sizeof(int) * (size_t)w.nb;
-  w.cursor = o;
-  o += sizeof(int) * (size_t)w.nb;
   w.zero_bytes = o;
   o = align_up(o);
   w.bucket_off = o;
@@ -119,6 +118,8 @@ PrefillWs prefill_layout(int B, long long N, int Hkv, int K) {
   w.tile_desc = o;
   o += align_up(sizeof(int4) * (size_t)w.max_tiles);
   w.surv = o;
+  o += align_up(sizeof(int32_t) * entries);
+  w.srank = o;
   o += align_up(sizeof(int32_t) * entries);
   w.list = o;
   o += align_up(sizeof(uint32_t) * entries);
@@ -201,6 +202,7 @@ int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t 
   W.causal = causal;
   W.table = reinterpret_cast<unsigned char*>(base + w.table);
   W.surv = surv;
+  W.srank = reinterpret_cast<int32_t*>(base + w.srank);
   W.count = reinterpret_cast<int*>(base + w.count);
   W.nchunks = w.nchunks;
   W.chunk_shift = w.chunk_shift;
@@ -224,7 +226,7 @@ int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t 
   L.nb = (int)w.nb;
   L.surv = surv;
   L.count = reinterpret_cast<int*>(base + w.count);
-  L.cursor = reinterpret_cast<int*>(base + w.cursor);
+  L.srank = reinterpret_cast<int32_t*>(base + w.srank);
   L.bucket_off = reinterpret_cast<int*>(base + w.bucket_off);
   L.tile_off = reinterpret_cast<int*>(base + w.tile_off);
   L.tile_desc = reinterpret_cast<int4*>(base + w.tile_desc);

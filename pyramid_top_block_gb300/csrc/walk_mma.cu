@@ -179,7 +179,8 @@ __device__ __forceinline__ Kids kids_of(int l, int c, int Mc, int n, int t, bool
 __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
     const __nv_bfloat16* __restrict__ Q, const float* __restrict__ summ, const unsigned char* __restrict__ table,
     Levels lv, RowOffsets ro, long long rows_per_bh, int N, int Hq, int Hkv, int K, int causal, int l_start,
-    int l_lo, int32_t* __restrict__ surv, int* __restrict__ count, int nchunks, int chunk_shift, int M2) {
+    int l_lo, int32_t* __restrict__ surv, int32_t* __restrict__ srank, int* __restrict__ count, int nchunks,
+    int chunk_shift, int M2) {
   extern __shared__ __align__(16) unsigned char wsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, j = lane & 3;
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
       int p = -1;
       if (lane < nS) p = S.cand[S.sel[lane]];
       out[lane] = p;
-      if (p >= 0) atomicAdd(count + ((bh * nchunks + (t >> chunk_shift)) * M2 + p), 1);
+      if (p >= 0) srank[job * K + lane] = atomicAdd(count + ((bh * nchunks + (t >> chunk_shift)) * M2 + p), 1);
     }
     __syncwarp();
   }
@@ -528,7 +529,8 @@ template <int NT>
 __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
     const __nv_bfloat16* __restrict__ Q, const unsigned char* __restrict__ table, Levels lv, RowOffsets ro,
     LevelTail tail, long long rows_per_bh, int N, int Hq, int Hkv, int K, int causal, int l_start, int l_lo,
-    int32_t* __restrict__ surv, int* __restrict__ count, int nchunks, int chunk_shift, int M2) {
+    int32_t* __restrict__ surv, int32_t* __restrict__ srank, int* __restrict__ count, int nchunks, int chunk_shift,
+    int M2) {
   extern __shared__ __align__(16) unsigned char wsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, j = lane & 3, s = j & 1;
@@ -568,6 +570,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
     __syncwarp();  // the previous query's reads of the candidate buffers are done
     const long long job = bh * N + t;
     int32_t* out = surv + job * K;
+    int32_t* rk = srank + job * K;  // a survivor's rank in its bucket: the count before it
     int* cnt = count + (bh * nchunks + (t >> chunk_shift)) * M2;
     if (l_start < 2) {
       // at most K nodes at level 2: every eligible level-2 node survives unscored
@@ -576,7 +579,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
       if (lane < K) {
         const int p = lane < el ? lane : -1;
         out[lane] = p;
-        if (p >= 0) atomicAdd(cnt + p, 1);
+        if (p >= 0) rk[lane] = atomicAdd(cnt + p, 1);
       }
       continue;
     }
@@ -715,7 +718,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
       if (l == 2) {
         if (j < 2 && keep) {
           out[before] = c;
-          atomicAdd(cnt + c, 1);
+          rk[before] = atomicAdd(cnt + c, 1);
         }
         const int nS = __popc(bk & (kLo | kHi));
         if (lane < K && lane >= nS) out[lane] = -1;
@@ -818,7 +821,8 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
       }
     }
     kern<<<grid, kWalkWarps * 32, smem, s>>>(W.Q, W.table, lv, ro, tail, rows, (int)W.N, W.Hq, W.Hkv, W.K, W.causal,
-                                              l_start, l_lo, W.surv, W.count, W.nchunks, W.chunk_shift, W.M2);
+                                              l_start, l_lo, W.surv, W.srank, W.count, W.nchunks, W.chunk_shift,
+                                              W.M2);
     note_launch();
     return cudaGetLastError();
   }
@@ -834,8 +838,8 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
     }
   }
   walk_mma_kernel<<<grid, kWalkWarps * 32, smem, s>>>(W.Q, W.summ, W.table, lv, ro, rows, (int)W.N, W.Hq, W.Hkv, W.K,
-                                                       W.causal, l_start, l_lo, W.surv, W.count, W.nchunks,
-                                                       W.chunk_shift, W.M2);
+                                                       W.causal, l_start, l_lo, W.surv, W.srank, W.count,
+                                                       W.nchunks, W.chunk_shift, W.M2);
   note_launch();
   return cudaGetLastError();
 }
