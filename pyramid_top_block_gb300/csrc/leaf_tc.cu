@@ -342,24 +342,24 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
       const int l = (int)lim;  // columns [0, l) count; chunk c holds columns [32c, 32c + 32)
       const int c0 = min(l, 32), c1 = min(max(l - 32, 0), 32), c2 = min(max(l - 64, 0), 32),
                 c3 = max(l - 96, 0);
+      // columns 0..63 (key half 0) first; columns 64..127 are loaded while half 0 is
+      // summed, and the accumulator is released as soon as they are in registers
       HalfLse h0, h1;
+      tmem_ld32(taddr + 32, xb);
       tmem_ld_wait();
       reg_fence32(xa);
-      tmem_ld32(taddr + 32, xb);
-      h0.first(xa, c0, __all_sync(kFull, c0 == 32));
-      tmem_ld_wait();
       reg_fence32(xb);
+      h0.first(xa, c0, __all_sync(kFull, c0 == 32));
       tmem_ld32(taddr + 64, xa);
       if (__any_sync(kFull, c1 > 0)) h0.add(xb, c1, __all_sync(kFull, c1 == 32));
+      tmem_ld32(taddr + 96, xb);
       tmem_ld_wait();
       reg_fence32(xa);
-      tmem_ld32(taddr + 96, xb);
-      const bool any1 = __any_sync(kFull, c2 > 0);
-      if (any1) h1.first(xa, c2 > 0 ? c2 : 1, __all_sync(kFull, c2 == 32));
-      tmem_ld_wait();
       reg_fence32(xb);
       tc_fence_before();
       mbar_arrive(&acc_empty[a]);
+      const bool any1 = __any_sync(kFull, c2 > 0);
+      if (any1) h1.first(xa, c2 > 0 ? c2 : 1, __all_sync(kFull, c2 == 32));
       if (any1 && __any_sync(kFull, c3 > 0)) h1.add(xb, c3, __all_sync(kFull, c3 == 32));
       const bool head = qvalid && h < G;
       float v0 = head ? h0.value() : 0.f, v1 = (head && any1) ? h1.value() : 0.f;
