@@ -33,6 +33,35 @@ METRIC = "selection ms/pass and query-rows/s at 32K–256K; % of roofline (1×GB
 UNIT = "query-rows/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# kernels that can dominate a pass, from one ncu capture of the workload named
+# (summaries under profiles/).  A figure is reported only while the kernel's
+# sources are byte-identical to the ones captured.
+KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
+                  "walk": ["walk_mma.cu", "tc.cuh", "common.cuh", "api.cuh"]}
+NCU_TRAFFIC = {
+    ("leaf", "latency-256k"): {"bytes": 1651877000 + 35289600, "src_sha1": "adb4ca081a19cc74d7aa5f88542363dc84fb0c38",
+                               "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
+    ("walk", "latency-256k"): {"bytes": 1077341000 + 35663104, "src_sha1": "be85c32c29e96b0b39838d8dc0912e8144da4509",
+                               "profile": "profiles/walk_k8_kernel_latency-256k.md"},
+}
+
+
+def source_sha1(kernel):
+    import hashlib
+    h = hashlib.sha1()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "pyramid_top_block_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(kernel, workload):
+    t = NCU_TRAFFIC.get((kernel, workload))
+    if t and t["src_sha1"] == source_sha1(kernel):
+        return t["bytes"]
+    return None
+
 
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -291,7 +320,7 @@ def run_ours(args):
     fl = alg["leaf_flops"] if dom == "leaf" else alg["inter_flops"]
     achieved = fl / (phase_ms[dom] / 1e3) / 1e12
     roof = {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
-            "frac": achieved / tf_peak, "traffic": None, "kernel": dom,
+            "frac": achieved / tf_peak, "traffic": ncu_traffic(dom, args.workload), "kernel": dom,
             "peak_source": f"{pk_kind} bf16 burst"}
     t_tensor = alg["flops"] / (tf_peak * 1e12) * 1e3
     t_hbm = alg["bytes"] / (pk["hbm_gbs"] * 1e9) * 1e3
