@@ -169,7 +169,7 @@ def dist_setup():
     return world, rank, local
 
 
-def oracle_rows_per_s(q, k, w, target_s: float):
+def oracle_rows_per_s(q, k, w, target_s: float, n_rows: int | None = None):
     """Time the fp64 oracle (as it stands, all host threads) on a bounded sample:
     its pyramid build over all N tokens, plus the walks of n query rows (all KV
     heads) spread evenly over the sequence.  A full pass is then
@@ -189,10 +189,15 @@ def oracle_rows_per_s(q, k, w, target_s: float):
         oracle.select(qr, kf, K=w["K"], t_list=t)
         return len(t), max(time.perf_counter() - t0 - t_build, 1e-9)
 
-    n0, s0 = run(16)
-    per = s0 / n0
-    n = int(max(16, min(N, (target_s - t_build) / max(per, 1e-9))))
-    n, secs = run(n)
+    # grow the sample until it takes about target_s (per-row cost from a small
+    # sample is inflated by fixed start-up costs)
+    budget = max(target_s - t_build, 0.2)
+    if n_rows:
+        n, secs = run(n_rows)
+    else:
+        n, secs = run(64)
+        while secs < 0.7 * budget and n < N:
+            n, secs = run(int(min(N, n * min(8.0, max(1.5, budget / secs)))))
     t_row = secs / (n * w["B"])
     t_full = t_build + w["B"] * N * t_row
     return dict(value=w["B"] * N / t_full, unit=UNIT, cores=oracle.max_threads(), kind="oracle",
@@ -211,8 +216,10 @@ def run_reference(args):
     vals = []
     info = None
     per_step = max(0.5, min(args.ref_step_s, 150.0 / (args.warmup + args.steps)))
+    n_rows = None
     for i in range(args.warmup + args.steps):
-        r = oracle_rows_per_s(q, k, w, target_s=per_step)
+        r = oracle_rows_per_s(q, k, w, target_s=per_step, n_rows=n_rows)
+        n_rows = r["rows"] // w["B"]  # the first step sizes the sample, the others reuse it
         if i >= args.warmup:
             vals.append(r["value"])
             info = r
