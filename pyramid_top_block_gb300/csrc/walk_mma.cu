@@ -546,8 +546,18 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
   unsigned char* czr = wsm;
   unsigned char* cdr = wsm + 16 * kCacheRowBytes;
   int* cbuf = reinterpret_cast<int*>(cdr + (size_t)ncache * kCacheRowBytes) + warp * kCandBuf;
+  // per level l: {row base (byte offset in the cache, or row index in the table), M_{l-1} - 1,
+  // ragged parent, -r of its children}
+  __shared__ int4 lvt[kMaxLevels + 2];
+  if (threadIdx.x >= 2 && threadIdx.x <= lv.L) {
+    const int l = threadIdx.x;
+    const bool cached = l >= l_lo && l <= l_start;
+    lvt[l] = make_int4(cached ? (int)((ro.o[l] - crow0) * kCacheRowBytes) : (int)ro.o[l], lv.M[l - 1] - 1,
+                       tail.node[l], __float_as_int(tail.nr[l]));
+  }
+  const unsigned char* tb = table + bh * rows_per_bh * kRowBytes;  // this (b, kv)'s table
   if (l_start >= 2) {
-    const unsigned char* src0 = table + bh * rows_per_bh * kRowBytes;
+    const unsigned char* src0 = tb;
     for (int e = threadIdx.x; e < 16 * 16; e += blockDim.x)
       *reinterpret_cast<uint4*>(czr + (e >> 4) * kCacheRowBytes + (e & 15) * 16) =
           __ldg(reinterpret_cast<const uint4*>(src0 + zrow0 * kRowBytes) + e);
@@ -621,10 +631,10 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
     }
     for (int l = l_start;; --l) {
       const bool scoring = nC > K;
-      const int Mc = lv.M[l - 1];
-      const int lim = causal ? min(Mc - 1, t >> (l + 4)) : Mc - 1;  // last eligible second child
-      const int rag = tail.node[l];
-      const float rnr = tail.nr[l];
+      const int4 lt4 = lvt[l];
+      const int lim = causal ? min(lt4.y, t >> (l + 4)) : lt4.y;  // last eligible second child
+      const int rag = lt4.z;
+      const float rnr = __int_as_float(lt4.w);
       // rows of the two MMA-row candidates
       const int c_oth = __shfl_xor_sync(kFull, c, 1);
       const int na = s ? c_oth : c, nb = s ? c : c_oth;
@@ -633,11 +643,11 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
       const int ra_row = va ? na : 0, rb_row = vb ? nb : 0;
       uint4 ra[4], rb[4];
       if (l >= l_lo) {
-        const unsigned char* base = cdr + (ro.o[l] - crow0) * kCacheRowBytes + 32 * j;
+        const unsigned char* base = cdr + lt4.x + 32 * j;
         ld_row(base + ra_row * kCacheRowBytes, true, ra[0], ra[1], ra[2], ra[3]);
         ld_row(base + rb_row * kCacheRowBytes, true, rb[0], rb[1], rb[2], rb[3]);
       } else {
-        const unsigned char* base = table + (bh * rows_per_bh + ro.o[l]) * kRowBytes + 32 * j;
+        const unsigned char* base = tb + (long long)lt4.x * kRowBytes + 32 * j;
         ld_row(base + ra_row * kRowBytes, false, ra[0], ra[1], ra[2], ra[3]);
         ld_row(base + rb_row * kRowBytes, false, rb[0], rb[1], rb[2], rb[3]);
       }
@@ -645,7 +655,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
       tile_dots<NT>(A, ra, rb, u);
       // per candidate of the pair: sum of u, sum of max(u, -r u), prod of (1 + 2^{-(1+r)|u|})
       float su[2], am[2], pr[2];
-      const bool any_rag = __any_sync(kFull, (va && na == rag) || (vb && nb == rag));
+      const bool any_rag = rag >= 0 && __any_sync(kFull, (va && na == rag) || (vb && nb == rag));
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         unsigned long long s2 = f2_pack(0.f, 0.f), m2 = s2, p2 = f2_pack(1.f, 1.f);
