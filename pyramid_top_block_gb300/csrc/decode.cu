@@ -1,0 +1,285 @@
+// decode.cu -- the decode step: append one key per sequence, refresh its leaf
+// and ancestor path, and walk the cached pyramid for the newest query.
+// "Block Sparse Attention with Log-Linear Complexity", §5.1 (decoding keeps the
+// mean pyramid cached and touches only the new token's path) and §3.2 / Scoring
+// / §4.1 for the walk.  fp32 arithmetic on the CUDA cores: bf16 inputs, fp32
+// summaries and accumulation.
+//
+// One CTA of kDecWarps warps per (b, kv).  Threads 0..63 update the path (one
+// feature each); then every level's candidates are scored one warp per candidate
+// (lanes = child x head for an intermediate node, lanes = keys for a leaf) and
+// warp 0 keeps the Top-K and expands the survivors.
+#include "api.cuh"
+#include "walk.cuh"
+
+namespace pisa {
+
+constexpr int kDecWarps = 16;
+constexpr int kQStride = kD + 4;  // padded row of the query heads in shared memory (conflict-free float4 reads)
+
+// Head-summed LSE score of candidate c at level l >= 2 over its children's
+// summaries; lane = (child lane >> 4, head lane & 15).  In decode the query is the
+// newest token, so every existing child is eligible.  Lanes 0..15 return it.
+template <int G>
+__device__ __forceinline__ float warp_node_score(const float* blk, const Levels& lv, int l, int c, const float* qs,
+                                                 int lane) {
+  const int ch = lane >> 4, h = lane & 15;
+  const long long node = 2LL * c + ch;
+  const bool two = 2LL * c + 1 < lv.M[l - 1];
+  float z = 0.f;
+  if (h < G && (ch == 0 || two)) {
+    const float4* r = reinterpret_cast<const float4*>(blk + (lv.off[l - 1] + node) * kD);
+    const float4* qv = reinterpret_cast<const float4*>(qs + h * kQStride);
+    float a = 0.f;
+#pragma unroll
+    for (int j = 0; j < kD / 4; ++j) {
+      const float4 k = r[j], q = qv[j];
+      a = fmaf(q.x, k.x, a);
+      a = fmaf(q.y, k.y, a);
+      a = fmaf(q.z, k.z, a);
+      a = fmaf(q.w, k.w, a);
+    }
+    z = a * kScale;
+  }
+  const float z1 = __shfl_xor_sync(kFull, z, 16);
+  float v = (ch == 0 && h < G) ? (two ? lse2(z, z1) : z) : 0.f;
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// Exact leaf score: sum over heads of log sum exp over the raw keys of leaf c
+// below n (all present keys); lane j holds keys 64c + j and 64c + j + 32.
+template <int G>
+__device__ __forceinline__ float warp_leaf_exact(const __nv_bfloat16* keys_b, int Hkv, int kv, long long c,
+                                                 long long n, const float* qs, int lane) {
+  float total = 0.f;
+  float z0[G], z1[G];
+  const long long r0 = c * kC + lane, r1 = r0 + 32;
+  const bool a0 = r0 < n, a1 = r1 < n;
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    const long long r = w ? r1 : r0;
+    float* z = w ? z1 : z0;
+    if (w ? a1 : a0) {
+      float k[kD];
+      const uint4* r4 = reinterpret_cast<const uint4*>(keys_b + (r * Hkv + kv) * kD);
+#pragma unroll
+      for (int j = 0; j < kD / 8; ++j) unpack8(r4[j], k + 8 * j);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float4* qv = reinterpret_cast<const float4*>(qs + h * kQStride);
+        float a = 0.f;
+#pragma unroll
+        for (int j = 0; j < kD / 4; ++j) {
+          const float4 q = qv[j];
+          a = fmaf(q.x, k[4 * j], a);
+          a = fmaf(q.y, k[4 * j + 1], a);
+          a = fmaf(q.z, k[4 * j + 2], a);
+          a = fmaf(q.w, k[4 * j + 3], a);
+        }
+        z[h] = a * kScale;
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float m = fmaxf(a0 ? z0[h] : -INFINITY, a1 ? z1[h] : -INFINITY);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    float e = (a0 ? expf(z0[h] - m) : 0.f) + (a1 ? expf(z1[h] - m) : 0.f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(kFull, e, o);
+    total += m + logf(e);
+  }
+  return total;
+}
+
+// One decode step for one (b, kv): append k_new at position p = lengths[b],
+// refresh the leaf mean and its ancestor path, then walk for the query at t = p
+// over the n = p + 1 tokens present.
+template <int G>
+__global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
+    const __nv_bfloat16* __restrict__ q_new, const __nv_bfloat16* __restrict__ k_new,
+    __nv_bfloat16* keys, float* summ, const int32_t* __restrict__ lengths, Levels cap_lv,
+    long long n_cap, int Hq, int Hkv, int K, int32_t* __restrict__ idx, float* __restrict__ scores,
+    int* status) {
+  __shared__ __align__(16) float qs[G * kQStride];
+  __shared__ float sib[kMaxLevels + 1][kD];  // siblings along the new token's path
+  __shared__ __align__(16) __nv_bfloat16 lk[kC * kD];  // the earlier keys of the new token's leaf
+  __shared__ WarpScratch ws;
+  __shared__ int nC_s;
+  const int b = blockIdx.x / Hkv, kv = blockIdx.x % Hkv;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long p = lengths[b];
+  int32_t* io = idx + (long long)blockIdx.x * K;
+  float* so = scores ? scores + (long long)blockIdx.x * K : nullptr;
+  if (p < 0 || p >= n_cap) {  // sequence full: leave it unchanged, report
+    if (tid == 0) set_status(status, PISA_ERR_DEVICE_BOUNDS);
+    if (tid < K) {
+      io[tid] = -1;
+      if (so) so[tid] = -INFINITY;
+    }
+    return;
+  }
+  const long long n = p + 1;
+  Levels lv;
+  lv.L = num_levels_for(n);
+  lv.total = cap_lv.total;
+  for (int l = 0; l <= lv.L; ++l) {
+    lv.M[l] = (int)level_size_for(n, l);
+    lv.off[l] = cap_lv.off[l];
+  }
+  __nv_bfloat16* keys_b = keys + (long long)b * n_cap * Hkv * kD;
+  float* blk = summ + ((long long)b * Hkv + kv) * cap_lv.total * kD;
+  const long long leaf = p >> kLog2C;
+  if (tid < kD) {
+    // siblings of the path nodes (levels 1..L-1), fetched together before the new token
+    // changes anything they depend on: none of them is on the path
+    const int e = tid;
+    long long i = leaf;
+    for (int l = 2; l <= lv.L; ++l) {
+      const long long s = i ^ 1;
+      sib[l][e] = s < lv.M[l - 1] ? blk[(lv.off[l - 1] + s) * kD + e] : 0.f;
+      i >>= 1;
+    }
+  } else if (tid >= 64 && tid < 64 + G * kD) {
+    for (int i = tid - 64; i < G * kD; i += kDecWarps * 32 - 64)
+      qs[(i / kD) * kQStride + (i % kD)] = bf2f(q_new[((long long)b * Hq + (long long)kv * G) * kD + i]);
+  }
+  {  // the leaf's earlier keys, 16 bytes per thread
+    const int nprev = (int)(p - leaf * kC);  // 0..63
+    for (int i = tid; i < nprev * (kD / 8); i += kDecWarps * 32) {
+      const int r = i / (kD / 8), v = i % (kD / 8);
+      reinterpret_cast<uint4*>(lk)[i] =
+          *reinterpret_cast<const uint4*>(keys_b + ((leaf * kC + r) * Hkv + kv) * kD + 8 * v);
+    }
+  }
+  __syncthreads();
+  if (tid < kD) {
+    // path update, feature e = tid: the leaf mean over its tokens in order, then the
+    // count-weighted merges up to the root (the same formula as the build)
+    const int e = tid;
+    const __nv_bfloat16 kn = k_new[((long long)b * Hkv + kv) * kD + e];
+    keys_b[(p * Hkv + kv) * kD + e] = kn;
+    float acc = 0.f;
+    for (int r = 0; r < (int)(p - leaf * kC); ++r) acc = __fadd_rn(acc, bf2f(lk[r * kD + e]));
+    acc = __fadd_rn(acc, bf2f(kn));
+    float m = __fdiv_rn(acc, (float)(p - leaf * kC + 1));
+    blk[(lv.off[1] + leaf) * kD + e] = m;
+    long long i = leaf;
+    for (int l = 2; l <= lv.L; ++l) {
+      const long long child = i;
+      i >>= 1;
+      const long long c0 = 2 * i, c1 = 2 * i + 1;
+      const int n0 = node_count(l - 1, c0, n);
+      const int n1 = c1 < lv.M[l - 1] ? node_count(l - 1, c1, n) : 0;
+      const float m0 = c0 == child ? m : sib[l][e];
+      const float m1 = n1 > 0 ? (c1 == child ? m : sib[l][e]) : 0.f;
+      m = merge_mean(m0, n0, m1, n1);
+      blk[(lv.off[l] + i) * kD + e] = m;
+    }
+  }
+  __threadfence_block();
+  __syncthreads();
+
+  // intermediate levels L-1 .. 2 (levels with at most K candidates are kept whole)
+  int nS = 1, myS = 0;  // survivors, held by warp 0 (lane j < nS holds the j-th)
+  for (int l = lv.L - 1; l >= 2; --l) {
+    if (warp == 0) {
+      const int nC = warp_expand(ws, nS, myS, l, lv.M[l], p, true, lane);
+      if (lane == 0) nC_s = nC;
+    }
+    __syncthreads();
+    const int nC = nC_s;
+    if (nC > K) {
+      for (int ci = warp; ci < nC; ci += kDecWarps) {
+        const float sc = warp_node_score<G>(blk, lv, l, ws.cand[ci], qs, lane);
+        if (lane == 0) ws.score[ci] = sc;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        warp_topk(ws, nC, K, lane);
+        nS = K;
+        myS = lane < K ? ws.next[lane] : 0;
+      }
+    } else if (warp == 0) {
+      nS = nC;
+      myS = lane < nC ? ws.cand[lane] : 0;
+    }
+    __syncthreads();
+  }
+  // leaves: children of the level-2 survivors, scored exactly when there are more
+  // than K of them or when scores are requested
+  if (warp == 0) {
+    const int nC = warp_expand(ws, nS, myS, 1, lv.M[1], p, true, lane);
+    if (lane == 0) nC_s = nC;
+  }
+  __syncthreads();
+  const int nC = nC_s;
+  if (nC > K || so != nullptr) {
+    for (int ci = warp; ci < nC; ci += kDecWarps) {
+      const float sc = warp_leaf_exact<G>(keys_b, Hkv, kv, ws.cand[ci], n, qs, lane);
+      if (lane == 0) ws.score[ci] = sc;
+    }
+    __syncthreads();
+  }
+  if (warp != 0) return;
+  int nOut;
+  if (nC > K) {
+    warp_topk(ws, nC, K, lane);
+    nOut = K;
+  } else {
+    if (lane < nC) ws.next[lane] = ws.cand[lane];
+    nOut = nC;
+    __syncwarp();
+  }
+  if (lane < K) {
+    const int lf = lane < nOut ? ws.next[lane] : -1;
+    io[lane] = lf;
+    if (so) {
+      float sc = -INFINITY;
+      for (int ci = 0; ci < nC; ++ci)
+        if (lf >= 0 && ws.cand[ci] == lf) sc = ws.score[ci];
+      so[lane] = sc;
+    }
+  }
+}
+
+__global__ void bump_lengths_kernel(int32_t* lengths, int B, long long n_cap) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B && lengths[b] >= 0 && lengths[b] < n_cap) lengths[b] += 1;
+}
+
+// ---------------------------------------------------------------- launchers
+
+template <int G>
+static cudaError_t launch_decode_G(const __nv_bfloat16* q_new, const __nv_bfloat16* k_new,
+                                   __nv_bfloat16* keys, float* summ, int32_t* lengths,
+                                   const Levels& cap_lv, long long n_cap, int B, int Hq, int Hkv,
+                                   int K, int32_t* idx, float* scores, int* status, cudaStream_t s) {
+  decode_kernel<G><<<B * Hkv, kDecWarps * 32, 0, s>>>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, Hq, Hkv,
+                                          K, idx, scores, status);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bump_lengths_kernel<<<(B + 127) / 128, 128, 0, s>>>(lengths, B, n_cap);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_warp(const __nv_bfloat16* q_new, const __nv_bfloat16* k_new,
+                               __nv_bfloat16* keys, float* summ, int32_t* lengths,
+                               const Levels& cap_lv, long long n_cap, int B, int Hq, int Hkv, int K,
+                               int32_t* idx, float* scores, int* status, cudaStream_t s) {
+  switch (Hq / Hkv) {
+    case 1: return launch_decode_G<1>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, s);
+    case 2: return launch_decode_G<2>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, s);
+    case 4: return launch_decode_G<4>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, s);
+    case 8: return launch_decode_G<8>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, s);
+    case 16: return launch_decode_G<16>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pisa
