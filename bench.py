@@ -96,10 +96,12 @@ def algorithmic(w):
     leaf_scored = min(sizes[0], g * K) > K
     leaf_flops = Hq * B * N * g * K * C * 2 * d if leaf_scored else 0
     inter_flops = Hq * B * N * scored_inter * g * K * g * 2 * d
+    exps = Hq * B * N * ((g * K * C if leaf_scored else 0) + scored_inter * g * K * g)
     pyr_bytes = B * Hkv * sum(sizes) * d * 4
     byts = B * N * Hq * d * 2 + B * N * Hkv * d * 2 + 2 * pyr_bytes + B * Hkv * N * K * 4
     return dict(flops=leaf_flops + inter_flops, leaf_flops=leaf_flops, inter_flops=inter_flops,
-                bytes=byts, scored_intermediate_levels=scored_inter, levels=L)
+                bytes=byts, scored_intermediate_levels=scored_inter, levels=L, exps=exps,
+                leaf_row_gather_bytes=B * Hkv * N * K * (Hq // Hkv) * d * 2)
 
 
 class Clocks:
@@ -160,6 +162,22 @@ class Clocks:
         return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
                 "reasons": sorted(reasons), "samples": len(rows),
                 "power_w_max": max(r["power"] for r in rows)}
+
+
+def max_over_ranks(x, dist, device):
+    """The slowest rank's value (every rank gets it)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(world, rows_per_rank, ms):
+    """Whole-job throughput: every rank processes rows_per_rank rows; the job takes
+    the slowest rank's ms."""
+    return world * rows_per_rank / (ms / 1000.0)
 
 
 def dist_setup():
@@ -310,13 +328,9 @@ def run_ours(args):
         dist.barrier()
     clk = clocks.stop() if clocks else None
     ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(n)]
-    total = sum(ms)
-    if dist:
-        t = torch.tensor([total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total = float(t.item())
+    total = max_over_ranks(sum(ms), dist, dev)
     ms_step = total / n
-    value = world * B * N / (ms_step / 1000.0)
+    value = job_rows_per_s(world, B * N, ms_step)
     phase_ms = {"build": statistics.mean(ev_s[i].elapsed_time(ev_b[i]) for i in range(n))}
     for j, name in enumerate(phases):
         phase_ms[name] = statistics.mean(pisa.event_elapsed_ms(ev_p[i][j], ev_p[i][j + 1]) for i in range(n))
@@ -331,6 +345,11 @@ def run_ours(args):
             "peak_source": f"{pk_kind} bf16 burst"}
     t_tensor = alg["flops"] / (tf_peak * 1e12) * 1e3
     t_hbm = alg["bytes"] / (pk["hbm_gbs"] * 1e9) * 1e3
+    ms_stats = {"mean": ms_step, "median": statistics.median(ms), "min": min(ms), "runs": n}
+    rates = {"query_rows_per_s": value, "kv_rows_per_s": value * Hkv, "head_rows_per_s": value * Hq}
+    work = {"exps": alg["exps"], "leaf_row_gather_bytes": alg["leaf_row_gather_bytes"],
+            "note": "north-star work model (non-causal upper bound); leaf_row_gather_bytes = query rows "
+                    "gathered once per (query, KV head, level-2 survivor)"}
     pass_roof = {"flops": alg["flops"], "min_bytes": alg["bytes"], "t_tensor_ms": t_tensor, "t_hbm_ms": t_hbm,
                  "t_roofline_ms": max(t_tensor, t_hbm), "frac": max(t_tensor, t_hbm) / ms_step,
                  "peaks": f"{pk_kind}: {tf_peak} TFLOP/s bf16 burst, {pk['hbm_gbs']} GB/s"}
@@ -360,12 +379,8 @@ def run_ours(args):
             idx_h.copy_(idx, non_blocking=True)
         ee.record(stream)
         torch.cuda.synchronize()
-        e_ms = es.elapsed_time(ee) / ne
-        if dist:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * B * N / (e_ms / 1e3), "unit": UNIT, "ms_per_step": e_ms,
+        e_ms = max_over_ranks(es.elapsed_time(ee) / ne, dist, dev)
+        e2e = {"value": job_rows_per_s(world, B * N, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "h2d_bytes_per_step": qh.numel() * 2 + kh.numel() * 2,
                "d2h_bytes_per_step": idx_h.numel() * 4}
 
@@ -383,7 +398,8 @@ def run_ours(args):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg(w, args),
-                "roofline": roof, "roofline_pass": pass_roof, "phases_ms": phase_ms,
+                "roofline": roof, "roofline_pass": pass_roof, "phases_ms": phase_ms, "ms_stats": ms_stats,
+                "rates": rates, "work": work,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
                 "device_status": device_status,
                 "decode": decode}

@@ -133,3 +133,17 @@ def test_decode_full_cache_reports_bounds():
     assert pisa.check_device_status(ws) == 6
     assert pyr.lengths.cpu().tolist() == [100, 100]
     assert (idx.cpu() == -1).all()
+
+
+@pytest.mark.parametrize("name,n_sample", [("latency-64k", 16384), ("latency-128k", 16384), ("latency-256k", 65536)])
+def test_latency_full_size_sampled(name, n_sample):
+    """Full-size passes (the benchmark's launch configuration) checked on a seeded
+    sample of query positions plus the last 1024, which the oracle walks one by one."""
+    q, k, w = synth.make(name)
+    _, idx, sc = _run_prefill(q, k, w["K"])
+    N = w["N"]
+    rng = np.random.default_rng(1234)
+    t = np.unique(np.concatenate([rng.choice(N - 1024, n_sample, replace=False), np.arange(N - 1024, N)]))
+    st = compare_prefill(idx[:, :, t], sc[:, :, t], _f32(q[:, t]), _f32(k), t, w["K"])
+    print(name, {a: b for a, b in st.items() if a != "messages"})
+    _assert_stats(st)
