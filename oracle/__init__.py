@@ -80,6 +80,9 @@ def _load():
         lib.pisa_oracle_leaf_scores.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, i32, i32,
                                                 vp, i64, i32, vp, vp, i32]
         lib.pisa_oracle_leaf_scores.restype = i32
+        lib.pisa_oracle_flat_select.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, i32, i32, i32,
+                                                vp, i64, vp, vp, vp, i32]
+        lib.pisa_oracle_flat_select.restype = i32
         lib.pisa_oracle_node_score.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, i64,
                                                i32, i64]
         lib.pisa_oracle_node_score.restype = dbl
@@ -175,6 +178,31 @@ def select_last(q_new, key_cache, lengths, K: int, C: int = 64, g: int = 2, thre
     if rc:
         raise ValueError("oracle select_last: bad arguments")
     return dict(idx=idx, scores=sc, min_gap=gap, n_scored=ns)
+
+
+def flat_select(q, keys, K: int, C: int = 64, g: int = 2, causal: bool = True, t_list=None,
+                threads: int = 0):
+    """Flat selection: every eligible leaf scored exactly, the K best kept
+    (ties to the lower index), ascending with -1 padding.
+
+    q: [B, n_t, Hq, d] rows of t_list (or all positions); keys: [B, N, Hkv, d].
+    Returns dict(idx [B,Hkv,n_t,K] int32, scores fp64, min_gap [B,Hkv,n_t], t)."""
+    k = _f32(keys)
+    B, N, Hkv, d = k.shape
+    Hq = q.shape[2]
+    t = np.arange(N, dtype=np.int64) if t_list is None else np.ascontiguousarray(t_list, dtype=np.int64)
+    qq = _f32(q)
+    if qq.shape[1] != len(t):
+        raise ValueError("q must hold one row per listed query position")
+    n_t = len(t)
+    idx = np.empty((B, Hkv, n_t, K), dtype=np.int32)
+    sc = np.empty((B, Hkv, n_t, K), dtype=np.float64)
+    gap = np.empty((B, Hkv, n_t), dtype=np.float64)
+    rc = _load().pisa_oracle_flat_select(_ptr(qq), _ptr(k), B, N, Hq, Hkv, d, C, g, K, int(causal),
+                                         _ptr(t), n_t, _ptr(idx), _ptr(sc), _ptr(gap), threads)
+    if rc:
+        raise ValueError("oracle flat_select: bad arguments")
+    return dict(idx=idx, scores=sc, min_gap=gap, t=t)
 
 
 def leaf_scores(q, keys, t_list, leaves, C: int = 64, g: int = 2, causal: bool = True,

@@ -384,6 +384,91 @@ int pisa_oracle_select(const float* q, const float* keys, int B, int64_t N, int 
 }
 
 /*
+ * Flat block selection, the conventional stage-1 baseline ([P1]: block-sparse
+ * attention such as BSA scores all N/C key blocks for every query): every
+ * eligible leaf gets the leaf score of ["Scoring: LogSumExp"] (exact raw-key
+ * LSE summed over the group's heads, keys after t masked when causal) and the K
+ * best are kept, ties to the lower index, listed ascending with -1 padding.
+ *   idx    : [B][Hkv][n_t][K], scores: [B][Hkv][n_t][K] (nullable)
+ *   min_gap: [B][Hkv][n_t] K-th best minus (K+1)-th best (+inf when at most K
+ *            leaves are eligible) (nullable)
+ */
+int pisa_oracle_flat_select(const float* q, const float* keys, int B, int64_t N, int Hq, int Hkv, int d,
+                            int C, int g, int K, int causal, const int64_t* t_list, int64_t n_t,
+                            int32_t* idx, double* scores, double* min_gap, int n_threads) {
+  oracle_levels lv;
+  if (B <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || K < 1 || levels_init(&lv, N, C, g)) return -1;
+  for (int64_t i = 0; i < n_t; ++i)
+    if (t_list[i] < 0 || t_list[i] >= N) return -1;
+  const int G = Hq / Hkv;
+  const int64_t M1 = lv.M[1];
+  const int64_t jobs = (int64_t)B * Hkv * n_t;
+  const int nt = resolve_threads(n_threads);
+#pragma omp parallel num_threads(nt)
+  {
+    double* cs = (double*)malloc(sizeof(double) * (size_t)M1);
+    char* taken = (char*)malloc((size_t)M1);
+    int64_t* best = (int64_t*)malloc(sizeof(int64_t) * (size_t)(K + 1));
+    double* work = (double*)malloc(sizeof(double) * (C > g ? C : g));
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t job = 0; job < jobs; ++job) {
+      int64_t it = job % n_t;
+      int kv = (int)((job / n_t) % Hkv);
+      int b = (int)(job / (n_t * Hkv));
+      walk_ctx w;
+      memset(&w, 0, sizeof(w));
+      w.q = q + ((int64_t)b * n_t + it) * Hq * d;
+      w.keys = keys;
+      w.lv = &lv;
+      w.n_cap = N;
+      w.b = b;
+      w.kv = kv;
+      w.Hkv = Hkv;
+      w.G = G;
+      w.d = d;
+      w.g = g;
+      w.causal = causal;
+      w.t = t_list[it];
+      w.scale = 1.0 / sqrt((double)d);
+      w.work = work;
+      int64_t nc = 0; /* eligible leaves are a prefix: 0 .. nc-1 */
+      while (nc < M1 && eligible(&w, 1, nc)) ++nc;
+      for (int64_t c = 0; c < nc; ++c) {
+        cs[c] = block_score(&w, 1, c);
+        taken[c] = 0;
+      }
+      /* the K+1 best by (score desc, index asc), one pass per rank */
+      int nb = 0;
+      for (; nb < K + 1 && nb < nc; ++nb) {
+        int64_t pick = -1;
+        for (int64_t c = 0; c < nc; ++c)
+          if (!taken[c] && (pick < 0 || better(cs[c], c, cs[pick], pick))) pick = c;
+        taken[pick] = 1;
+        best[nb] = pick;
+      }
+      int64_t o = ((int64_t)b * Hkv + kv) * n_t + it;
+      if (min_gap) min_gap[o] = nc > K ? cs[best[K - 1]] - cs[best[K]] : INFINITY;
+      int w_out = 0;
+      for (int64_t c = 0; c < nc && w_out < K; ++c)
+        if (taken[c] && (nc <= K || c != best[K])) {
+          idx[o * K + w_out] = (int32_t)c;
+          if (scores) scores[o * K + w_out] = cs[c];
+          ++w_out;
+        }
+      for (; w_out < K; ++w_out) {
+        idx[o * K + w_out] = -1;
+        if (scores) scores[o * K + w_out] = -INFINITY;
+      }
+    }
+    free(cs);
+    free(taken);
+    free(best);
+    free(work);
+  }
+  return 0;
+}
+
+/*
  * Decode selection ([P1] decoding keeps a cached mean pyramid and walks for the
  * one new query).  By definition it equals the prefill walk of the last query
  * over the keys present, so this routine rebuilds the pyramid over the first

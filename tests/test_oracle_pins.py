@@ -321,3 +321,67 @@ def test_candidates_per_level_bounded_and_output_well_formed():
             assert np.all(sel <= t // 64)
             assert len(sel) == min(K, t // 64 + 1)
             assert np.all(row[len(sel):] == -1)
+
+
+# ---------------------------------------------------------------- flat selection
+# The conventional baseline scores every eligible leaf ("PISA cuts block-sparse
+# attention selection ...": BSA scores all N/C blocks per query).
+
+def test_flat_equals_walk_when_every_leaf_reaches_the_leaf_level():
+    from pyramid_top_block_gb300 import synth
+    """M_2 <= K: the walk keeps every level-2 node, so every eligible leaf is scored
+    at level 1 and the walk's answer is the flat Top-K."""
+    q, k = synth.iid(1, 2048, 8, 2, seed=11)  # M_1 = 32, M_2 = 16
+    t = np.arange(0, 2048, 7)
+    qr = q[:, t].float().numpy()
+    kf = k.float().numpy()
+    walk = oracle.select(qr, kf, K=16, t_list=t)
+    flat = oracle.flat_select(qr, kf, K=16, t_list=t)
+    np.testing.assert_array_equal(walk["idx"], flat["idx"])
+    np.testing.assert_allclose(walk["scores"], flat["scores"], rtol=0, atol=0)
+
+
+def test_flat_matches_brute_force_logsumexp():
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(5)
+    B, N, Hkv, G, d, K = 1, 300, 2, 3, 64, 2
+    q = rng.standard_normal((B, N, Hkv * G, d)).astype(np.float32)
+    k = rng.standard_normal((B, N, Hkv, d)).astype(np.float32)
+    t = np.array([0, 63, 64, 130, 199, 255, 299])
+    got = oracle.flat_select(q[:, t], k, K=K, t_list=t)
+    for kv in range(Hkv):
+        for i, tt in enumerate(t):
+            n_leaves = tt // 64 + 1
+            sc = []
+            for c in range(n_leaves):
+                keys = k[0, c * 64:min((c + 1) * 64, tt + 1), kv].astype(np.float64)
+                s = 0.0
+                for h in range(G):
+                    qh = q[0, tt, kv * G + h].astype(np.float64)
+                    s += logsumexp(keys @ qh / 8.0)
+                sc.append(s)
+            order = sorted(range(n_leaves), key=lambda c: (-sc[c], c))[:K]
+            want = sorted(order) + [-1] * (K - len(order))
+            assert got["idx"][0, kv, i].tolist() == want
+            for j, c in enumerate(want):
+                if c >= 0:
+                    assert got["scores"][0, kv, i, j] == pytest.approx(sc[c], rel=1e-12, abs=1e-12)
+                else:
+                    assert got["scores"][0, kv, i, j] == -np.inf
+            if n_leaves > K:
+                s_sorted = sorted(sc, reverse=True)
+                assert got["min_gap"][0, kv, i] == pytest.approx(s_sorted[K - 1] - s_sorted[K], abs=1e-12)
+            else:
+                assert got["min_gap"][0, kv, i] == np.inf
+
+
+def test_flat_ties_go_to_the_lower_index():
+    """Constant keys: every full leaf has the same score; the K lowest full leaves win."""
+    B, N, Hkv, d = 1, 512, 1, 64
+    k = np.zeros((B, N, Hkv, d), np.float32)
+    k[..., 0] = 0.5
+    q = np.zeros((B, 1, 2, d), np.float32)
+    q[..., 0] = 8.0
+    got = oracle.flat_select(q, k, K=3, t_list=np.array([511]))
+    assert got["idx"][0, 0, 0].tolist() == [0, 1, 2]
+    assert got["min_gap"][0, 0, 0] == 0.0
