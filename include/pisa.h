@@ -118,6 +118,27 @@ int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t 
                         int causal, int32_t* idx, float* scores, void* ws, size_t ws_bytes,
                         void* stream);
 
+/* Workspace bytes pisa_select_flat needs (0 on bad or unsupported sizes).  It
+ * grows as N^2 / C: one fp32 score per (b, kv, query, leaf) plus the tile list. */
+size_t pisa_flat_workspace_bytes(int B, int64_t N, int Hq, int Hkv, int K);
+
+/*
+ * pisa_select_flat -- the flat block selector the pyramid walk replaces: "PISA
+ * cuts block-sparse attention selection to O(N log N) ..." (conventional
+ * block-sparse attention such as BSA scores all N/C key blocks per query).
+ * Every eligible leaf gets its exact leaf score ("Block Sparse Attention with
+ * Log-Linear Complexity", Scoring: LogSumExp: raw-key LSE summed over the
+ * group's heads, keys after t masked when causal) and the K best are kept
+ * (ties to the lower leaf index).  Arguments, layouts, ownership and errors as
+ * for pisa_select_prefill; only pyr->keys is read (the summaries are unused).
+ *   idx    : device int32 [B, Hkv, N, K] out: ascending, -1 padded
+ *   scores : device fp32 [B, Hkv, N, K] out (may be NULL), -inf padded
+ *   ws     : at least pisa_flat_workspace_bytes(...) bytes, 256-byte aligned
+ * PISA_ERR_UNSUPPORTED when the tile count reaches 2^31.
+ */
+int pisa_select_flat(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
+                     int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream);
+
 /* Workspace bytes pisa_decode_append_and_select needs (0 on bad sizes). */
 size_t pisa_decode_workspace_bytes(int B, int Hq, int Hkv, int K);
 

@@ -60,6 +60,10 @@ def load(path: str | None = None):
     lib.pisa_select_workspace_bytes.restype = sz
     lib.pisa_select_prefill.argtypes = [vp, i32, vp, i64, i32, i32, vp, vp, vp, sz, vp]
     lib.pisa_select_prefill.restype = i32
+    lib.pisa_flat_workspace_bytes.argtypes = [i32, i64, i32, i32, i32]
+    lib.pisa_flat_workspace_bytes.restype = sz
+    lib.pisa_select_flat.argtypes = [vp, i32, vp, i64, i32, i32, vp, vp, vp, sz, vp]
+    lib.pisa_select_flat.restype = i32
     lib.pisa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.pisa_decode_workspace_bytes.restype = sz
     lib.pisa_decode_append_and_select.argtypes = [vp, vp, i32, vp, i32, vp, vp, vp, sz, vp]
@@ -213,6 +217,37 @@ def select_prefill(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True, N
     _check(lib.pisa_select_prefill(_ptr(Q), Hq, ctypes.byref(st), N, K, int(causal), _ptr(idx),
                                    _ptr(scores), _ptr(workspace), workspace.numel(), _stream(stream)),
            "pisa_select_prefill")
+    return idx, scores
+
+
+def flat_workspace_bytes(B: int, N: int, Hq: int, Hkv: int, K: int) -> int:
+    return int(load().pisa_flat_workspace_bytes(B, N, Hq, Hkv, K))
+
+
+def select_flat(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True, N: int | None = None,
+                with_scores: bool = True, workspace: torch.Tensor | None = None,
+                out: tuple | None = None, stream=None):
+    """Flat selection: every eligible leaf scored exactly, the K best kept.
+    Same arguments and outputs as select_prefill (only pyr.keys is read)."""
+    if Q.dtype != torch.bfloat16 or not Q.is_cuda or Q.dim() != 4:
+        raise ValueError("Q must be a CUDA bf16 tensor [B, N, Hq, d]")
+    B, NQ, Hq, _ = Q.shape
+    N = NQ if N is None else N
+    lib = load()
+    if workspace is None:
+        need = lib.pisa_flat_workspace_bytes(B, N, Hq, pyr.Hkv, K)
+        if need == 0:
+            _check(2, "pisa_flat_workspace_bytes")
+        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    if out is None:
+        idx = torch.empty(B, pyr.Hkv, N, K, dtype=torch.int32, device=Q.device)
+        scores = torch.empty(B, pyr.Hkv, N, K, dtype=torch.float32, device=Q.device) if with_scores else None
+    else:
+        idx, scores = out
+    st = pyr.struct()
+    _check(lib.pisa_select_flat(_ptr(Q), Hq, ctypes.byref(st), N, K, int(causal), _ptr(idx), _ptr(scores),
+                                _ptr(workspace), workspace.numel(), _stream(stream)),
+           "pisa_select_flat")
     return idx, scores
 
 

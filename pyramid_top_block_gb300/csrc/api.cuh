@@ -40,6 +40,12 @@ struct LeafTcLaunch {
 };
 
 cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s);
+cudaError_t launch_leaf_tc_kernel(const LeafTcLaunch& L, int flat, long long flat_stride, cudaStream_t s);
+
+// The flat selector (flat.cu): L.list, L.tile_desc and L.leaf_scores are its
+// workspace slices; T1 tiles per (b, kv); stride = floats per (b, kv, t) score row.
+cudaError_t launch_select_flat(const LeafTcLaunch& L, long long T1, long long stride, int* total, cudaStream_t s);
+long long flat_tiles_per_bh(long long N, int G, int K, bool causal);
 
 // The intermediate levels of the prefill walk (walk_mma.cu).
 struct WalkLaunch {

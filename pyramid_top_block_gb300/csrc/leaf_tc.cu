@@ -63,6 +63,10 @@ struct LeafTcParams {
   int causal;
   float* leaf_scores;
   int* status;
+  // flat mode: every query row of a tile is scored against the tile's key block and the two
+  // leaf scores go to leaf_scores[(b * Hkv + kv) * N + t][2p, 2p + 1] (row stride flat_stride)
+  int flat;
+  long long flat_stride;
 };
 
 // Global index of this CTA's k-th tile: blocks of kTileBlock consecutive tiles,
@@ -368,7 +372,8 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
         v1 += __shfl_xor_sync(kFull, v1, o);
       }
       if (qvalid && h == 0) {
-        float* out = P.leaf_scores + ((long long)tbh * P.N + t) * (2 * P.K) + 2 * qslot;
+        float* out = P.flat ? P.leaf_scores + ((long long)tbh * P.N + t) * P.flat_stride + 2 * tp
+                            : P.leaf_scores + ((long long)tbh * P.N + t) * (2 * P.K) + 2 * qslot;
         out[0] = v0;
         out[1] = l > 64 ? v1 : -INFINITY;
       }
@@ -584,26 +589,12 @@ int sm_count() {
 
 }  // namespace
 
-cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
-  const long long entries = (long long)L.B * L.Hkv * L.N * L.K;
+// The persistent leaf kernel over the tiles described by L.tile_desc (their count is
+// L.tile_off[L.nb]); flat != 0 selects the flat output layout.
+cudaError_t launch_leaf_tc_kernel(const LeafTcLaunch& L, int flat, long long flat_stride, cudaStream_t s) {
   const int G = L.Hq / L.Hkv;
   const int Gp = G < 8 ? 8 : G;
   const int R = 128 / Gp;
-  const unsigned eg = (unsigned)((entries + 255) / 256);
-  // bucket sizes were counted by the walk kernel as it wrote the survivors
-  leaf_scan_kernel<<<1, 1024, 0, s>>>(L.count, L.nb, R, L.bucket_off, L.tile_off);
-  note_launch();
-  leaf_scatter_kernel<<<eg, 256, 0, s>>>(L.surv, entries, L.K, L.N, L.nchunks, L.chunk_shift, L.M2, L.bucket_off,
-                                         L.srank, L.list);
-  note_launch();
-  leaf_tile_desc_kernel<<<(unsigned)((L.max_tiles + 255) / 256), 256, 0, s>>>(L.tile_off, L.bucket_off, L.nb,
-                                                                               L.max_tiles, R, L.M2, L.nchunks,
-                                                                               L.tile_desc);
-  note_launch();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  mark_phase(3, s);
-
   CUtensorMap qmap, kmap;
   if (!make_map(&qmap, L.Q, (long long)L.B * L.N, L.Hq, G, 1) ||
       !make_map(&kmap, L.keys, (long long)L.B * L.n_cap, L.Hkv, 1, 128))
@@ -613,6 +604,8 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
     cudaFuncSetAttribute(leaf_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLeafSmem);
   });
   LeafTcParams P;
+  P.flat = flat;
+  P.flat_stride = flat_stride;
   P.Q = L.Q;
   P.Hq = L.Hq;
   P.list = L.list;
@@ -634,7 +627,30 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
   P.status = L.status;
   leaf_tc_kernel<<<sm_count(), kLeafWarps * 32, kLeafSmem, s>>>(qmap, kmap, P);
   note_launch();
-  e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
+  const long long entries = (long long)L.B * L.Hkv * L.N * L.K;
+  const int G = L.Hq / L.Hkv;
+  const int Gp = G < 8 ? 8 : G;
+  const int R = 128 / Gp;
+  const unsigned eg = (unsigned)((entries + 255) / 256);
+  // bucket sizes were counted by the walk kernel as it wrote the survivors
+  leaf_scan_kernel<<<1, 1024, 0, s>>>(L.count, L.nb, R, L.bucket_off, L.tile_off);
+  note_launch();
+  leaf_scatter_kernel<<<eg, 256, 0, s>>>(L.surv, entries, L.K, L.N, L.nchunks, L.chunk_shift, L.M2, L.bucket_off,
+                                         L.srank, L.list);
+  note_launch();
+  leaf_tile_desc_kernel<<<(unsigned)((L.max_tiles + 255) / 256), 256, 0, s>>>(L.tile_off, L.bucket_off, L.nb,
+                                                                               L.max_tiles, R, L.M2, L.nchunks,
+                                                                               L.tile_desc);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mark_phase(3, s);
+
+  e = launch_leaf_tc_kernel(L, 0, 0, s);
   if (e != cudaSuccess) return e;
   mark_phase(4, s);
   const long long jobs = (long long)L.B * L.Hkv * L.N;

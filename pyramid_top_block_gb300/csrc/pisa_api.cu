@@ -131,6 +131,33 @@ PrefillWs prefill_layout(int B, long long N, int Hkv, int K) {
   return w;
 }
 
+// Workspace of the flat selector: [status 256 B][tile count 256 B][list N uint32]
+// [tile_desc T int4][leaf scores B*Hkv*N*2*M2 fp32], T = B*Hkv*T1 tiles.
+struct FlatWs {
+  size_t status, total, list, desc, leaf, size;
+  long long T1, T, stride;
+};
+
+FlatWs flat_layout(int B, long long N, int Hq, int Hkv, int K, bool causal) {
+  FlatWs w;
+  w.T1 = flat_tiles_per_bh(N, Hq / Hkv, K, causal);
+  w.T = w.T1 * B * Hkv;
+  w.stride = 2 * level_size_for(N, 2);
+  size_t o = 0;
+  w.status = o;
+  o += align_up(kStatusBytes);
+  w.total = o;
+  o += align_up(sizeof(int));
+  w.list = o;
+  o += align_up(sizeof(uint32_t) * (size_t)N);
+  w.desc = o;
+  o += align_up(sizeof(int4) * (size_t)w.T);
+  w.leaf = o;
+  o += align_up(sizeof(float) * (size_t)B * Hkv * (size_t)N * (size_t)w.stride);
+  w.size = o;
+  return w;
+}
+
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PISA_OK : PISA_ERR_CUDA; }
 
 }  // namespace
@@ -237,6 +264,49 @@ int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t 
   L.scores = scores;
   L.status = reinterpret_cast<int*>(base + w.status);
   return cuda_status(launch_prefill_leaf_tc(L, s));
+}
+
+size_t pisa_flat_workspace_bytes(int B, int64_t N, int Hq, int Hkv, int K) {
+  if (check_geometry(B, N, Hq, Hkv, kD, kC, 2, K) != PISA_OK) return 0;
+  const FlatWs w = flat_layout(B, N, Hq, Hkv, K, true);
+  if (w.T >= (1LL << 31)) return 0;
+  return flat_layout(B, N, Hq, Hkv, K, false).size;  // the non-causal layout is the larger
+}
+
+int pisa_select_flat(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
+                     int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream) {
+  int st = check_pyr(pyr);
+  if (st) return st;
+  if (!Q || !idx || !ws) return PISA_ERR_INVALID_ARG;
+  st = check_geometry(pyr->B, N, Hq, pyr->Hkv, pyr->d, pyr->C, pyr->g, K);
+  if (st) return st;
+  if (N > pyr->n_cap) return PISA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(Q) & 15) || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)))
+    return PISA_ERR_INVALID_ARG;
+  const FlatWs w = flat_layout(pyr->B, N, Hq, pyr->Hkv, K, causal != 0);
+  if (w.T >= (1LL << 31) || (long long)pyr->B * pyr->n_cap >= (1LL << 31)) return PISA_ERR_UNSUPPORTED;
+  if (ws_bytes < w.size) return PISA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws);
+  if (cudaMemsetAsync(base, 0, kStatusBytes, s) != cudaSuccess) return PISA_ERR_CUDA;
+  LeafTcLaunch L{};
+  L.Q = static_cast<const __nv_bfloat16*>(Q);
+  L.keys = static_cast<const __nv_bfloat16*>(pyr->keys);
+  L.B = pyr->B;
+  L.Hq = Hq;
+  L.Hkv = pyr->Hkv;
+  L.K = K;
+  L.causal = causal != 0;
+  L.N = N;
+  L.n_cap = pyr->n_cap;
+  L.M2 = (int)level_size_for(N, 2);
+  L.list = reinterpret_cast<uint32_t*>(base + w.list);
+  L.tile_desc = reinterpret_cast<int4*>(base + w.desc);
+  L.leaf_scores = reinterpret_cast<float*>(base + w.leaf);
+  L.idx = idx;
+  L.scores = scores;
+  L.status = reinterpret_cast<int*>(base + w.status);
+  return cuda_status(launch_select_flat(L, w.T1, w.stride, reinterpret_cast<int*>(base + w.total), s));
 }
 
 size_t pisa_decode_workspace_bytes(int B, int Hq, int Hkv, int K) {

@@ -34,6 +34,13 @@ def compare_prefill(gpu_idx, gpu_scores, q_rows, keys, t_list, K, causal=True):
     return _compare(gpu_idx, gpu_scores, orc, q_rows, keys, t_list, K, causal)
 
 
+def compare_flat(gpu_idx, gpu_scores, q_rows, keys, t_list, K, causal=True):
+    """The flat selector against the oracle's flat selection (same rules; the
+    near-tie gap is the oracle's K-th minus (K+1)-th leaf score)."""
+    orc = oracle.flat_select(q_rows, keys, K=K, causal=causal, t_list=t_list)
+    return _compare(gpu_idx, gpu_scores, orc, q_rows, keys, t_list, K, causal)
+
+
 def _compare(gpu_idx, gpu_scores, orc, q_rows, keys, t_list, K, causal):
     oi, osc, gap = orc["idx"], orc["scores"], orc["min_gap"]
     same = np.all(gpu_idx == oi, axis=-1)  # [B, Hkv, n_t]
