@@ -388,6 +388,10 @@ def run_ours(args):
     if not args.no_decode and rank == 0:
         decode = bench_decode(torch, pisa, synth, dev, args)
 
+    flat = None
+    if args.flat and rank == 0:
+        flat = [bench_flat(torch, pisa, synth, dev, name) for name in args.flat.split(",")]
+
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         cpu = oracle_rows_per_s(q, k, w, target_s=args.cpu_s)
@@ -402,11 +406,59 @@ def run_ours(args):
                 "rates": rates, "work": work,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
                 "device_status": device_status,
-                "decode": decode}
+                "decode": decode, "flat": flat}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
     return 0
+
+
+def bench_flat(torch, pisa, synth, dev, name, runs=5):
+    """The flat selector (every eligible leaf scored exactly, the conventional
+    baseline) against the pyramid pass on the same workload: ms per selection
+    (build included for the pyramid), and the synthetic Recall@K of the pyramid's
+    blocks in the flat selector's, over query positions with more than K eligible
+    leaves (random inputs: not the pages' full-attention diagnostic)."""
+    q, k, w = synth.make(name)
+    B, N, Hq, Hkv, K = w["B"], w["N"], w["Hq"], w["Hkv"], w["K"]
+    qd, kd = q.to(dev), k.to(dev)
+    del q, k
+    pyr = pisa.Pyramid.allocate(kd)
+    ws = torch.empty(pisa.select_workspace_bytes(B, N, Hq, Hkv, K), dtype=torch.uint8, device=dev)
+    wf = torch.empty(pisa.flat_workspace_bytes(B, N, Hq, Hkv, K), dtype=torch.uint8, device=dev)
+    ip = torch.empty(B, Hkv, N, K, dtype=torch.int32, device=dev)
+    iflat = torch.empty_like(ip)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        out = []
+        for i in range(runs + 2):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                out.append(a.elapsed_time(b))
+        return statistics.median(out)
+
+    def pyr_pass():
+        pisa.build_pyramid(pyr)
+        pisa.select_prefill(qd, pyr, K, workspace=ws, out=(ip, None), with_scores=False)
+
+    t_pyr = timed(pyr_pass)
+    t_flat = timed(lambda: pisa.select_flat(qd, pyr, K, workspace=wf, out=(iflat, None), with_scores=False))
+    st = pisa.check_device_status(wf)
+    a, b = ip.cpu(), iflat.cpu()
+    t = torch.arange(N)
+    rows = (t // 64 + 1) > K  # more than K eligible leaves
+    hit = (a.unsqueeze(-1) == b.unsqueeze(-2)) & (a.unsqueeze(-1) >= 0)
+    recall = hit.any(-1).sum(-1).float() / K  # [B, Hkv, N]
+    return {"workload": name, "N": N, "K": K, "pyramid_ms": t_pyr, "flat_ms": t_flat,
+            "flat_over_pyramid": t_flat / t_pyr, "recall_at_k": float(recall[:, :, rows].mean()),
+            "recall_rows": int(rows.sum()) * B * Hkv, "status": st}
 
 
 def bench_decode(torch, pisa, synth, dev, args):
@@ -450,6 +502,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flat", default="latency-32k",
+                    help="comma-separated workloads for the flat-selector comparison ('' to skip)")
     ap.add_argument("--cpu-s", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=6.0, help="seconds of oracle work per reference step")
     ap.add_argument("--decode-steps", type=int, default=256)
