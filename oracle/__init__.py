@@ -72,19 +72,19 @@ def _load():
         lib.pisa_oracle_build_pyramid.argtypes = [vp, i32, i64, i64, i32, i32, i32, i32, i32, vp]
         lib.pisa_oracle_build_pyramid.restype = i32
         lib.pisa_oracle_select.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, i32, i32, i32,
-                                           vp, i64, vp, vp, vp, vp, i32]
+                                           vp, i64, vp, vp, vp, vp, i32, i32]
         lib.pisa_oracle_select.restype = i32
         lib.pisa_oracle_select_last.argtypes = [vp, vp, i32, i64, vp, i32, i32, i32, i32, i32, i32,
                                                 vp, vp, vp, vp, i32]
         lib.pisa_oracle_select_last.restype = i32
         lib.pisa_oracle_leaf_scores.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, i32, i32,
-                                                vp, i64, i32, vp, vp, i32]
+                                                vp, i64, i32, vp, vp, i32, i32]
         lib.pisa_oracle_leaf_scores.restype = i32
         lib.pisa_oracle_flat_select.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, i32, i32, i32,
-                                                vp, i64, vp, vp, vp, i32]
+                                                vp, i64, vp, vp, vp, i32, i32]
         lib.pisa_oracle_flat_select.restype = i32
         lib.pisa_oracle_node_score.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, i64,
-                                               i32, i64]
+                                               i32, i64, i32]
         lib.pisa_oracle_node_score.restype = dbl
         _lib = lib
         return lib
@@ -130,8 +130,9 @@ def build_pyramid(keys, n: int | None = None, C: int = 64, g: int = 2, recursive
 
 
 def select(q, keys, K: int, C: int = 64, g: int = 2, causal: bool = True, t_list=None,
-           threads: int = 0):
-    """Prefill selection.
+           threads: int = 0, mode: int = 0):
+    """Prefill selection.  mode: block score, 0 = LSE (PISA), 1 = mean of the
+    child logits (PISA-1), 2 = mean plus half their variance (PISA-2).
 
     q: [B, N, Hq, d] (all positions) or [B, len(t_list), Hq, d] (rows of t_list).
     keys: [B, N, Hkv, d].  Returns dict(idx [B,Hkv,n_t,K] int32, scores fp64,
@@ -153,7 +154,7 @@ def select(q, keys, K: int, C: int = 64, g: int = 2, causal: bool = True, t_list
     gap = np.empty((B, Hkv, n_t), dtype=np.float64)
     ns = np.empty((B, Hkv, n_t), dtype=np.int32)
     rc = _load().pisa_oracle_select(_ptr(qq), _ptr(k), B, N, Hq, Hkv, d, C, g, K, int(causal),
-                                    _ptr(t), n_t, _ptr(idx), _ptr(sc), _ptr(gap), _ptr(ns), threads)
+                                    _ptr(t), n_t, _ptr(idx), _ptr(sc), _ptr(gap), _ptr(ns), threads, mode)
     if rc:
         raise ValueError("oracle select: bad arguments")
     return dict(idx=idx, scores=sc, min_gap=gap, n_scored=ns, t=t)
@@ -181,7 +182,7 @@ def select_last(q_new, key_cache, lengths, K: int, C: int = 64, g: int = 2, thre
 
 
 def flat_select(q, keys, K: int, C: int = 64, g: int = 2, causal: bool = True, t_list=None,
-                threads: int = 0):
+                threads: int = 0, mode: int = 0):
     """Flat selection: every eligible leaf scored exactly, the K best kept
     (ties to the lower index), ascending with -1 padding.
 
@@ -199,14 +200,14 @@ def flat_select(q, keys, K: int, C: int = 64, g: int = 2, causal: bool = True, t
     sc = np.empty((B, Hkv, n_t, K), dtype=np.float64)
     gap = np.empty((B, Hkv, n_t), dtype=np.float64)
     rc = _load().pisa_oracle_flat_select(_ptr(qq), _ptr(k), B, N, Hq, Hkv, d, C, g, K, int(causal),
-                                         _ptr(t), n_t, _ptr(idx), _ptr(sc), _ptr(gap), threads)
+                                         _ptr(t), n_t, _ptr(idx), _ptr(sc), _ptr(gap), threads, mode)
     if rc:
         raise ValueError("oracle flat_select: bad arguments")
     return dict(idx=idx, scores=sc, min_gap=gap, t=t)
 
 
 def leaf_scores(q, keys, t_list, leaves, C: int = 64, g: int = 2, causal: bool = True,
-                threads: int = 0):
+                threads: int = 0, mode: int = 0):
     """Exact head-summed raw-key LSE of given leaves for given query positions.
 
     q [B, n_t, Hq, d]; leaves [B, Hkv, n_t, K] int (-1 -> -inf).
@@ -220,18 +221,18 @@ def leaf_scores(q, keys, t_list, leaves, C: int = 64, g: int = 2, causal: bool =
     Kc = lv.shape[-1]
     out = np.empty(lv.shape, dtype=np.float64)
     rc = _load().pisa_oracle_leaf_scores(_ptr(qq), _ptr(k), B, N, Hq, Hkv, d, C, g, int(causal),
-                                         _ptr(t), len(t), Kc, _ptr(lv), _ptr(out), threads)
+                                         _ptr(t), len(t), Kc, _ptr(lv), _ptr(out), threads, mode)
     if rc:
         raise ValueError("oracle leaf_scores: bad arguments")
     return out
 
 
 def node_score(q_row, keys, level: int, node: int, t: int, kv: int = 0, C: int = 64, g: int = 2,
-               causal: bool = True) -> float:
+               causal: bool = True, mode: int = 0) -> float:
     """Head-summed LSE score of one node for one query (q_row [Hq, d], keys [1, N, Hkv, d])."""
     k = _f32(keys)
     _, N, Hkv, d = k.shape
     qq = _f32(q_row)
     Hq = qq.shape[0]
     return float(_load().pisa_oracle_node_score(_ptr(qq), _ptr(k), N, Hq, Hkv, d, C, g, int(causal),
-                                                kv, t, level, node))
+                                                kv, t, level, node, mode))

@@ -195,7 +195,23 @@ typedef struct {
   int64_t t;           /* query position                                           */
   double scale;        /* 1/sqrt(d)                                                */
   double* work;        /* scratch of >= max(C, g) doubles                          */
+  int mode;            /* block score: 0 LSE, 1 mean (PISA-1), 2 mean + var/2 (PISA-2) */
 } walk_ctx;
+
+/* ["Scoring: LogSumExp"]: the Taylor expansion of log sum_i e^{z_i} around the mean,
+ * without the log m term, truncated at first order gives the mean of the logits
+ * (the PISA-1 ablation) and at second order the mean plus half their variance (PISA-2).
+ * Mean and (population) variance over the m logits present. */
+static double mode_score(const double* x, int m, int mode) {
+  if (mode == 0) return lse(x, m);
+  double mean = 0.0;
+  for (int i = 0; i < m; ++i) mean += x[i];
+  mean /= m;
+  if (mode == 1) return mean;
+  double var = 0.0;
+  for (int i = 0; i < m; ++i) var += (x[i] - mean) * (x[i] - mean);
+  return mean + 0.5 * (var / m);
+}
 
 static int eligible(const walk_ctx* w, int l, int64_t i) {
   return !w->causal || node_start(w->lv, l, i) <= w->t;
@@ -229,7 +245,7 @@ static double block_score(const walk_ctx* w, int l, int64_t c) {
         w->work[m++] = dot * w->scale;
       }
     }
-    total += lse(w->work, m); /* m >= 1: an eligible candidate's first child is eligible */
+    total += mode_score(w->work, m, w->mode); /* m >= 1: an eligible candidate's first child is */
   }
   return total;
 }
@@ -328,7 +344,7 @@ int pisa_oracle_max_threads(void) { return resolve_threads(0); }
 int pisa_oracle_select(const float* q, const float* keys, int B, int64_t N, int Hq, int Hkv, int d,
                        int C, int g, int K, int causal, const int64_t* t_list, int64_t n_t,
                        int32_t* idx, double* scores, double* min_gap, int32_t* n_scored,
-                       int n_threads) {
+                       int n_threads, int mode) {
   oracle_levels lv;
   if (B <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || K < 1 || levels_init(&lv, N, C, g)) return -1;
   for (int64_t i = 0; i < n_t; ++i)
@@ -368,6 +384,7 @@ int pisa_oracle_select(const float* q, const float* keys, int B, int64_t N, int 
       w.t = t_list[it];
       w.scale = 1.0 / sqrt((double)d);
       w.work = work;
+      w.mode = mode;
       int64_t o = ((int64_t)b * Hkv + kv) * n_t + it;
       int ns = walk_one(&w, K, idx + o * K, scores ? scores + o * K : NULL,
                         min_gap ? min_gap + o : NULL, S, cand, cs, order);
@@ -395,7 +412,7 @@ int pisa_oracle_select(const float* q, const float* keys, int B, int64_t N, int 
  */
 int pisa_oracle_flat_select(const float* q, const float* keys, int B, int64_t N, int Hq, int Hkv, int d,
                             int C, int g, int K, int causal, const int64_t* t_list, int64_t n_t,
-                            int32_t* idx, double* scores, double* min_gap, int n_threads) {
+                            int32_t* idx, double* scores, double* min_gap, int n_threads, int mode) {
   oracle_levels lv;
   if (B <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || K < 1 || levels_init(&lv, N, C, g)) return -1;
   for (int64_t i = 0; i < n_t; ++i)
@@ -431,6 +448,7 @@ int pisa_oracle_flat_select(const float* q, const float* keys, int B, int64_t N,
       w.t = t_list[it];
       w.scale = 1.0 / sqrt((double)d);
       w.work = work;
+      w.mode = mode;
       int64_t nc = 0; /* eligible leaves are a prefix: 0 .. nc-1 */
       while (nc < M1 && eligible(&w, 1, nc)) ++nc;
       for (int64_t c = 0; c < nc; ++c) {
@@ -521,6 +539,7 @@ int pisa_oracle_select_last(const float* q, const float* keys, int B, int64_t n_
     w.t = lengths[b] - 1;
     w.scale = 1.0 / sqrt((double)d);
     w.work = work;
+    w.mode = 0; /* decode: LSE only */
     int64_t o = job;
     int ns = walk_one(&w, K, idx + o * K, scores ? scores + o * K : NULL,
                       min_gap ? min_gap + o : NULL, S, cand, cs, order);
@@ -543,7 +562,7 @@ int pisa_oracle_select_last(const float* q, const float* keys, int B, int64_t n_
  */
 int pisa_oracle_leaf_scores(const float* q, const float* keys, int B, int64_t N, int Hq, int Hkv,
                             int d, int C, int g, int causal, const int64_t* t_list, int64_t n_t,
-                            int K, const int32_t* leaves, double* out, int n_threads) {
+                            int K, const int32_t* leaves, double* out, int n_threads, int mode) {
   oracle_levels lv;
   if (B <= 0 || Hkv <= 0 || Hq % Hkv || levels_init(&lv, N, C, g)) return -1;
   const int G = Hq / Hkv;
@@ -573,6 +592,7 @@ int pisa_oracle_leaf_scores(const float* q, const float* keys, int B, int64_t N,
       w.t = t_list[it];
       w.scale = 1.0 / sqrt((double)d);
       w.work = work;
+      w.mode = mode;
       for (int k = 0; k < K; ++k) {
         int64_t o = job * K + k;
         int32_t c = leaves[o];
@@ -594,7 +614,7 @@ int pisa_oracle_leaf_scores(const float* q, const float* keys, int B, int64_t N,
  * query q ([Hq][d]) of group kv at position t.
  */
 double pisa_oracle_node_score(const float* q, const float* keys, int64_t N, int Hq, int Hkv, int d,
-                              int C, int g, int causal, int kv, int64_t t, int level, int64_t c) {
+                              int C, int g, int causal, int kv, int64_t t, int level, int64_t c, int mode) {
   oracle_levels lv;
   if (levels_init(&lv, N, C, g) || level < 1 || level > lv.L || c < 0 || c >= lv.M[level])
     return NAN;
@@ -617,6 +637,7 @@ double pisa_oracle_node_score(const float* q, const float* keys, int64_t N, int 
   w.t = t;
   w.scale = 1.0 / sqrt((double)d);
   w.work = work;
+  w.mode = mode;
   double s = block_score(&w, level, c);
   free(work);
   free(pyr);

@@ -385,3 +385,98 @@ def test_flat_ties_go_to_the_lower_index():
     got = oracle.flat_select(q, k, K=3, t_list=np.array([511]))
     assert got["idx"][0, 0, 0].tolist() == [0, 1, 2]
     assert got["min_gap"][0, 0, 0] == 0.0
+
+
+# ---------------------------------------------------------------- score modes
+# "Scoring: LogSumExp": the Taylor expansion of the LSE around the mean of the
+# logits, without log m, gives the two ablations: first order = mean (PISA-1),
+# second order = mean + variance / 2 (PISA-2).
+
+def _hand_case(name):
+    with open(os.path.join(os.path.dirname(__file__), "golden", "hand_trees.json")) as f:
+        return next(c for c in json.load(f)["cases"] if c["name"] == name)
+
+
+def _hand_inputs(case):
+    N, G, d = case["N"], case["G"], 64
+    k = np.zeros((1, N, 1, d), np.float32)
+    for leaf, vals in enumerate(case["leaf_values"]):
+        for h, v in enumerate(vals):
+            k[0, leaf * 64:min((leaf + 1) * 64, N), 0, h] = v
+    q = np.zeros((1, 1, G, d), np.float32)
+    for h in range(G):
+        q[0, 0, h, h] = 8.0
+    return q, k
+
+
+def test_modes_on_the_lse_versus_mean_tree():
+    """Case B: leaves 1.5, -1.0 | 0.5, 0.5 (values = logits).  The mean of node 0's
+    children is 0.25 and of node 1's 0.5, so PISA-1 walks into node 1 and then ties
+    its two leaves (mean 0.5 each): leaf 2.  PISA-2 adds half the variance of the
+    children: 0.25 + 0.5 * 1.25^2 = 1.03125 > 0.5, so it keeps node 0 and then leaf 0
+    (constant keys: no variance, score 1.5)."""
+    case = _hand_case("B_lse_differs_from_mean")
+    q, k = _hand_inputs(case)
+    t = np.array([case["t"]])
+    r1 = oracle.select(q, k, K=1, causal=False, t_list=t, mode=1)
+    assert r1["idx"][0, 0, 0].tolist() == [2]
+    assert r1["scores"][0, 0, 0, 0] == pytest.approx(0.5, abs=1e-12)
+    assert r1["min_gap"][0, 0, 0] == pytest.approx(0.0, abs=1e-12)
+    r2 = oracle.select(q, k, K=1, causal=False, t_list=t, mode=2)
+    assert r2["idx"][0, 0, 0].tolist() == [0]
+    assert r2["scores"][0, 0, 0, 0] == pytest.approx(1.5, abs=1e-12)
+    assert r2["min_gap"][0, 0, 0] == pytest.approx(min(1.03125 - 0.5, 1.5 - (-1.0)), abs=1e-12)
+
+
+def test_mean_mode_at_a_full_node_is_the_parent_mean_logit():
+    rng = np.random.default_rng(9)
+    N, Hkv, G, d = 1024, 2, 3, 64
+    k = rng.standard_normal((1, N, Hkv, d)).astype(np.float32)
+    q = rng.standard_normal((Hkv * G, d)).astype(np.float32)
+    for level, node in [(2, 3), (3, 1), (4, 0)]:
+        span = 64 * 2 ** (level - 1)
+        for kv in range(Hkv):
+            kbar = k[0, node * span:(node + 1) * span, kv].astype(np.float64).mean(0)
+            want = sum(float(q[kv * G + h].astype(np.float64) @ kbar) / 8.0 for h in range(G))
+            got = oracle.node_score(q, k, level, node, t=N - 1, kv=kv, causal=False, mode=1)
+            assert got == pytest.approx(want, rel=1e-12, abs=1e-12)
+
+
+def test_second_order_mode_misses_the_lse_by_log_cosh_minus_half_square():
+    """Two equal children with logits m +/- delta: log(e^{m+delta} + e^{m-delta}) - log 2
+    = m + log cosh(delta), while mean + var/2 = m + delta^2 / 2."""
+    rng = np.random.default_rng(10)
+    N, G, d = 512, 2, 64
+    k = rng.standard_normal((1, N, 1, d)).astype(np.float32)
+    q = rng.standard_normal((G, d)).astype(np.float32)
+    level, node = 3, 1  # children: level-2 nodes 2 and 3, 128 tokens each
+    lse = oracle.node_score(q, k, level, node, t=N - 1, causal=False, mode=0)
+    p2 = oracle.node_score(q, k, level, node, t=N - 1, causal=False, mode=2)
+    want = 0.0
+    for h in range(G):
+        z = [float(q[h].astype(np.float64) @ k[0, c * 128:(c + 1) * 128, 0].astype(np.float64).mean(0)) / 8.0
+             for c in (2, 3)]
+        delta = (z[0] - z[1]) / 2
+        want += math.log(math.cosh(delta)) - delta * delta / 2
+    assert (lse - G * math.log(2)) - p2 == pytest.approx(want, rel=1e-9, abs=1e-12)
+
+
+def test_leaf_level_modes_are_moments_of_the_raw_key_logits():
+    rng = np.random.default_rng(12)
+    N, Hkv, G, d = 200, 1, 2, 64
+    k = rng.standard_normal((1, N, Hkv, d)).astype(np.float32)
+    q = rng.standard_normal((1, 3, G, d)).astype(np.float32)
+    t = np.array([70, 150, 199])
+    leaves = np.array([[[[0, 1], [1, 2], [3, -1]]]], np.int32)
+    for mode in (1, 2):
+        got = oracle.leaf_scores(q, k, t, leaves, mode=mode)
+        for i, tt in enumerate(t):
+            for j, c in enumerate(leaves[0, 0, i]):
+                if c < 0:
+                    assert got[0, 0, i, j] == -np.inf
+                    continue
+                want = 0.0
+                for h in range(G):
+                    z = k[0, c * 64:min((c + 1) * 64, tt + 1), 0].astype(np.float64) @ q[0, i, h].astype(np.float64) / 8
+                    want += z.mean() + (0.5 * z.var() if mode == 2 else 0.0)
+                assert got[0, 0, i, j] == pytest.approx(want, rel=1e-12, abs=1e-12)
