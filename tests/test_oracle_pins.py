@@ -392,12 +392,12 @@ def test_flat_ties_go_to_the_lower_index():
 # logits, without log m, gives the two ablations: first order = mean (PISA-1),
 # second order = mean + variance / 2 (PISA-2).
 
-def _hand_case(name):
+def _mode_case(name):
     with open(os.path.join(os.path.dirname(__file__), "golden", "hand_trees.json")) as f:
         return next(c for c in json.load(f)["cases"] if c["name"] == name)
 
 
-def _hand_inputs(case):
+def _mode_inputs(case):
     N, G, d = case["N"], case["G"], 64
     k = np.zeros((1, N, 1, d), np.float32)
     for leaf, vals in enumerate(case["leaf_values"]):
@@ -415,8 +415,8 @@ def test_modes_on_the_lse_versus_mean_tree():
     its two leaves (mean 0.5 each): leaf 2.  PISA-2 adds half the variance of the
     children: 0.25 + 0.5 * 1.25^2 = 1.03125 > 0.5, so it keeps node 0 and then leaf 0
     (constant keys: no variance, score 1.5)."""
-    case = _hand_case("B_lse_differs_from_mean")
-    q, k = _hand_inputs(case)
+    case = _mode_case("B_lse_differs_from_mean")
+    q, k = _mode_inputs(case)
     t = np.array([case["t"]])
     r1 = oracle.select(q, k, K=1, causal=False, t_list=t, mode=1)
     assert r1["idx"][0, 0, 0].tolist() == [2]
