@@ -139,6 +139,29 @@ size_t pisa_flat_workspace_bytes(int B, int64_t N, int Hq, int Hkv, int K);
 int pisa_select_flat(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
                      int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Score modes of the _ex entry points ("Block Sparse Attention with Log-Linear
+ * Complexity", Scoring: LogSumExp -- the Taylor expansion of the LSE around the
+ * mean of the logits, without log m, truncated at first order gives the mean
+ * (the PISA-1 ablation), at second order the mean plus half the variance
+ * (PISA-2)).  The mode replaces the block score at every scored level,
+ * intermediate (over the children's summary logits) and leaf (over the raw-key
+ * logits); the reported scores are the leaf scores under that mode.
+ */
+#define PISA_SCORE_LSE 0
+#define PISA_SCORE_MEAN 1
+#define PISA_SCORE_MEAN_HALF_VAR 2
+
+/* pisa_select_prefill with a score mode (PISA_ERR_UNSUPPORTED for other modes). */
+int pisa_select_prefill_ex(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K,
+                           int causal, int32_t* idx, float* scores, void* ws, size_t ws_bytes,
+                           void* stream, int score_mode);
+
+/* pisa_select_flat with a score mode (PISA_ERR_UNSUPPORTED for other modes). */
+int pisa_select_flat_ex(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
+                        int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream,
+                        int score_mode);
+
 /* Workspace bytes pisa_decode_append_and_select needs (0 on bad sizes). */
 size_t pisa_decode_workspace_bytes(int B, int Hq, int Hkv, int K);
 

@@ -64,6 +64,10 @@ def load(path: str | None = None):
     lib.pisa_flat_workspace_bytes.restype = sz
     lib.pisa_select_flat.argtypes = [vp, i32, vp, i64, i32, i32, vp, vp, vp, sz, vp]
     lib.pisa_select_flat.restype = i32
+    lib.pisa_select_prefill_ex.argtypes = [vp, i32, vp, i64, i32, i32, vp, vp, vp, sz, vp, i32]
+    lib.pisa_select_prefill_ex.restype = i32
+    lib.pisa_select_flat_ex.argtypes = [vp, i32, vp, i64, i32, i32, vp, vp, vp, sz, vp, i32]
+    lib.pisa_select_flat_ex.restype = i32
     lib.pisa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.pisa_decode_workspace_bytes.restype = sz
     lib.pisa_decode_append_and_select.argtypes = [vp, vp, i32, vp, i32, vp, vp, vp, sz, vp]
@@ -192,8 +196,9 @@ def select_workspace_bytes(B: int, N: int, Hq: int, Hkv: int, K: int) -> int:
 
 def select_prefill(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True, N: int | None = None,
                    with_scores: bool = True, workspace: torch.Tensor | None = None,
-                   out: tuple | None = None, stream=None):
-    """Coarse-to-fine Top-K for every query (§3.2).
+                   out: tuple | None = None, stream=None, mode: int = 0):
+    """Coarse-to-fine Top-K for every query (§3.2).  mode: block score, 0 = LSE,
+    1 = mean of the child logits (PISA-1), 2 = mean + half their variance (PISA-2).
 
     Q [B, N, Hq, 64] bf16 (CUDA).  Returns (idx [B, Hkv, N, K] int32, scores
     [B, Hkv, N, K] fp32 or None).
@@ -214,9 +219,10 @@ def select_prefill(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True, N
     else:
         idx, scores = out
     st = pyr.struct()
-    _check(lib.pisa_select_prefill(_ptr(Q), Hq, ctypes.byref(st), N, K, int(causal), _ptr(idx),
-                                   _ptr(scores), _ptr(workspace), workspace.numel(), _stream(stream)),
-           "pisa_select_prefill")
+    _check(lib.pisa_select_prefill_ex(_ptr(Q), Hq, ctypes.byref(st), N, K, int(causal), _ptr(idx),
+                                      _ptr(scores), _ptr(workspace), workspace.numel(), _stream(stream),
+                                      int(mode)),
+           "pisa_select_prefill_ex")
     return idx, scores
 
 
@@ -226,7 +232,7 @@ def flat_workspace_bytes(B: int, N: int, Hq: int, Hkv: int, K: int) -> int:
 
 def select_flat(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True, N: int | None = None,
                 with_scores: bool = True, workspace: torch.Tensor | None = None,
-                out: tuple | None = None, stream=None):
+                out: tuple | None = None, stream=None, mode: int = 0):
     """Flat selection: every eligible leaf scored exactly, the K best kept.
     Same arguments and outputs as select_prefill (only pyr.keys is read)."""
     if Q.dtype != torch.bfloat16 or not Q.is_cuda or Q.dim() != 4:
@@ -245,9 +251,10 @@ def select_flat(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True, N: i
     else:
         idx, scores = out
     st = pyr.struct()
-    _check(lib.pisa_select_flat(_ptr(Q), Hq, ctypes.byref(st), N, K, int(causal), _ptr(idx), _ptr(scores),
-                                _ptr(workspace), workspace.numel(), _stream(stream)),
-           "pisa_select_flat")
+    _check(lib.pisa_select_flat_ex(_ptr(Q), Hq, ctypes.byref(st), N, K, int(causal), _ptr(idx),
+                                   _ptr(scores), _ptr(workspace), workspace.numel(), _stream(stream),
+                                   int(mode)),
+           "pisa_select_flat_ex")
     return idx, scores
 
 

@@ -37,6 +37,7 @@ struct LeafTcLaunch {
   int32_t* idx;
   float* scores;
   int* status;
+  int mode;  // leaf score: 0 LSE over the keys, 1 mean logit, 2 mean + variance / 2
 };
 
 cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s);
@@ -59,6 +60,7 @@ struct WalkLaunch {
   int32_t* srank;  // rank of each survivor inside its bucket (the bucket count before it)
   int* count;
   int nchunks, chunk_shift, M2;
+  int mode;  // block score: 0 LSE, 1 mean of the child logits, 2 mean + variance / 2
 };
 
 long long route_rows_per_bh(const Levels& lv);

@@ -24,6 +24,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "api.cuh"
 #include "tc.cuh"
@@ -160,6 +161,53 @@ struct HalfLse {
   }
 };
 
+// The score modes' counterpart of HalfLse: mean (MODE 1) or mean + variance / 2
+// (MODE 2) of the logits z = x / 8 of one 64-key half, from shifted sums
+// sum (x - x0) and sum (x - x0)^2 (x0 = the half's first key) for conditioning.
+template <int MODE>
+struct HalfMom {
+  float ref, s1, s2;
+  int n;
+  __device__ __forceinline__ void first(const float (&x)[32], int cnt, bool full) {
+    ref = x[0];
+    s1 = s2 = 0.f;
+    n = 0;
+    add(x, cnt, full);
+  }
+  __device__ __forceinline__ void add(const float (&x)[32], int cnt, bool full) {
+    if (full) {
+      const unsigned long long nr2 = f2_pack(-ref, -ref);
+      unsigned long long a1 = 0ull, a2 = 0ull;
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        const unsigned long long d2 = f2_add(f2_pack(x[c], x[c + 1]), nr2);
+        a1 = f2_add(a1, d2);
+        a2 = f2_fma(d2, d2, a2);
+      }
+      float p, q;
+      f2_unpack(a1, p, q);
+      s1 += p + q;
+      f2_unpack(a2, p, q);
+      s2 += p + q;
+      n += 32;
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float dd = c < cnt ? x[c] - ref : 0.f;
+        s1 += dd;
+        s2 = fmaf(dd, dd, s2);
+      }
+      n += cnt;
+    }
+  }
+  __device__ __forceinline__ float value() const {  // natural-log units
+    const float inv = 1.f / (float)n, m = s1 * inv;
+    float v = (ref + m) * 0.125f;
+    if (MODE == 2) v += 0.5f * fmaxf(s2 * inv - m * m, 0.f) * 0.015625f;
+    return v;
+  }
+};
+
 // Orders the uses of registers written by tcgen05.ld after the wait::ld that
 // completes them.
 __device__ __forceinline__ void reg_fence32(float (&x)[32]) {
@@ -169,6 +217,8 @@ __device__ __forceinline__ void reg_fence32(float (&x)[32]) {
                  "+f"(x[i + 6]), "+f"(x[i + 7]));
 }
 
+// MODE: 0 LSE over each leaf's keys, 1 their mean logit, 2 mean + variance / 2.
+template <int MODE>
 __global__ void __launch_bounds__(kLeafWarps * 32, 1)
     leaf_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    LeafTcParams P) {
@@ -348,7 +398,8 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
                 c3 = max(l - 96, 0);
       // columns 0..63 (key half 0) first; columns 64..127 are loaded while half 0 is
       // summed, and the accumulator is released as soon as they are in registers
-      HalfLse h0, h1;
+      using Acc = typename std::conditional<MODE == 0, HalfLse, HalfMom<MODE>>::type;
+      Acc h0, h1;
       tmem_ld32(taddr + 32, xb);
       tmem_ld_wait();
       reg_fence32(xa);
@@ -601,7 +652,9 @@ cudaError_t launch_leaf_tc_kernel(const LeafTcLaunch& L, int flat, long long fla
     return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {
-    cudaFuncSetAttribute(leaf_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLeafSmem);
+    cudaFuncSetAttribute(leaf_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLeafSmem);
+    cudaFuncSetAttribute(leaf_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLeafSmem);
+    cudaFuncSetAttribute(leaf_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLeafSmem);
   });
   LeafTcParams P;
   P.flat = flat;
@@ -625,7 +678,8 @@ cudaError_t launch_leaf_tc_kernel(const LeafTcLaunch& L, int flat, long long fla
   P.causal = L.causal;
   P.leaf_scores = L.leaf_scores;
   P.status = L.status;
-  leaf_tc_kernel<<<sm_count(), kLeafWarps * 32, kLeafSmem, s>>>(qmap, kmap, P);
+  auto kern = L.mode == 1 ? leaf_tc_kernel<1> : L.mode == 2 ? leaf_tc_kernel<2> : leaf_tc_kernel<0>;
+  kern<<<sm_count(), kLeafWarps * 32, kLeafSmem, s>>>(qmap, kmap, P);
   note_launch();
   return cudaGetLastError();
 }

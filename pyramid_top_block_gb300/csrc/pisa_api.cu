@@ -197,8 +197,9 @@ size_t pisa_select_workspace_bytes(int B, int64_t N, int Hq, int Hkv, int K) {
   return prefill_layout(B, N, Hkv, K).total;
 }
 
-int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
-                        int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream) {
+static int select_prefill_impl(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
+                               int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream, int mode) {
+  if (mode < 0 || mode > 2) return PISA_ERR_UNSUPPORTED;
   int st = check_pyr(pyr);
   if (st) return st;
   if (!Q || !idx || !ws) return PISA_ERR_INVALID_ARG;
@@ -234,6 +235,7 @@ int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t 
   W.nchunks = w.nchunks;
   W.chunk_shift = w.chunk_shift;
   W.M2 = w.M2;
+  W.mode = mode;
   e = launch_prefill_walk_mma(W, s);
   if (e != cudaSuccess) return PISA_ERR_CUDA;
   mark_phase(2, s);
@@ -263,7 +265,19 @@ int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t 
   L.idx = idx;
   L.scores = scores;
   L.status = reinterpret_cast<int*>(base + w.status);
+  L.mode = mode;
   return cuda_status(launch_prefill_leaf_tc(L, s));
+}
+
+int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
+                        int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream) {
+  return select_prefill_impl(Q, Hq, pyr, N, K, causal, idx, scores, ws, ws_bytes, stream, 0);
+}
+
+int pisa_select_prefill_ex(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
+                           int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream,
+                           int score_mode) {
+  return select_prefill_impl(Q, Hq, pyr, N, K, causal, idx, scores, ws, ws_bytes, stream, score_mode);
 }
 
 size_t pisa_flat_workspace_bytes(int B, int64_t N, int Hq, int Hkv, int K) {
@@ -273,8 +287,9 @@ size_t pisa_flat_workspace_bytes(int B, int64_t N, int Hq, int Hkv, int K) {
   return flat_layout(B, N, Hq, Hkv, K, false).size;  // the non-causal layout is the larger
 }
 
-int pisa_select_flat(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
-                     int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream) {
+static int select_flat_impl(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
+                            int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream, int mode) {
+  if (mode < 0 || mode > 2) return PISA_ERR_UNSUPPORTED;
   int st = check_pyr(pyr);
   if (st) return st;
   if (!Q || !idx || !ws) return PISA_ERR_INVALID_ARG;
@@ -306,7 +321,18 @@ int pisa_select_flat(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, 
   L.idx = idx;
   L.scores = scores;
   L.status = reinterpret_cast<int*>(base + w.status);
+  L.mode = mode;
   return cuda_status(launch_select_flat(L, w.T1, w.stride, reinterpret_cast<int*>(base + w.total), s));
+}
+
+int pisa_select_flat(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
+                     int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream) {
+  return select_flat_impl(Q, Hq, pyr, N, K, causal, idx, scores, ws, ws_bytes, stream, 0);
+}
+
+int pisa_select_flat_ex(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
+                        int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream, int score_mode) {
+  return select_flat_impl(Q, Hq, pyr, N, K, causal, idx, scores, ws, ws_bytes, stream, score_mode);
 }
 
 size_t pisa_decode_workspace_bytes(int B, int Hq, int Hkv, int K) {

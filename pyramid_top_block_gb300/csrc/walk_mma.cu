@@ -44,6 +44,7 @@
 // first scored level (zero beyond its size): q_h . kbar for every head is one
 // MMA tile, which gives that level's head-summed Z.
 #include <mutex>
+#include <type_traits>
 
 #include "api.cuh"
 #include "tc.cuh"
@@ -180,7 +181,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
     const __nv_bfloat16* __restrict__ Q, const float* __restrict__ summ, const unsigned char* __restrict__ table,
     Levels lv, RowOffsets ro, long long rows_per_bh, int N, int Hq, int Hkv, int K, int causal, int l_start,
     int l_lo, int32_t* __restrict__ surv, int32_t* __restrict__ srank, int* __restrict__ count, int nchunks,
-    int chunk_shift, int M2) {
+    int chunk_shift, int M2, int mode) {
   extern __shared__ __align__(16) unsigned char wsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, j = lane & 3;
@@ -347,8 +348,12 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
                     const float u = (dh[nt][2 * cc + e] + dl[nt][2 * cc + e]) * kLn2;
                     su += u;
                     if (scoring && kd.two) {
-                      am += u >= 0.f ? u : -kd.r * u;
-                      pr *= 1.f + ex2_approx(-(1.f + kd.r) * fabsf(u) * kL2e);
+                      if (mode == 0) {
+                        am += u >= 0.f ? u : -kd.r * u;
+                        pr *= 1.f + ex2_approx(-(1.f + kd.r) * fabsf(u) * kL2e);
+                      } else {
+                        am += u * u;  // for the variance of the two children's logits
+                      }
                     }
                   }
                 }
@@ -366,7 +371,9 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
               S.su[ci] = su;
               if (scoring) {
                 const float z = S.zs[ci];
-                S.score[ci] = kd.two ? z + am + lg2_approx(pr) * kLn2 : z + (kd.ref1 ? -kd.r : 1.f) * su;
+                float two_sc = am + lg2_approx(pr) * kLn2;  // LSE: z + max part + log(1 + ...)
+                if (mode != 0) two_sc = 0.5f * (1.f - kd.r) * su + (mode == 2 ? 0.125f * (1.f + kd.r) * (1.f + kd.r) * am : 0.f);
+                S.score[ci] = kd.two ? z + two_sc : z + (kd.ref1 ? -kd.r : 1.f) * su;
               }
             }
           }
@@ -525,7 +532,10 @@ __device__ __forceinline__ float keep_mul(float pa, float pb, int s) {
   return mine * __shfl_xor_sync(kFull, send, 1);
 }
 
-template <int NT>
+// MODE: 0 LSE over the two children (PISA), 1 their mean (PISA-1), 2 mean + variance / 2
+// (PISA-2).  With children logits z + u and z - r u: mean = z + (1 - r) u / 2, variance / 2 =
+// (1 + r)^2 u^2 / 8 (natural units; ln 2 (1 + r)^2 u^2 / 8 for base-2 logits u).
+template <int NT, int MODE>
 __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
     const __nv_bfloat16* __restrict__ Q, const unsigned char* __restrict__ table, Levels lv, RowOffsets ro,
     LevelTail tail, long long rows_per_bh, int N, int Hq, int Hkv, int K, int causal, int l_start, int l_lo,
@@ -655,9 +665,25 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
       tile_dots<NT>(A, ra, rb, u);
       // per candidate of the pair: sum of u, sum of max(u, -r u), prod of (1 + 2^{-(1+r)|u|})
       float su[2], am[2], pr[2];
-      const bool any_rag = rag >= 0 && __any_sync(kFull, (va && na == rag) || (vb && nb == rag));
+      const bool any_rag = MODE == 0 && rag >= 0 && __any_sync(kFull, (va && na == rag) || (vb && nb == rag));
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < 2 && MODE != 0; ++cc) {  // moments: sum of u and of u^2 over the lane's heads
+        unsigned long long s2 = f2_pack(0.f, 0.f), q2 = s2;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const unsigned long long u2 = f2_pack(u[nt][2 * cc], u[nt][2 * cc + 1]);
+          s2 = f2_add(s2, u2);
+          if (MODE == 2) q2 = f2_fma(u2, u2, q2);
+        }
+        float a, bb;
+        f2_unpack(s2, a, bb);
+        su[cc] = a + bb;
+        f2_unpack(q2, a, bb);
+        am[cc] = a + bb;
+        pr[cc] = 1.f;
+      }
+#pragma unroll
+      for (int cc = 0; cc < 2 && MODE == 0; ++cc) {
         unsigned long long s2 = f2_pack(0.f, 0.f), m2 = s2, p2 = f2_pack(1.f, 1.f);
         if (!any_rag) {  // r = 1: max(u, -u) = |u|, exponent -2|u|
           const unsigned long long m2c = f2_pack(-2.f, -2.f);
@@ -697,16 +723,21 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
       }
       // head sums for the owned candidate
       float sum_u = keep_add(su[0], su[1], s);
-      float part = keep_add(am[0], am[1], s) + lg2_approx(keep_mul(pr[0], pr[1], s));
+      float part = 0.f;  // MODE 0: sum of the LSE excess over z; MODE 2: sum of u^2
+      if (MODE == 0) part = keep_add(am[0], am[1], s) + lg2_approx(keep_mul(pr[0], pr[1], s));
+      if (MODE == 2) part = keep_add(am[0], am[1], s);
       sum_u += __shfl_xor_sync(kFull, sum_u, 2);
-      part += __shfl_xor_sync(kFull, part, 2);
+      if (MODE != 1) part += __shfl_xor_sync(kFull, part, 2);
       const bool valid = oc < nC;
       const bool two = 2 * c + 1 <= lim;
       const bool ref1 = c == rag;
       const float nr = ref1 ? rnr : -1.f;
       bool keep = valid;
       if (scoring) {
-        const float sc = Z + (two ? part : (ref1 ? nr : 1.f) * sum_u);
+        float two_sc = part;  // the candidate's score minus Z when both children count
+        if (MODE == 1) two_sc = 0.5f * (1.f + nr) * sum_u;
+        if (MODE == 2) two_sc = 0.5f * (1.f + nr) * sum_u + 0.69314718055994531f * 0.125f * (1.f - nr) * (1.f - nr) * part;
+        const float sc = Z + (two ? two_sc : (ref1 ? nr : 1.f) * sum_u);
         // order-preserving integer key; the low 4 bits hold 15 - candidate (lower index wins a tie)
         const unsigned fb = __float_as_uint(sc);
         unsigned key = fb ^ ((unsigned)((int)fb >> 31) | 0x80000000u);
@@ -819,15 +850,19 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
       }
     }
     const size_t smem = (size_t)(16 + crows) * kCacheRowBytes + (size_t)kWalkWarps * kCandBuf * 4;
-    auto kern = G > 8 ? walk_k8_kernel<2> : walk_k8_kernel<1>;
+    auto pick = [&](auto nt) {
+      constexpr int NT = decltype(nt)::value;
+      return W.mode == 1 ? walk_k8_kernel<NT, 1> : W.mode == 2 ? walk_k8_kernel<NT, 2> : walk_k8_kernel<NT, 0>;
+    };
+    auto kern = G > 8 ? pick(std::integral_constant<int, 2>()) : pick(std::integral_constant<int, 1>());
     {
       static std::mutex mu;
-      static size_t attr[2] = {0, 0};
+      static size_t attr[2][3] = {};
       std::lock_guard<std::mutex> lock(mu);
-      if (smem > attr[G > 8]) {
+      if (smem > attr[G > 8][W.mode]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr[G > 8] = smem;
+        attr[G > 8][W.mode] = smem;
       }
     }
     kern<<<grid, kWalkWarps * 32, smem, s>>>(W.Q, W.table, lv, ro, tail, rows, (int)W.N, W.Hq, W.Hkv, W.K, W.causal,
@@ -849,7 +884,7 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
   }
   walk_mma_kernel<<<grid, kWalkWarps * 32, smem, s>>>(W.Q, W.summ, W.table, lv, ro, rows, (int)W.N, W.Hq, W.Hkv, W.K,
                                                        W.causal, l_start, l_lo, W.surv, W.srank, W.count,
-                                                       W.nchunks, W.chunk_shift, W.M2);
+                                                       W.nchunks, W.chunk_shift, W.M2, W.mode);
   note_launch();
   return cudaGetLastError();
 }

@@ -27,21 +27,21 @@ def _score_ok(got, want):
     return np.where(inf, got == want, close)
 
 
-def compare_prefill(gpu_idx, gpu_scores, q_rows, keys, t_list, K, causal=True):
+def compare_prefill(gpu_idx, gpu_scores, q_rows, keys, t_list, K, causal=True, mode=0):
     """gpu_idx/gpu_scores: [B, Hkv, n_t, K] numpy for the positions in t_list;
     q_rows [B, n_t, Hq, d] float32; keys [B, N, Hkv, d] float32."""
-    orc = oracle.select(q_rows, keys, K=K, causal=causal, t_list=t_list)
-    return _compare(gpu_idx, gpu_scores, orc, q_rows, keys, t_list, K, causal)
+    orc = oracle.select(q_rows, keys, K=K, causal=causal, t_list=t_list, mode=mode)
+    return _compare(gpu_idx, gpu_scores, orc, q_rows, keys, t_list, K, causal, mode)
 
 
-def compare_flat(gpu_idx, gpu_scores, q_rows, keys, t_list, K, causal=True):
+def compare_flat(gpu_idx, gpu_scores, q_rows, keys, t_list, K, causal=True, mode=0):
     """The flat selector against the oracle's flat selection (same rules; the
     near-tie gap is the oracle's K-th minus (K+1)-th leaf score)."""
-    orc = oracle.flat_select(q_rows, keys, K=K, causal=causal, t_list=t_list)
-    return _compare(gpu_idx, gpu_scores, orc, q_rows, keys, t_list, K, causal)
+    orc = oracle.flat_select(q_rows, keys, K=K, causal=causal, t_list=t_list, mode=mode)
+    return _compare(gpu_idx, gpu_scores, orc, q_rows, keys, t_list, K, causal, mode)
 
 
-def _compare(gpu_idx, gpu_scores, orc, q_rows, keys, t_list, K, causal):
+def _compare(gpu_idx, gpu_scores, orc, q_rows, keys, t_list, K, causal, mode=0):
     oi, osc, gap = orc["idx"], orc["scores"], orc["min_gap"]
     same = np.all(gpu_idx == oi, axis=-1)  # [B, Hkv, n_t]
     near = gap < TIE
@@ -82,7 +82,7 @@ def _compare(gpu_idx, gpu_scores, orc, q_rows, keys, t_list, K, causal):
                 msgs.append(f"invalid excused row b={b} kv={kv} t={t} gpu={row.tolist()}")
         if gpu_scores is not None:
             lv = np.where(exc[..., None], gpu_idx, -1).astype(np.int32)
-            want = oracle.leaf_scores(q_rows, keys, t_list, lv, causal=causal)
+            want = oracle.leaf_scores(q_rows, keys, t_list, lv, causal=causal, mode=mode)
             ok = _score_ok(gpu_scores, want) | ~exc[..., None]
             stats["score_bad"] += int((~ok).sum())
             if (~ok).any():
