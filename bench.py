@@ -388,6 +388,24 @@ def run_ours(args):
     if not args.no_decode and rank == 0:
         decode = bench_decode(torch, pisa, synth, dev, args)
 
+    modes = None
+    if args.modes and rank == 0:
+        modes = {}
+        for m in (1, 2):
+            ms_m = []
+            for i in range(max(3, min(n, 10)) + 2):
+                flush.zero_()
+                a, b = mk(), mk()
+                a.record(stream)
+                pisa.build_pyramid(pyr)
+                pisa.select_prefill(qd, pyr, K, workspace=ws, out=(idx, None), with_scores=False, mode=m)
+                b.record(stream)
+                torch.cuda.synchronize()
+                if i >= 2:
+                    ms_m.append(a.elapsed_time(b))
+            modes[["lse", "mean", "mean_half_var"][m]] = {"ms_median": statistics.median(ms_m),
+                                                          "status": pisa.check_device_status(ws)}
+
     flat = None
     if args.flat and rank == 0:
         flat = [bench_flat(torch, pisa, synth, dev, name) for name in args.flat.split(",")]
@@ -406,7 +424,7 @@ def run_ours(args):
                 "rates": rates, "work": work,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
                 "device_status": device_status,
-                "decode": decode, "flat": flat}
+                "decode": decode, "flat": flat, "score_modes": modes}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -502,6 +520,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--modes", type=int, default=1, help="also time the PISA-1 / PISA-2 score modes")
     ap.add_argument("--flat", default="latency-32k",
                     help="comma-separated workloads for the flat-selector comparison ('' to skip)")
     ap.add_argument("--cpu-s", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
