@@ -83,6 +83,9 @@ def _load():
         lib.pisa_oracle_flat_select.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, i32, i32, i32,
                                                 vp, i64, vp, vp, vp, i32, i32]
         lib.pisa_oracle_flat_select.restype = i32
+        lib.pisa_oracle_attention.argtypes = [vp, vp, vp, i32, i64, i32, i32, i32, i32, i32, vp, i64,
+                                              i32, vp, vp, i32]
+        lib.pisa_oracle_attention.restype = i32
         lib.pisa_oracle_node_score.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, i64,
                                                i32, i64, i32]
         lib.pisa_oracle_node_score.restype = dbl
@@ -204,6 +207,28 @@ def flat_select(q, keys, K: int, C: int = 64, g: int = 2, causal: bool = True, t
     if rc:
         raise ValueError("oracle flat_select: bad arguments")
     return dict(idx=idx, scores=sc, min_gap=gap, t=t)
+
+
+def attention(q, keys, values, idx, t_list, C: int = 64, causal: bool = True, threads: int = 0):
+    """Stage-two block-sparse attention: for each listed position and query head, the
+    softmax-weighted sum of the values of the keys inside the selected leaves
+    idx [B, Hkv, n_t, K] (-1 skipped; keys after t masked when causal).
+    q [B, n_t, Hq, d] rows of t_list; keys, values [B, N, Hkv, d].  Returns
+    [B, n_t, Hq, d] float64."""
+    k = _f32(keys)
+    v = _f32(values)
+    B, N, Hkv, d = k.shape
+    qq = _f32(q)
+    Hq = qq.shape[2]
+    t = np.ascontiguousarray(t_list, dtype=np.int64)
+    ii = np.ascontiguousarray(idx, dtype=np.int32)
+    K = ii.shape[-1]
+    out = np.empty((B, len(t), Hq, d), dtype=np.float64)
+    rc = _load().pisa_oracle_attention(_ptr(qq), _ptr(k), _ptr(v), B, N, Hq, Hkv, d, C, int(causal), _ptr(t),
+                                       len(t), K, _ptr(ii), _ptr(out), threads)
+    if rc:
+        raise ValueError("oracle attention: bad arguments")
+    return out
 
 
 def leaf_scores(q, keys, t_list, leaves, C: int = 64, g: int = 2, causal: bool = True,

@@ -487,6 +487,69 @@ int pisa_oracle_flat_select(const float* q, const float* keys, int B, int64_t N,
 }
 
 /*
+ * Stage two of block-sparse attention ([P2] "Background: two stages": each query
+ * attends over the original keys and values inside its selected blocks).  For
+ * query position t and query head h of KV group kv:
+ *   o = sum_r softmax_r(q . k_r / sqrt(d)) v_r
+ * over the keys r of the selected leaves idx[b][kv][it][0..K) (entries < 0 are
+ * skipped), keys after t masked when causal; one softmax over all of them.
+ *   q  : [B][n_t][Hq][d] rows of t_list; k, v: [B][N][Hkv][d]
+ *   out: [B][n_t][Hq][d] (a row with no key is all zeros)
+ */
+int pisa_oracle_attention(const float* q, const float* keys, const float* vals, int B, int64_t N, int Hq,
+                          int Hkv, int d, int C, int causal, const int64_t* t_list, int64_t n_t, int K,
+                          const int32_t* idx, double* out, int n_threads) {
+  if (B <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || C <= 0 || K < 1) return -1;
+  for (int64_t i = 0; i < n_t; ++i)
+    if (t_list[i] < 0 || t_list[i] >= N) return -1;
+  const int G = Hq / Hkv;
+  const int nt = resolve_threads(n_threads);
+  const int64_t jobs = (int64_t)B * n_t * Hq;
+  const double scale = 1.0 / sqrt((double)d);
+#pragma omp parallel num_threads(nt)
+  {
+    double* z = (double*)malloc(sizeof(double) * (size_t)K * C);
+    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)K * C);
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t job = 0; job < jobs; ++job) {
+      const int h = (int)(job % Hq);
+      const int64_t it = (job / Hq) % n_t;
+      const int b = (int)(job / (Hq * n_t));
+      const int kv = h / G;
+      const int64_t t = t_list[it];
+      const float* qh = q + (((int64_t)b * n_t + it) * Hq + h) * d;
+      const int32_t* sel = idx + (((int64_t)b * Hkv + kv) * n_t + it) * K;
+      int m = 0;
+      for (int i = 0; i < K; ++i) {
+        if (sel[i] < 0) continue;
+        for (int64_t r = (int64_t)sel[i] * C; r < (int64_t)(sel[i] + 1) * C && r < N; ++r) {
+          if (causal && r > t) break;
+          double dot = 0.0;
+          for (int j = 0; j < d; ++j) dot += (double)qh[j] * key_at(keys, N, Hkv, d, b, r, kv, j);
+          z[m] = dot * scale;
+          rows[m++] = r;
+        }
+      }
+      double* o = out + (((int64_t)b * n_t + it) * Hq + h) * d;
+      for (int j = 0; j < d; ++j) o[j] = 0.0;
+      if (m == 0) continue;
+      double mx = z[0];
+      for (int i = 1; i < m; ++i)
+        if (z[i] > mx) mx = z[i];
+      double den = 0.0;
+      for (int i = 0; i < m; ++i) den += exp(z[i] - mx);
+      for (int i = 0; i < m; ++i) {
+        const double p = exp(z[i] - mx) / den;
+        for (int j = 0; j < d; ++j) o[j] += p * key_at(vals, N, Hkv, d, b, rows[i], kv, j);
+      }
+    }
+    free(z);
+    free(rows);
+  }
+  return 0;
+}
+
+/*
  * Decode selection ([P1] decoding keeps a cached mean pyramid and walks for the
  * one new query).  By definition it equals the prefill walk of the last query
  * over the keys present, so this routine rebuilds the pyramid over the first

@@ -480,3 +480,41 @@ def test_leaf_level_modes_are_moments_of_the_raw_key_logits():
                     z = k[0, c * 64:min((c + 1) * 64, tt + 1), 0].astype(np.float64) @ q[0, i, h].astype(np.float64) / 8
                     want += z.mean() + (0.5 * z.var() if mode == 2 else 0.0)
                 assert got[0, 0, i, j] == pytest.approx(want, rel=1e-12, abs=1e-12)
+
+
+# ---------------------------------------------------------------- stage two
+# "Background: two stages": each query attends over the keys and values of its
+# selected blocks with one softmax.
+
+def test_attention_over_every_block_is_dense_causal_attention():
+    rng = np.random.default_rng(21)
+    B, N, Hkv, G, d = 1, 300, 2, 2, 64
+    q = rng.standard_normal((B, N, Hkv * G, d)).astype(np.float32)
+    k = rng.standard_normal((B, N, Hkv, d)).astype(np.float32)
+    v = rng.standard_normal((B, N, Hkv, d)).astype(np.float32)
+    t = np.array([0, 5, 63, 64, 200, 299])
+    idx = np.tile(np.arange(5, dtype=np.int32), (B, Hkv, len(t), 1))  # all 5 leaves (with padding beyond t)
+    got = oracle.attention(q[:, t], k, v, idx, t)
+    for i, tt in enumerate(t):
+        for h in range(Hkv * G):
+            kv = h // G
+            logits = k[0, :tt + 1, kv].astype(np.float64) @ q[0, tt, h].astype(np.float64) / 8
+            p = np.exp(logits - logits.max())
+            p /= p.sum()
+            want = p @ v[0, :tt + 1, kv].astype(np.float64)
+            np.testing.assert_allclose(got[0, i, h], want, rtol=1e-11, atol=1e-12)
+
+
+def test_attention_with_constant_keys_averages_the_values():
+    """Equal logits: the output is the plain mean of the values of the selected keys <= t."""
+    rng = np.random.default_rng(22)
+    B, N, Hkv, d = 1, 256, 1, 64
+    k = np.zeros((B, N, Hkv, d), np.float32)
+    v = rng.standard_normal((B, N, Hkv, d)).astype(np.float32)
+    q = rng.standard_normal((B, 2, 1, d)).astype(np.float32)
+    t = np.array([100, 255])
+    idx = np.array([[[[0, 1, -1], [1, 3, -1]]]], np.int32)
+    got = oracle.attention(q, k, v, idx, t)
+    np.testing.assert_allclose(got[0, 0, 0], v[0, :101, 0].astype(np.float64).mean(0), rtol=1e-12, atol=1e-12)
+    want = np.concatenate([v[0, 64:128, 0], v[0, 192:256, 0]]).astype(np.float64).mean(0)
+    np.testing.assert_allclose(got[0, 1, 0], want, rtol=1e-12, atol=1e-12)
