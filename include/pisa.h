@@ -162,6 +162,24 @@ int pisa_select_flat_ex(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t 
                         int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream,
                         int score_mode);
 
+/*
+ * pisa_sparse_attention -- stage two of block-sparse attention ("Block Sparse
+ * Attention with Log-Linear Complexity", Background: two stages): each query
+ * attends over the original keys and values inside its selected blocks, one
+ * softmax over all of them (scale 1/sqrt(d)), keys after the query masked when
+ * causal.  Arithmetic: bf16 inputs and bf16 probabilities on the tensor cores,
+ * fp32 accumulation and softmax.
+ *   Q      : device bf16 [B, N, Hq, d]
+ *   K, V   : device bf16 [B, N, Hkv, d] (d = 64)
+ *   idx    : device int32 [B, Hkv, N, Ksel] leaf blocks (C = 64 keys) per query
+ *            and KV head, as pisa_select_prefill writes them; -1 entries skipped
+ *   out    : device fp32 [B, N, Hq, d] out; a query without keys gets zeros
+ * 1 <= Ksel <= 64, Hq/Hkv in {1, 2, 4, 8, 16}.  No workspace.  Asynchronous on
+ * stream; argument errors return before any launch.
+ */
+int pisa_sparse_attention(const void* Q, int Hq, const void* K, const void* V, int B, int64_t N, int Hkv,
+                          const int32_t* idx, int Ksel, int causal, float* out, void* stream);
+
 /* Workspace bytes pisa_decode_append_and_select needs (0 on bad sizes). */
 size_t pisa_decode_workspace_bytes(int B, int Hq, int Hkv, int K);
 

@@ -68,6 +68,8 @@ def load(path: str | None = None):
     lib.pisa_select_prefill_ex.restype = i32
     lib.pisa_select_flat_ex.argtypes = [vp, i32, vp, i64, i32, i32, vp, vp, vp, sz, vp, i32]
     lib.pisa_select_flat_ex.restype = i32
+    lib.pisa_sparse_attention.argtypes = [vp, i32, vp, vp, i32, i64, i32, vp, i32, i32, vp, vp]
+    lib.pisa_sparse_attention.restype = i32
     lib.pisa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.pisa_decode_workspace_bytes.restype = sz
     lib.pisa_decode_append_and_select.argtypes = [vp, vp, i32, vp, i32, vp, vp, vp, sz, vp]
@@ -256,6 +258,24 @@ def select_flat(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True, N: i
                                    int(mode)),
            "pisa_select_flat_ex")
     return idx, scores
+
+
+def sparse_attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, idx: torch.Tensor, causal: bool = True,
+                     out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Stage-two block-sparse attention over the blocks in idx [B, Hkv, N, Ksel].
+    Q [B, N, Hq, 64], K and V [B, N, Hkv, 64] bf16 CUDA; returns fp32 [B, N, Hq, 64]."""
+    for x in (Q, K, V):
+        if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 4 or not x.is_contiguous():
+            raise ValueError("Q, K, V must be contiguous CUDA bf16 tensors [B, N, H, d]")
+    if idx.dtype != torch.int32 or not idx.is_contiguous():
+        raise ValueError("idx must be contiguous int32 [B, Hkv, N, Ksel]")
+    B, N, Hq, d = Q.shape
+    if out is None:
+        out = torch.empty(B, N, Hq, d, dtype=torch.float32, device=Q.device)
+    _check(load().pisa_sparse_attention(_ptr(Q), Hq, _ptr(K), _ptr(V), B, N, K.shape[2], _ptr(idx), idx.shape[-1],
+                                        int(causal), _ptr(out), _stream(stream)),
+           "pisa_sparse_attention")
+    return out
 
 
 def select_prefill_noalloc(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True,

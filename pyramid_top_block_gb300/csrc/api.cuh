@@ -48,6 +48,11 @@ cudaError_t launch_leaf_tc_kernel(const LeafTcLaunch& L, int flat, long long fla
 cudaError_t launch_select_flat(const LeafTcLaunch& L, long long T1, long long stride, int* total, cudaStream_t s);
 long long flat_tiles_per_bh(long long N, int G, int K, bool causal);
 
+// Stage-two block-sparse attention (attend.cu).
+cudaError_t launch_sparse_attention(const __nv_bfloat16* Q, const __nv_bfloat16* K, const __nv_bfloat16* V,
+                                    const int32_t* idx, int B, long long N, int Hq, int Hkv, int Ksel, int causal,
+                                    float* out, cudaStream_t s);
+
 // The intermediate levels of the prefill walk (walk_mma.cu).
 struct WalkLaunch {
   const __nv_bfloat16* Q;

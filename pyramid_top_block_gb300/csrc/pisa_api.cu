@@ -280,6 +280,21 @@ int pisa_select_prefill_ex(const void* Q, int Hq, const pisa_pyramid* pyr, int64
   return select_prefill_impl(Q, Hq, pyr, N, K, causal, idx, scores, ws, ws_bytes, stream, score_mode);
 }
 
+int pisa_sparse_attention(const void* Q, int Hq, const void* K, const void* V, int B, int64_t N, int Hkv,
+                          const int32_t* idx, int Ksel, int causal, float* out, void* stream) {
+  if (!Q || !K || !V || !idx || !out || B < 1 || N < 1 || Hkv < 1 || Hq < 1) return PISA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V) |
+       reinterpret_cast<uintptr_t>(out)) & 15)
+    return PISA_ERR_INVALID_ARG;
+  if (Hq % Hkv) return PISA_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  if ((G & (G - 1)) || G > 16 || Ksel < 1 || Ksel > 64 || (long long)B * Hkv * N >= (1LL << 40))
+    return PISA_ERR_UNSUPPORTED;
+  return cuda_status(launch_sparse_attention(static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
+                                             static_cast<const __nv_bfloat16*>(V), idx, B, N, Hq, Hkv, Ksel,
+                                             causal != 0, out, static_cast<cudaStream_t>(stream)));
+}
+
 size_t pisa_flat_workspace_bytes(int B, int64_t N, int Hq, int Hkv, int K) {
   if (check_geometry(B, N, Hq, Hkv, kD, kC, 2, K) != PISA_OK) return 0;
   const FlatWs w = flat_layout(B, N, Hq, Hkv, K, true);

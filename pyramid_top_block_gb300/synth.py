@@ -14,6 +14,8 @@ from __future__ import annotations
 
 import math
 
+import numpy as np
+
 import torch
 
 
@@ -90,3 +92,19 @@ def make(name: str):
     fn = iid if w["kind"] == "iid" else structured
     q, k = fn(w["B"], w["N"], w["Hq"], w["Hkv"], 64, seed=w["seed"])
     return q, k, w
+
+
+def random_blocks(B: int, Hkv: int, N: int, K: int, seed: int, C: int = 64, causal: bool = True):
+    """Seeded block sets for stage-two tests: for every (b, kv, t), min(K, eligible)
+    distinct leaves drawn uniformly from the eligible ones (start <= t when causal),
+    ascending, -1 padded.  int32 [B, Hkv, N, K]."""
+    rng = np.random.default_rng(seed)
+    out = np.full((B, Hkv, N, K), -1, dtype=np.int32)
+    M1 = -(-N // C)
+    for b in range(B):
+        for kv in range(Hkv):
+            for t in range(N):
+                n_el = min(M1, t // C + 1) if causal else M1
+                k = min(K, n_el)
+                out[b, kv, t, :k] = np.sort(rng.choice(n_el, size=k, replace=False))
+    return torch.from_numpy(out)
