@@ -406,6 +406,29 @@ def run_ours(args):
             modes[["lse", "mean", "mean_half_var"][m]] = {"ms_median": statistics.median(ms_m),
                                                           "status": pisa.check_device_status(ws)}
 
+    attention = None
+    if args.attention and rank == 0:
+        # stage two over this pass's selection, with seeded random values
+        gv = torch.Generator().manual_seed(3)
+        vd = torch.randn(B, N, Hkv, 64, generator=gv).to(torch.bfloat16).to(dev)
+        att_out = torch.empty(B, N, Hq, 64, dtype=torch.float32, device=dev)
+        step()
+        ms_a = []
+        for i in range(7):
+            flush.zero_()
+            a, b = mk(), mk()
+            a.record(stream)
+            pisa.sparse_attention(qd, kd, vd, idx, out=att_out)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                ms_a.append(a.elapsed_time(b))
+        t_att = statistics.median(ms_a)
+        fl = 4.0 * B * N * Hq * K * 64 * 64  # QK^T and PV over K full leaves (upper bound)
+        attention = {"ms_median": t_att, "forward_ms": ms_step + t_att, "tflops_upper_bound": fl / t_att / 1e9,
+                     "note": "stage two over the pass's idx, random bf16 V, fp32 output"}
+        del vd, att_out
+
     flat = None
     if args.flat and rank == 0:
         flat = [bench_flat(torch, pisa, synth, dev, name) for name in args.flat.split(",")]
@@ -424,7 +447,7 @@ def run_ours(args):
                 "rates": rates, "work": work,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
                 "device_status": device_status,
-                "decode": decode, "flat": flat, "score_modes": modes}
+                "decode": decode, "flat": flat, "score_modes": modes, "attention": attention}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -520,6 +543,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--attention", type=int, default=1, help="also time stage-two attention on the selection")
     ap.add_argument("--modes", type=int, default=1, help="also time the PISA-1 / PISA-2 score modes")
     ap.add_argument("--flat", default="latency-32k",
                     help="comma-separated workloads for the flat-selector comparison ('' to skip)")
