@@ -97,6 +97,17 @@ int64_t pisa_level_offset(int64_t n_cap, int C, int g, int level);
  */
 int pisa_build_pyramid(const pisa_pyramid* pyr, int64_t N, void* stream);
 
+/*
+ * pisa_build_pyramid_ragged -- pisa_build_pyramid for a batch of sequences of
+ * different lengths (§3.1 per sequence): sequence b holds pyr->lengths[b] tokens
+ * (device int32, read on the device, clamped to [0, n_cap]); its nodes are the
+ * means over its own tokens, nodes past its own level sizes are left untouched.
+ * Nothing is read back to the host, so the call can be captured in a CUDA graph.
+ * Equal lengths give the same bits as pisa_build_pyramid.  Decode steps then
+ * append to each sequence at its own length.
+ */
+int pisa_build_pyramid_ragged(const pisa_pyramid* pyr, void* stream);
+
 /* Workspace bytes pisa_select_prefill needs for these sizes (0 on bad sizes). */
 size_t pisa_select_workspace_bytes(int B, int64_t N, int Hq, int Hkv, int K);
 

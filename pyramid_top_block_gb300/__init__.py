@@ -70,6 +70,8 @@ def load(path: str | None = None):
     lib.pisa_select_flat_ex.restype = i32
     lib.pisa_sparse_attention.argtypes = [vp, i32, vp, vp, i32, i64, i32, vp, i32, i32, vp, vp]
     lib.pisa_sparse_attention.restype = i32
+    lib.pisa_build_pyramid_ragged.argtypes = [vp, vp]
+    lib.pisa_build_pyramid_ragged.restype = i32
     lib.pisa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.pisa_decode_workspace_bytes.restype = sz
     lib.pisa_decode_append_and_select.argtypes = [vp, vp, i32, vp, i32, vp, vp, vp, sz, vp]
@@ -230,6 +232,15 @@ def select_prefill(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True, N
 
 def flat_workspace_bytes(B: int, N: int, Hq: int, Hkv: int, K: int) -> int:
     return int(load().pisa_flat_workspace_bytes(B, N, Hq, Hkv, K))
+
+
+def build_pyramid_ragged(pyr: Pyramid, stream=None) -> Pyramid:
+    """Build every sequence over its own length pyr.lengths[b] (set by the caller)."""
+    if pyr.lengths is None:
+        raise ValueError("a ragged build needs a Pyramid with lengths")
+    st = pyr.struct()
+    _check(load().pisa_build_pyramid_ragged(ctypes.byref(st), _stream(stream)), "pisa_build_pyramid_ragged")
+    return pyr
 
 
 def select_flat(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True, N: int | None = None,

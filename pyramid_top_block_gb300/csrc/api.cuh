@@ -15,7 +15,7 @@ void mark_phase(int i, cudaStream_t s);
 
 cudaError_t launch_build_pyramid(const __nv_bfloat16* keys, float* summ, const Levels& lv,
                                  long long N, long long n_cap, int B, int Hkv, int32_t* lengths,
-                                 cudaStream_t s);
+                                 cudaStream_t s, bool ragged = false);
 
 // Everything the leaf level of the prefill walk needs (buffers are caller
 // workspace slices; see pisa_api.cu for the layout).

@@ -192,6 +192,17 @@ int pisa_build_pyramid(const pisa_pyramid* pyr, int64_t N, void* stream) {
                                           static_cast<cudaStream_t>(stream)));
 }
 
+int pisa_build_pyramid_ragged(const pisa_pyramid* pyr, void* stream) {
+  int st = check_pyr(pyr);
+  if (st) return st;
+  if (!pyr->lengths) return PISA_ERR_INVALID_ARG;
+  if (pyr->n_cap > (1LL << 27)) return PISA_ERR_UNSUPPORTED;
+  const Levels lv = make_levels(pyr->n_cap, pyr->n_cap);
+  return cuda_status(launch_build_pyramid(static_cast<const __nv_bfloat16*>(pyr->keys), pyr->summaries, lv,
+                                          pyr->n_cap, pyr->n_cap, pyr->B, pyr->Hkv, pyr->lengths,
+                                          static_cast<cudaStream_t>(stream), true));
+}
+
 size_t pisa_select_workspace_bytes(int B, int64_t N, int Hq, int Hkv, int K) {
   if (check_geometry(B, N, Hq, Hkv, kD, kC, 2, K) != PISA_OK) return 0;
   return prefill_layout(B, N, Hkv, K).total;

@@ -27,7 +27,7 @@ __host__ __device__ inline int leaves_per_block(int Hkv) {
 
 __global__ void __launch_bounds__(256) pyramid_leaves_kernel(
     const __nv_bfloat16* __restrict__ keys, float* __restrict__ summ, Levels lv, long long N,
-    long long n_cap, int Hkv, int lpb, int merge_levels) {
+    long long n_cap, int Hkv, int lpb, int merge_levels, const int32_t* __restrict__ lens) {
   extern __shared__ float sm[];  // [lpb][Hkv][64]
   const int chunks = Hkv * 8;
   const int tid = threadIdx.x;
@@ -37,7 +37,10 @@ __global__ void __launch_bounds__(256) pyramid_leaves_kernel(
   const int jl = tid / chunks;  // local leaf
   const int b = blockIdx.y;
   const long long leaf = (long long)blockIdx.x * lpb + jl;
-  const long long M1 = lv.M[1];
+  // ragged batch: sequence b holds lens[b] tokens (clamped to [0, n_cap]); nodes past its
+  // own level sizes are left untouched
+  if (lens) N = min((long long)max(lens[b], 0), n_cap);
+  const long long M1 = level_size_for(N, 1);
   float* blk = summ + ((long long)b * Hkv + kv) * lv.total * kD;
 
   float acc[8];
@@ -78,13 +81,13 @@ __global__ void __launch_bounds__(256) pyramid_leaves_kernel(
   for (int l = 2; l <= merge_levels + 1; ++l) {
     const int nodes = lpb >> (l - 1);
     const long long i = (long long)blockIdx.x * nodes + jl;
-    const bool active = jl < nodes && i < lv.M[l];
+    const bool active = jl < nodes && i < level_size_for(N, l);
     float out[8];
     __syncthreads();
     if (active) {
       const long long c0 = 2 * i, c1 = 2 * i + 1;
       const int n0 = node_count(l - 1, c0, N);
-      const int n1 = c1 < lv.M[l - 1] ? node_count(l - 1, c1, N) : 0;
+      const int n1 = c1 < level_size_for(N, l - 1) ? node_count(l - 1, c1, N) : 0;
       const float* s0 = sm + ((2 * jl) * Hkv + kv) * kD + c8 * 8;
       const float* s1 = sm + ((2 * jl + 1) * Hkv + kv) * kD + c8 * 8;
 #pragma unroll
@@ -103,11 +106,13 @@ __global__ void __launch_bounds__(256) pyramid_leaves_kernel(
 
 // Levels first_level .. L for one (b, kv) per CTA, level by level.
 __global__ void __launch_bounds__(256) pyramid_top_kernel(float* __restrict__ summ, Levels lv,
-                                                           long long N, int Hkv, int first_level) {
+                                                           long long N, int Hkv, int first_level,
+                                                           const int32_t* __restrict__ lens, long long n_cap) {
   const int b = blockIdx.x / Hkv, kv = blockIdx.x % Hkv;
+  if (lens) N = min((long long)max(lens[b], 0), n_cap);
   float* blk = summ + ((long long)b * Hkv + kv) * lv.total * kD;
   for (int l = first_level; l <= lv.L; ++l) {
-    const long long M = lv.M[l], Mc = lv.M[l - 1];
+    const long long M = level_size_for(N, l), Mc = level_size_for(N, l - 1);
     for (long long w = threadIdx.x; w < M * kD; w += blockDim.x) {
       const long long i = w / kD;
       const int e = (int)(w % kD);
@@ -130,7 +135,8 @@ __global__ void fill_lengths_kernel(int32_t* lengths, int B, int value) {
 // Host launcher (declared in api.cuh).
 cudaError_t launch_build_pyramid(const __nv_bfloat16* keys, float* summ, const Levels& lv,
                                  long long N, long long n_cap, int B, int Hkv, int32_t* lengths,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, bool ragged) {
+  const int32_t* lens = ragged ? lengths : nullptr;  // per-sequence lengths read on the device
   const int lpb = leaves_per_block(Hkv);
   int merge_levels = 0;
   while ((1 << (merge_levels + 1)) <= lpb) ++merge_levels;
@@ -139,17 +145,17 @@ cudaError_t launch_build_pyramid(const __nv_bfloat16* keys, float* summ, const L
   dim3 grid((unsigned)((M1 + lpb - 1) / lpb), (unsigned)B);
   const int threads = lpb * Hkv * 8;
   const size_t smem = (size_t)lpb * Hkv * kD * sizeof(float);
-  pyramid_leaves_kernel<<<grid, threads, smem, s>>>(keys, summ, lv, N, n_cap, Hkv, lpb, merge_levels);
+  pyramid_leaves_kernel<<<grid, threads, smem, s>>>(keys, summ, lv, N, n_cap, Hkv, lpb, merge_levels, lens);
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (merge_levels + 2 <= lv.L) {
-    pyramid_top_kernel<<<B * Hkv, 256, 0, s>>>(summ, lv, N, Hkv, merge_levels + 2);
+    pyramid_top_kernel<<<B * Hkv, 256, 0, s>>>(summ, lv, N, Hkv, merge_levels + 2, lens, n_cap);
     note_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  if (lengths) {
+  if (lengths && !ragged) {
     fill_lengths_kernel<<<(B + 127) / 128, 128, 0, s>>>(lengths, B, (int)N);
     note_launch();
     e = cudaGetLastError();
