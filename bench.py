@@ -529,8 +529,26 @@ def bench_decode(torch, pisa, synth, dev, args):
     ee.record(stream)
     torch.cuda.synchronize()
     st = pisa.check_device_status(ws)
-    return {"us_per_step": es.elapsed_time(ee) * 1000.0 / steps, "steps": steps, "B": B, "n_ctx": n_ctx,
-            "Hq": Hq, "Hkv": Hkv, "K": K, "status": st}
+    us_eager = es.elapsed_time(ee) * 1000.0 / steps
+    # the same steps captured once in a CUDA graph and replayed (a fresh cache)
+    cache, g = synth.decode_context(B, n_ctx, n_cap, Hkv, seed=2)
+    pyr_g = pisa.Pyramid.allocate(cache.to(dev), with_lengths=True)
+    del cache
+    pisa.build_pyramid(pyr_g, N=n_ctx)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for s in range(steps):
+            pisa.decode_append_and_select(qd[s], kd[s], pyr_g, K, workspace=ws, out=(idx, None), with_scores=False)
+    torch.cuda.synchronize()
+    es.record(stream)
+    graph.replay()
+    ee.record(stream)
+    torch.cuda.synchronize()
+    return {"us_per_step": us_eager, "us_per_step_graph": es.elapsed_time(ee) * 1000.0 / steps, "steps": steps,
+            "B": B, "n_ctx": n_ctx, "Hq": Hq, "Hkv": Hkv, "K": K, "status": st,
+            "status_graph": pisa.check_device_status(ws)}
 
 
 def main():
