@@ -40,9 +40,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
                   "walk": ["walk_mma.cu", "tc.cuh", "common.cuh", "api.cuh"]}
 NCU_TRAFFIC = {
-    ("leaf", "latency-256k"): {"bytes": 1651877000 + 35289600, "src_sha1": "adb4ca081a19cc74d7aa5f88542363dc84fb0c38",
+    ("leaf", "latency-256k"): {"bytes": 1665541000 + 35650048, "src_sha1": "f332ea7cd4719a4dd8d50adacfef0f500bbc3610",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
-    ("walk", "latency-256k"): {"bytes": 1077341000 + 35663104, "src_sha1": "be85c32c29e96b0b39838d8dc0912e8144da4509",
+    ("walk", "latency-256k"): {"bytes": 1076188000 + 35827456, "src_sha1": "47d708aa450c87ad3ae24699c7919e6c9d506aa0",
                                "profile": "profiles/walk_k8_kernel_latency-256k.md"},
 }
 
