@@ -35,6 +35,7 @@ constexpr int kAccBufs = 4;       // TMEM accumulators of 128 fp32 columns
 // Query-row stages (16 KB each), one per accumulator: the stage of tile k is free again
 // once tile k's MMAs have completed, which acc_full already signals.
 constexpr int kLeafStages = kAccBufs;
+static_assert((kAccBufs & (kAccBufs - 1)) == 0, "stage and accumulator indices are taken with a mask");
 constexpr int kLeafWarps = 16;    // key-block loader, MMA, 2 query-row warps, 3 epilogue warpgroups
 constexpr int kEpiGroups = 3;     // epilogue warpgroups (warps 4..15)
 // A warpgroup waits for tile k only after finishing tile k - kEpiGroups, so with
@@ -297,32 +298,42 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
           ++nchg;
         }
       } else {
-        // lane 0 issues the block's tiles; the warp learns of an abort once per block
+        // the whole warp walks the block's tiles and waits on the barriers (so that it stays
+        // converged); lane 0 alone issues the MMAs and their commits, which tcgen05.commit
+        // tracks per issuing thread.  Stage, accumulator and parity come from shifts,
+        // operand descriptors from a base plus an offset (the descriptor's address field
+        // counts 16-byte units; shared memory stays below 2^18 bytes).
         bool w = true;
-        if (lane == 0) {
-          for (int m = 0; m < n && w; ++m) {
-            const int kt = k + m;
-            const int s = kt % kLeafStages, a = kt % kAccBufs;
-            if ((chg >> m) & 1) {
-              if (nchg > 0) umma_commit(&b_empty[cur]);  // fires once the previous block's MMAs are done
-              cur = nchg % kKeyBufs;
-              w = mbar_wait(&b_full[cur], (nchg / kKeyBufs) & 1, abort);
-              ++nchg;
-            }
-            w = w && mbar_wait(&a_full[s], (kt / kLeafStages) & 1, abort);
-            w = w && (kt < kAccBufs || mbar_wait(&acc_empty[a], ((kt / kAccBufs) - 1) & 1, abort));
-            if (w) {
-              tc_fence_after();
-              const uint64_t da = umma_desc_sw128(sA + s * kTileBytes);
-              const uint64_t db = umma_desc_sw128(sB + cur * kTileBytes);
+        const uint64_t da0 = umma_desc_sw128(sA), db0 = umma_desc_sw128(sB);
+        uint64_t db = db0 + (uint64_t)(cur * (kTileBytes >> 4));
+        for (int m = 0; m < n && w; ++m) {
+          const unsigned kt = (unsigned)(k + m);
+          const unsigned s = kt & (kAccBufs - 1), ph = (kt / kAccBufs) & 1;
+          if ((chg >> m) & 1) {  // warp-uniform (a ballot)
+            if (nchg > 0 && lane == 0) umma_commit(&b_empty[cur]);  // fires once the previous block's MMAs are done
+            cur = nchg % kKeyBufs;
+            db = db0 + (uint64_t)(cur * (kTileBytes >> 4));
+            w = mbar_wait(&b_full[cur], (nchg / kKeyBufs) & 1, abort);
+            ++nchg;
+          }
+          w = w && mbar_wait(&a_full[s], ph, abort);
+          w = w && (kt < (unsigned)kAccBufs || mbar_wait(&acc_empty[s], ph ^ 1u, abort));
+          w = __all_sync(kFull, w);
+          if (w) {
+            tc_fence_after();
+            if (lane == 0) {
+              const uint64_t da = da0 + (uint64_t)(s * (kTileBytes >> 4));
+              const uint32_t td = tmem + s * 128;
+              umma_bf16_first(td, da, db, idesc);
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + a * 128, da + 2 * kk, db + 2 * kk, idesc, kk > 0);
-              umma_commit(&acc_full[a]);  // also frees the tile's query-row stage
+              for (int kk = 1; kk < 4; ++kk) umma_bf16_acc(td, da + 2 * kk, db + 2 * kk, idesc);
+              umma_commit(&acc_full[s]);  // also frees the tile's query-row stage
             }
+            __syncwarp();
           }
         }
         k += n;
-        ok = __shfl_sync(kFull, w, 0);
+        ok = w;
       }
     }
     if (!ok && lane == 0) leaf_abort(abort, P.status);

@@ -98,6 +98,18 @@ __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t 
       "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
+// The same MMA with the accumulate flag fixed: D = A*B (first k-step) or D += A*B.
+__device__ __forceinline__ void umma_bf16_first(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, 0, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc));
+}
+__device__ __forceinline__ void umma_bf16_acc(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc) {
+  asm volatile(
+      "{ .reg .pred p; setp.eq.b32 p, 0, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc));
+}
+
 // Arrive on `bar` once all tcgen05 operations issued so far by this thread complete.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
