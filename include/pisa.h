@@ -129,6 +129,33 @@ int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t 
                         int causal, int32_t* idx, float* scores, void* ws, size_t ws_bytes,
                         void* stream);
 
+/*
+ * pisa_select_prefill_host -- pisa_build_pyramid + pisa_select_prefill for inputs
+ * and output in host memory, with the transfers overlapped with the selection
+ * ("Block Sparse Attention with Log-Linear Complexity", §3.1 and §3.2; the
+ * computation and its results are exactly those of the two device calls).  The
+ * keys are copied into pyr->keys and the pyramid is built over N tokens; the
+ * queries are copied into Q_dev in runs of query chunks on copy_stream while
+ * `stream` runs the selection of each run as soon as its rows are in, and each
+ * run's indices are copied back as soon as they are final.
+ *   pyr        : device pyramid, n_cap >= N; its keys, summaries and lengths are
+ *                overwritten
+ *   K_host     : host bf16 [B, N, Hkv, d]   (pinned memory for overlap)
+ *   Q_host     : host bf16 [B, N, Hq, d]    (pinned memory for overlap)
+ *   Q_dev      : device bf16 [B, N, Hq, d] staging buffer, 16-byte aligned
+ *   idx_host   : host int32 [B, Hkv, N, K] out (pinned memory for overlap)
+ *   idx_dev    : device int32 [B, Hkv, N, K] staging buffer
+ *   ws         : as for pisa_select_prefill
+ *   copy_stream: stream for the copies (NULL: `stream`, no overlap)
+ * Asynchronous: host buffers must stay valid until the work completes; work
+ * enqueued on `stream` after this call is ordered after all of it, copies
+ * included.  Errors as pisa_select_prefill; PISA_ERR_CUDA if a copy or an event
+ * cannot be enqueued.  Calls are serialised on a library lock while they enqueue.
+ */
+int pisa_select_prefill_host(const pisa_pyramid* pyr, const void* K_host, int64_t N, const void* Q_host,
+                             void* Q_dev, int Hq, int K, int causal, int32_t* idx_host, int32_t* idx_dev,
+                             void* ws, size_t ws_bytes, void* stream, void* copy_stream);
+
 /* Workspace bytes pisa_select_flat needs (0 on bad or unsupported sizes).  It
  * grows as N^2 / C: one fp32 score per (b, kv, query, leaf) plus the tile list. */
 size_t pisa_flat_workspace_bytes(int B, int64_t N, int Hq, int Hkv, int K);

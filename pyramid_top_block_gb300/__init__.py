@@ -66,6 +66,8 @@ def load(path: str | None = None):
     lib.pisa_select_flat.restype = i32
     lib.pisa_select_prefill_ex.argtypes = [vp, i32, vp, i64, i32, i32, vp, vp, vp, sz, vp, i32]
     lib.pisa_select_prefill_ex.restype = i32
+    lib.pisa_select_prefill_host.argtypes = [vp, vp, i64, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp, vp]
+    lib.pisa_select_prefill_host.restype = i32
     lib.pisa_select_flat_ex.argtypes = [vp, i32, vp, i64, i32, i32, vp, vp, vp, sz, vp, i32]
     lib.pisa_select_flat_ex.restype = i32
     lib.pisa_sparse_attention.argtypes = [vp, i32, vp, vp, i32, i64, i32, vp, i32, i32, vp, vp]
@@ -228,6 +230,52 @@ def select_prefill(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True, N
                                       int(mode)),
            "pisa_select_prefill_ex")
     return idx, scores
+
+
+_COPY_STREAMS: dict = {}
+
+
+def select_prefill_host(q_host: torch.Tensor, k_host: torch.Tensor, pyr: Pyramid, K: int, causal: bool = True,
+                        idx_host: torch.Tensor | None = None, q_dev: torch.Tensor | None = None,
+                        idx_dev: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                        stream=None, copy_stream=None) -> torch.Tensor:
+    """Pyramid build + prefill selection for host-resident Q [B, N, Hq, 64] and K
+    [B, N, Hkv, 64] (bf16, pinned for overlap): the library copies K into pyr.keys and
+    Q into q_dev in runs of query chunks on copy_stream while `stream` selects, and
+    copies each run's indices back into idx_host [B, Hkv, N, K] (int32, pinned) as soon
+    as they are final.  Asynchronous: synchronise `stream` before reading idx_host.
+    The device staging buffers are allocated here when not given.
+    """
+    if q_host.dtype != torch.bfloat16 or k_host.dtype != torch.bfloat16 or q_host.is_cuda or k_host.is_cuda:
+        raise ValueError("q_host and k_host must be host bf16 tensors")
+    if q_host.dim() != 4 or k_host.dim() != 4 or not q_host.is_contiguous() or not k_host.is_contiguous():
+        raise ValueError("q_host [B, N, Hq, d] and k_host [B, N, Hkv, d] must be contiguous")
+    B, N, Hq, _ = q_host.shape
+    if k_host.shape[0] != B or k_host.shape[1] != N or k_host.shape[2] != pyr.Hkv:
+        raise ValueError("k_host must be [B, N, Hkv, d] with the pyramid's B and Hkv")
+    dev = pyr.keys.device
+    lib = load()
+    need = lib.pisa_select_workspace_bytes(B, N, Hq, pyr.Hkv, K)
+    if need == 0:
+        _check(2, "pisa_select_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if q_dev is None:
+        q_dev = torch.empty(B, N, Hq, q_host.shape[3], dtype=torch.bfloat16, device=dev)
+    if idx_dev is None:
+        idx_dev = torch.empty(B, pyr.Hkv, N, K, dtype=torch.int32, device=dev)
+    if idx_host is None:
+        idx_host = torch.empty(B, pyr.Hkv, N, K, dtype=torch.int32, pin_memory=True)
+    if copy_stream is None:  # a side stream of the library's own, one per device
+        copy_stream = _COPY_STREAMS.get(dev.index)
+        if copy_stream is None:
+            copy_stream = _COPY_STREAMS[dev.index] = torch.cuda.Stream(device=dev)
+    st = pyr.struct()
+    _check(lib.pisa_select_prefill_host(ctypes.byref(st), _ptr(k_host), N, _ptr(q_host), _ptr(q_dev), Hq, K,
+                                        int(causal), _ptr(idx_host), _ptr(idx_dev), _ptr(workspace),
+                                        workspace.numel(), _stream(stream), _stream(copy_stream)),
+           "pisa_select_prefill_host")
+    return idx_host
 
 
 def flat_workspace_bytes(B: int, N: int, Hq: int, Hkv: int, K: int) -> int:

@@ -25,6 +25,8 @@ struct LeafTcLaunch {
   int B, Hq, Hkv, K, causal;
   long long N, n_cap;
   int M2, nchunks, chunk_shift, nb;
+  long long t0, t1;  // query positions of this launch: whole query chunks (or up to N)
+  int b0, b1;        // their buckets
   const int32_t* surv;
   int* count;
   const int32_t* srank;  // rank of each survivor inside its bucket (from the walk)
@@ -64,8 +66,10 @@ struct WalkLaunch {
   int32_t* surv;
   int32_t* srank;  // rank of each survivor inside its bucket (the bucket count before it)
   int* count;
-  int nchunks, chunk_shift, M2;
+  int nchunks, chunk_shift, M2;  // buckets are chunk-major: ((t >> chunk_shift) * B * Hkv + b * Hkv + kv) * M2 + p
   int mode;  // block score: 0 LSE, 1 mean of the child logits, 2 mean + variance / 2
+  long long t0, t1;  // the query positions walked by this launch
+  bool build_table;  // build the route table first (once per pyramid state)
 };
 
 long long route_rows_per_bh(const Levels& lv);

@@ -28,10 +28,14 @@ __global__ void flat_list_kernel(uint32_t* __restrict__ list, long long N) {
 }
 
 // Tile i of (b, kv) = i / T1: {first position, rows, key block p, b * Hkv + kv}.
+// total[0..1] = {0, tile count}: the leaf kernel's tile range.
 __global__ void flat_desc_kernel(int4* __restrict__ desc, int* __restrict__ total, long long T1, int BH,
                                  long long N, int R, int u, long long M2, int causal) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i == 0) *total = (int)(T1 * BH);
+  if (i == 0) {
+    total[0] = 0;
+    total[1] = (int)(T1 * BH);
+  }
   if (i >= T1 * BH) return;
   const int bh = (int)(i / T1);
   const long long j = i % T1;
@@ -133,7 +137,8 @@ cudaError_t launch_select_flat(const LeafTcLaunch& L, long long T1, long long st
   if (e != cudaSuccess) return e;
   LeafTcLaunch F = L;
   F.tile_off = total;
-  F.nb = 0;
+  F.b0 = 0;
+  F.b1 = 1;
   e = launch_leaf_tc_kernel(F, 1, stride, s);
   if (e != cudaSuccess) return e;
   const long long jobs = (long long)BH * L.N;

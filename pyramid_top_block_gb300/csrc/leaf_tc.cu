@@ -58,7 +58,7 @@ struct LeafTcParams {
   const int* bucket_off;
   const int* tile_off;
   const int4* tile_desc;  // per tile: first entry, rows, level-2 survivor p, b * Hkv + kv
-  int nb;
+  int b0, b1;  // the buckets of this launch; their tiles are tile_off[b0] .. tile_off[b1] - 1
   int Hq, Hkv, G, Gp, R, K;
   long long N, n_cap;
   int M2, nchunks;
@@ -255,7 +255,9 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   const int Gp = P.Gp, G = P.G;
-  const int total = __ldg(P.tile_off + P.nb);
+  const int first = __ldg(P.tile_off + P.b0);
+  const int total = __ldg(P.tile_off + P.b1) - first;
+  const int4* __restrict__ tdesc = P.tile_desc + first;
   int my_tiles = 0;
   for (int blk = blockIdx.x; blk * kTileBlock < total; blk += gridDim.x) my_tiles += min(kTileBlock, total - blk * kTileBlock);
 
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
     for (int blk = blockIdx.x; ok && blk * kTileBlock < total; blk += gridDim.x) {
       const int i0 = blk * kTileBlock;
       const int n = min(kTileBlock, total - i0);
-      const int4 d = lane < n ? __ldg(P.tile_desc + i0 + lane) : make_int4(0, 0, -1, -1);
+      const int4 d = lane < n ? __ldg(tdesc + i0 + lane) : make_int4(0, 0, -1, -1);
       int pp = __shfl_up_sync(kFull, d.z, 1), pb = __shfl_up_sync(kFull, d.w, 1);
       if (lane == 0) {
         pp = prev_p;
@@ -349,15 +351,15 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
     // descriptors are read two tiles ahead and the entries one tile ahead.
     const int tw = warp - 2;
     int4 d1 = make_int4(0, 0, 0, 0), d2 = make_int4(0, 0, 0, 0);
-    if (tw < my_tiles) d1 = __ldg(P.tile_desc + tile_of(tw));
-    if (tw + 2 < my_tiles) d2 = __ldg(P.tile_desc + tile_of(tw + 2));
+    if (tw < my_tiles) d1 = __ldg(tdesc + tile_of(tw));
+    if (tw + 2 < my_tiles) d2 = __ldg(tdesc + tile_of(tw + 2));
     uint32_t e1 = lane < d1.y ? __ldg(P.list + d1.x + lane) : 0u;
     for (int k = tw; k < my_tiles; k += 2) {
       const int4 d = d1;
       const uint32_t ent = e1;
       d1 = d2;
       e1 = (k + 2 < my_tiles && lane < d1.y) ? __ldg(P.list + d1.x + lane) : 0u;
-      if (k + 4 < my_tiles) d2 = __ldg(P.tile_desc + tile_of(k + 4));
+      if (k + 4 < my_tiles) d2 = __ldg(tdesc + tile_of(k + 4));
       const int s = k % kLeafStages;
       bool w = true;
       if (lane == 0) {
@@ -380,13 +382,13 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const int r = row / Gp, h = row % Gp;
-    int4 dn = wg < my_tiles ? __ldg(P.tile_desc + tile_of(wg)) : make_int4(0, 0, 0, 0);
+    int4 dn = wg < my_tiles ? __ldg(tdesc + tile_of(wg)) : make_int4(0, 0, 0, 0);
     for (int k = wg; k < my_tiles; k += kEpiGroups) {
       const int a = k % kAccBufs;
       const int4 d = dn;  // this tile's descriptor (read one tile ahead)
       const bool qvalid = r < d.y;
       const uint32_t ent = qvalid ? __ldg(P.list + d.x + r) : 0u;
-      if (k + kEpiGroups < my_tiles) dn = __ldg(P.tile_desc + tile_of(k + kEpiGroups));
+      if (k + kEpiGroups < my_tiles) dn = __ldg(tdesc + tile_of(k + kEpiGroups));
       const bool ok = __all_sync(kFull, mbar_wait(&acc_full[a], (k / kAccBufs) & 1, abort));
       if (!ok) {  // warp-uniform exit
         leaf_abort(abort, P.status);
@@ -456,35 +458,45 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
 
 // ------------------------------------------------------------ bucketing
 
-__device__ __forceinline__ int bucket_of(long long job, int p, long long N, int nchunks, int chunk_shift, int M2) {
+// Buckets are chunk-major, (query chunk, b * Hkv + kv, level-2 node p), so that the buckets
+// and tiles of a run of query chunks are contiguous.
+__device__ __forceinline__ int bucket_of(long long job, int p, long long N, int BH, int chunk_shift, int M2) {
   const long long t = job % N;
   const long long bkv = job / N;
-  return (int)((bkv * nchunks + (t >> chunk_shift)) * M2 + p);
+  return (int)(((t >> chunk_shift) * BH + bkv) * M2 + p);
 }
 
-__global__ void leaf_scatter_kernel(const int32_t* __restrict__ surv, long long entries, int K, long long N,
-                                    int nchunks, int chunk_shift, int M2, const int* __restrict__ bucket_off,
+// Entries of query positions [t0, t1) of every (b, kv): e = ((b * Hkv + kv) * N + t) * K + slot.
+__global__ void leaf_scatter_kernel(const int32_t* __restrict__ surv, long long t0, long long t1, int BH, int K,
+                                    long long N, int chunk_shift, int M2, const int* __restrict__ bucket_off,
                                     const int32_t* __restrict__ srank, uint32_t* __restrict__ list) {
-  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= entries) return;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long per_bh = (t1 - t0) * K;
+  if (i >= per_bh * BH) return;
+  const long long e = ((i / per_bh) * N + t0) * K + i % per_bh;
   const int p = surv[e];
   if (p < 0) return;
   const long long job = e / K;
-  const int bkt = bucket_of(job, p, N, nchunks, chunk_shift, M2);
+  const int bkt = bucket_of(job, p, N, BH, chunk_shift, M2);
   const int pos = bucket_off[bkt] + srank[e];
   list[pos] = ((uint32_t)(job % N) << 5) | (uint32_t)(e % K);
 }
 
 // Exclusive scans of the bucket sizes (entries) and of their tile counts
-// ceil(size / R).  One CTA of 1024 threads sweeps the buckets in tiles of 4096,
-// each thread four consecutive buckets (coalesced), warp shuffles and one shared
-// array for the in-tile scan, a running carry between tiles.
-__global__ void __launch_bounds__(1024) leaf_scan_kernel(const int* __restrict__ count, int nb, int R,
+// ceil(size / R) over buckets [0, nb) of the pointers given, continuing from the
+// offsets already at bucket_off[0] / tile_off[0] (zero when `first`).  One CTA of
+// 1024 threads sweeps the buckets in tiles of 4096, each thread four consecutive
+// buckets (coalesced), warp shuffles and one shared array for the in-tile scan, a
+// running carry between tiles.
+__global__ void __launch_bounds__(1024) leaf_scan_kernel(const int* __restrict__ count, int nb, int R, int first,
                                                           int* __restrict__ bucket_off, int* __restrict__ tile_off) {
   __shared__ int we[32], wt[32];
   __shared__ int carry[2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) carry[0] = carry[1] = 0;
+  if (tid == 0) {
+    carry[0] = first ? 0 : bucket_off[0];
+    carry[1] = first ? 0 : tile_off[0];
+  }
   __syncthreads();
   for (int base = 0; base < nb; base += 4096) {
     const int i = base + 4 * tid;
@@ -549,24 +561,28 @@ __global__ void __launch_bounds__(1024) leaf_scan_kernel(const int* __restrict__
   }
 }
 
-// Descriptor of leaf tile i: its bucket is the largest bucket whose first tile is
-// <= i; {first entry, rows, level-2 survivor p, b * Hkv + kv}.
-__global__ void leaf_tile_desc_kernel(const int* __restrict__ tile_off, const int* __restrict__ bucket_off, int nb,
-                                      long long max_tiles, int R, int M2, int nchunks, int4* __restrict__ desc) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= max_tiles || i >= tile_off[nb]) return;
-  const int bkt = find_bucket(tile_off, nb, (int)i);
+// Descriptor of leaf tile i among the tiles of buckets [b0, b1): its bucket is the
+// largest one whose first tile is <= i; {first entry, rows, level-2 survivor p,
+// b * Hkv + kv}.
+__global__ void leaf_tile_desc_kernel(const int* __restrict__ tile_off, const int* __restrict__ bucket_off, int b0,
+                                      int b1, long long max_tiles, int R, int M2, int BH, int4* __restrict__ desc) {
+  const long long i = tile_off[b0] + (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= tile_off[b0] + max_tiles || i >= tile_off[b1]) return;
+  const int bkt = b0 + find_bucket(tile_off + b0, b1 - b0, (int)i);
   const int e0 = bucket_off[bkt] + ((int)i - tile_off[bkt]) * R;
   const int nrows = min(R, bucket_off[bkt + 1] - e0);
-  desc[i] = make_int4(e0, nrows, bkt % M2, bkt / M2 / nchunks);
+  desc[i] = make_int4(e0, nrows, bkt % M2, (bkt / M2) % BH);
 }
 
 // Final Top-K per (b, kv, t) over the leaf candidates (children of the level-2
 // survivors, ascending); ineligible children carry -inf and are skipped.
+// Jobs (b * Hkv + kv) * N + t for t in [t0, t1).
 __global__ void leaf_final_kernel(const int32_t* __restrict__ surv, const float* __restrict__ leaf_scores,
-                                  long long jobs, int K, int32_t* __restrict__ idx, float* __restrict__ scores) {
-  const long long job = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (job >= jobs) return;
+                                  long long t0, long long t1, int BH, long long N, int K, int32_t* __restrict__ idx,
+                                  float* __restrict__ scores) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (t1 - t0) * BH) return;
+  const long long job = (i / (t1 - t0)) * N + t0 + i % (t1 - t0);
   const int32_t* s2 = surv + job * K;
   const float* ls = leaf_scores + job * 2 * K;
   int cid[2 * kMaxK];
@@ -676,7 +692,8 @@ cudaError_t launch_leaf_tc_kernel(const LeafTcLaunch& L, int flat, long long fla
   P.bucket_off = L.bucket_off;
   P.tile_off = L.tile_off;
   P.tile_desc = L.tile_desc;
-  P.nb = L.nb;
+  P.b0 = L.b0;
+  P.b1 = L.b1;
   P.Hkv = L.Hkv;
   P.G = G;
   P.Gp = Gp;
@@ -695,21 +712,27 @@ cudaError_t launch_leaf_tc_kernel(const LeafTcLaunch& L, int flat, long long fla
   return cudaGetLastError();
 }
 
+// The leaf level of the prefill selection for query positions [L.t0, L.t1), whose
+// buckets are [L.b0, L.b1) (whole query chunks, chunk-major buckets).
 cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
-  const long long entries = (long long)L.B * L.Hkv * L.N * L.K;
+  if (L.t1 <= L.t0) return cudaSuccess;
+  const int BH = L.B * L.Hkv;
+  const long long span = L.t1 - L.t0;
+  const long long entries = (long long)BH * span * L.K;
   const int G = L.Hq / L.Hkv;
   const int Gp = G < 8 ? 8 : G;
   const int R = 128 / Gp;
-  const unsigned eg = (unsigned)((entries + 255) / 256);
   // bucket sizes were counted by the walk kernel as it wrote the survivors
-  leaf_scan_kernel<<<1, 1024, 0, s>>>(L.count, L.nb, R, L.bucket_off, L.tile_off);
+  leaf_scan_kernel<<<1, 1024, 0, s>>>(L.count + L.b0, L.b1 - L.b0, R, L.b0 == 0, L.bucket_off + L.b0,
+                                      L.tile_off + L.b0);
   note_launch();
-  leaf_scatter_kernel<<<eg, 256, 0, s>>>(L.surv, entries, L.K, L.N, L.nchunks, L.chunk_shift, L.M2, L.bucket_off,
-                                         L.srank, L.list);
+  leaf_scatter_kernel<<<(unsigned)((entries + 255) / 256), 256, 0, s>>>(
+      L.surv, L.t0, L.t1, BH, L.K, L.N, L.chunk_shift, L.M2, L.bucket_off, L.srank, L.list);
   note_launch();
-  leaf_tile_desc_kernel<<<(unsigned)((L.max_tiles + 255) / 256), 256, 0, s>>>(L.tile_off, L.bucket_off, L.nb,
-                                                                               L.max_tiles, R, L.M2, L.nchunks,
-                                                                               L.tile_desc);
+  // a tile holds R >= 8 entries of one bucket: at most entries / 8 + (buckets) tiles
+  const long long max_tiles = entries / 8 + (L.b1 - L.b0) + 1;
+  leaf_tile_desc_kernel<<<(unsigned)((max_tiles + 255) / 256), 256, 0, s>>>(L.tile_off, L.bucket_off, L.b0, L.b1,
+                                                                          max_tiles, R, L.M2, BH, L.tile_desc);
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -718,9 +741,8 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
   e = launch_leaf_tc_kernel(L, 0, 0, s);
   if (e != cudaSuccess) return e;
   mark_phase(4, s);
-  const long long jobs = (long long)L.B * L.Hkv * L.N;
-  leaf_final_kernel<<<(unsigned)((jobs + 127) / 128), 128, 0, s>>>(L.surv, L.leaf_scores, jobs, L.K, L.idx,
-                                                                   L.scores);
+  leaf_final_kernel<<<(unsigned)((BH * span + 127) / 128), 128, 0, s>>>(L.surv, L.leaf_scores, L.t0, L.t1, BH, L.N,
+                                                                       L.K, L.idx, L.scores);
   note_launch();
   e = cudaGetLastError();
   mark_phase(5, s);

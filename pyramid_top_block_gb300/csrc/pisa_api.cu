@@ -2,7 +2,12 @@
 // layout and launch sequencing.  No allocation, no exceptions, one stream.
 #include <atomic>
 #include <cmath>
+#include <cstdint>
 #include <cstring>
+
+#include <algorithm>
+#include <mutex>
+#include <vector>
 
 #include "api.cuh"
 
@@ -208,8 +213,17 @@ size_t pisa_select_workspace_bytes(int B, int64_t N, int Hq, int Hkv, int K) {
   return prefill_layout(B, N, Hkv, K).total;
 }
 
-static int select_prefill_impl(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
-                               int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream, int mode) {
+// The launch descriptions of one prefill selection (buffers are workspace slices);
+// the query range and bucket range are set per stage.
+struct PrefillPlan {
+  Levels lv;
+  PrefillWs w;
+  WalkLaunch W;
+  LeafTcLaunch L;
+};
+
+static int prefill_check(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int mode, const void* idx,
+                         const void* ws, size_t ws_bytes) {
   if (mode < 0 || mode > 2) return PISA_ERR_UNSUPPORTED;
   int st = check_pyr(pyr);
   if (st) return st;
@@ -222,17 +236,20 @@ static int select_prefill_impl(const void* Q, int Hq, const pisa_pyramid* pyr, i
   const PrefillWs w = prefill_layout(pyr->B, N, pyr->Hkv, K);
   if (w.nb >= (1LL << 31) || (long long)pyr->B * pyr->n_cap >= (1LL << 31)) return PISA_ERR_UNSUPPORTED;
   if (ws_bytes < w.total) return PISA_ERR_WORKSPACE_TOO_SMALL;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return PISA_OK;
+}
+
+static void prefill_plan(PrefillPlan& P, const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
+                         int32_t* idx, float* scores, void* ws, int mode) {
+  P.lv = make_levels(N, pyr->n_cap);
+  P.w = prefill_layout(pyr->B, N, pyr->Hkv, K);
+  const PrefillWs& w = P.w;
   char* base = static_cast<char*>(ws);
-  cudaError_t e = cudaMemsetAsync(base, 0, w.zero_bytes, s);
-  if (e != cudaSuccess) return PISA_ERR_CUDA;
-  const Levels lv = make_levels(N, pyr->n_cap);
   int32_t* surv = reinterpret_cast<int32_t*>(base + w.surv);
-  mark_phase(0, s);
-  WalkLaunch W;
+  WalkLaunch& W = P.W;
   W.Q = static_cast<const __nv_bfloat16*>(Q);
   W.summ = pyr->summaries;
-  W.lv = &lv;
+  W.lv = &P.lv;
   W.N = N;
   W.B = pyr->B;
   W.Hq = Hq;
@@ -247,10 +264,10 @@ static int select_prefill_impl(const void* Q, int Hq, const pisa_pyramid* pyr, i
   W.chunk_shift = w.chunk_shift;
   W.M2 = w.M2;
   W.mode = mode;
-  e = launch_prefill_walk_mma(W, s);
-  if (e != cudaSuccess) return PISA_ERR_CUDA;
-  mark_phase(2, s);
-  LeafTcLaunch L;
+  W.t0 = 0;
+  W.t1 = N;
+  W.build_table = true;
+  LeafTcLaunch& L = P.L;
   L.Q = static_cast<const __nv_bfloat16*>(Q);
   L.keys = static_cast<const __nv_bfloat16*>(pyr->keys);
   L.B = pyr->B;
@@ -277,7 +294,144 @@ static int select_prefill_impl(const void* Q, int Hq, const pisa_pyramid* pyr, i
   L.scores = scores;
   L.status = reinterpret_cast<int*>(base + w.status);
   L.mode = mode;
-  return cuda_status(launch_prefill_leaf_tc(L, s));
+  L.t0 = 0;
+  L.t1 = N;
+  L.b0 = 0;
+  L.b1 = (int)w.nb;
+}
+
+// Query chunks [c0, c1) of a planned selection: walk, bucketing, leaf level, final
+// Top-K.  Buckets are chunk-major, so the chunks' buckets are one contiguous range.
+static cudaError_t prefill_stage(PrefillPlan& P, int c0, int c1, bool build_table, cudaStream_t s) {
+  const long long BHM = (long long)P.L.B * P.L.Hkv * P.w.M2;
+  const long long t0 = (long long)c0 << P.w.chunk_shift;
+  const long long t1 = std::min((long long)c1 << P.w.chunk_shift, (long long)P.W.N);
+  P.W.t0 = P.L.t0 = t0;
+  P.W.t1 = P.L.t1 = t1;
+  P.W.build_table = build_table;
+  P.L.b0 = (int)(c0 * BHM);
+  P.L.b1 = (int)(c1 * BHM);
+  cudaError_t e = launch_prefill_walk_mma(P.W, s);
+  if (e != cudaSuccess) return e;
+  mark_phase(2, s);
+  return launch_prefill_leaf_tc(P.L, s);
+}
+
+static int select_prefill_impl(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,
+                               int32_t* idx, float* scores, void* ws, size_t ws_bytes, void* stream, int mode) {
+  const int st = prefill_check(Q, Hq, pyr, N, K, mode, idx, ws, ws_bytes);
+  if (st) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PrefillPlan P;
+  prefill_plan(P, Q, Hq, pyr, N, K, causal, idx, scores, ws, mode);
+  cudaError_t e = cudaMemsetAsync(ws, 0, P.w.zero_bytes, s);
+  if (e != cudaSuccess) return PISA_ERR_CUDA;
+  mark_phase(0, s);
+  return cuda_status(prefill_stage(P, 0, P.w.nchunks, true, s));
+}
+
+// Events of the host-buffer pipeline, kept per device and reused from call to call:
+// a stream wait captures the event's latest record at the time of the wait, so a
+// later call re-recording it cannot disturb waits already enqueued.  The lock is
+// held while a call enqueues its work.
+constexpr int kHostStages = 16;  // query stages the transfers are split into
+static std::mutex g_host_mu;
+static std::vector<cudaEvent_t> g_host_ev[64];
+
+// `height` rows of `width` bytes: one pitched copy, or one copy per row where the
+// pitch is beyond what a pitched copy accepts (or there is a single row).
+static cudaError_t copy_rows(void* dst, size_t dpitch, const void* src, size_t spitch, size_t width, size_t height,
+                             cudaMemcpyKind kind, cudaStream_t s) {
+  if (height == 1) return cudaMemcpyAsync(dst, src, width, kind, s);
+  if (dpitch <= (size_t)INT32_MAX && spitch <= (size_t)INT32_MAX)
+    return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, kind, s);
+  for (size_t r = 0; r < height; ++r) {
+    const cudaError_t e = cudaMemcpyAsync(static_cast<char*>(dst) + r * dpitch,
+                                          static_cast<const char*>(src) + r * spitch, width, kind, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+static cudaEvent_t* host_events(int dev, int n) {
+  std::vector<cudaEvent_t>& v = g_host_ev[dev];
+  while ((int)v.size() < n) {
+    cudaEvent_t ev;
+    if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    v.push_back(ev);
+  }
+  return v.data();
+}
+
+int pisa_select_prefill_host(const pisa_pyramid* pyr, const void* K_host, int64_t N, const void* Q_host,
+                             void* Q_dev, int Hq, int K, int causal, int32_t* idx_host, int32_t* idx_dev,
+                             void* ws, size_t ws_bytes, void* stream, void* copy_stream) {
+  int st = prefill_check(Q_dev, Hq, pyr, N, K, 0, idx_dev, ws, ws_bytes);
+  if (st) return st;
+  if (!K_host || !Q_host || !idx_host || N < 1) return PISA_ERR_INVALID_ARG;
+  if (N > (1LL << 27) || pyr->n_cap > (1LL << 27)) return PISA_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PISA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStream_t c = copy_stream ? static_cast<cudaStream_t>(copy_stream) : s;
+  PrefillPlan P;
+  prefill_plan(P, Q_dev, Hq, pyr, N, K, causal, idx_dev, nullptr, ws, 0);
+  const int nch = P.w.nchunks;
+  const int per = (nch + kHostStages - 1) / kHostStages;  // query chunks per stage
+  const int ns = (nch + per - 1) / per;
+  const int BH = pyr->B * pyr->Hkv;
+  const size_t qrow = (size_t)Hq * kD * 2, krow = (size_t)pyr->Hkv * kD * 2, irow = (size_t)K * 4;
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  cudaEvent_t* ev = host_events(dev, 2 * ns + 2);
+  if (!ev) return PISA_ERR_CUDA;
+  cudaEvent_t e_keys = ev[0], e_done = ev[1 + 2 * ns];
+  auto stage_t = [&](int i, long long& t0, long long& t1) {
+    t0 = (long long)(i * per) << P.w.chunk_shift;
+    t1 = std::min((long long)std::min((i + 1) * per, nch) << P.w.chunk_shift, (long long)N);
+  };
+  cudaError_t e = cudaSuccess;
+  auto ok = [&](cudaError_t r) {
+    if (e == cudaSuccess) e = r;
+    return e == cudaSuccess;
+  };
+  // copy stream: the keys, then the query rows stage by stage
+  ok(copy_rows(pyr->keys, (size_t)pyr->n_cap * krow, K_host, (size_t)N * krow, (size_t)N * krow, pyr->B,
+               cudaMemcpyHostToDevice, c));
+  ok(cudaEventRecord(e_keys, c));
+  for (int i = 0; i < ns; ++i) {
+    long long t0, t1;
+    stage_t(i, t0, t1);
+    ok(copy_rows(static_cast<char*>(Q_dev) + t0 * qrow, (size_t)N * qrow, static_cast<const char*>(Q_host) + t0 * qrow,
+                 (size_t)N * qrow, (size_t)(t1 - t0) * qrow, pyr->B, cudaMemcpyHostToDevice, c));
+    ok(cudaEventRecord(ev[1 + i], c));
+  }
+  // compute stream: pyramid and route table once the keys are in, then each stage
+  // once its query rows are in
+  ok(cudaStreamWaitEvent(s, e_keys, 0));
+  ok(cudaMemsetAsync(ws, 0, P.w.zero_bytes, s));
+  ok(launch_build_pyramid(static_cast<const __nv_bfloat16*>(pyr->keys), pyr->summaries, P.lv, N, pyr->n_cap, pyr->B,
+                          pyr->Hkv, pyr->lengths, s));
+  P.W.t0 = P.W.t1 = 0;
+  P.W.build_table = true;
+  ok(launch_prefill_walk_mma(P.W, s));
+  for (int i = 0; i < ns && e == cudaSuccess; ++i) {
+    ok(cudaStreamWaitEvent(s, ev[1 + i], 0));
+    ok(prefill_stage(P, i * per, std::min((i + 1) * per, nch), false, s));
+    ok(cudaEventRecord(ev[1 + ns + i], s));
+  }
+  // copy stream: each stage's indices once the stage is done; the compute stream
+  // then waits for the last copy, so work queued on it after this call sees them
+  for (int i = 0; i < ns && e == cudaSuccess; ++i) {
+    long long t0, t1;
+    stage_t(i, t0, t1);
+    ok(cudaStreamWaitEvent(c, ev[1 + ns + i], 0));
+    ok(copy_rows(reinterpret_cast<char*>(idx_host) + t0 * irow, (size_t)N * irow,
+                 reinterpret_cast<const char*>(idx_dev) + t0 * irow, (size_t)N * irow, (size_t)(t1 - t0) * irow, BH,
+                 cudaMemcpyDeviceToHost, c));
+  }
+  ok(cudaEventRecord(e_done, c));
+  ok(cudaStreamWaitEvent(s, e_done, 0));
+  return e == cudaSuccess ? PISA_OK : PISA_ERR_CUDA;
 }
 
 int pisa_select_prefill(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int causal,

@@ -180,7 +180,7 @@ __device__ __forceinline__ Kids kids_of(int l, int c, int Mc, int n, int t, bool
 __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
     const __nv_bfloat16* __restrict__ Q, const float* __restrict__ summ, const unsigned char* __restrict__ table,
     Levels lv, RowOffsets ro, long long rows_per_bh, int N, int Hq, int Hkv, int K, int causal, int l_start,
-    int l_lo, int32_t* __restrict__ surv, int32_t* __restrict__ srank, int* __restrict__ count, int nchunks,
+    int l_lo, int32_t* __restrict__ surv, int32_t* __restrict__ srank, int* __restrict__ count, int t0, int t1,
     int chunk_shift, int M2, int mode) {
   extern __shared__ __align__(16) unsigned char wsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
   constexpr float kL2e = 1.4426950408889634f;
   constexpr float kLn2 = 0.69314718055994531f;
 
-  for (int t = blockIdx.x + gridDim.x * warp; t < N; t += gridDim.x * kWalkWarps) {
+  for (int t = t0 + blockIdx.x + gridDim.x * warp; t < t1; t += gridDim.x * kWalkWarps) {
     const long long job = bh * N + t;
     const int kv = (int)(bh % Hkv);
     const long long b = bh / Hkv;
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
       int p = -1;
       if (lane < nS) p = S.cand[S.sel[lane]];
       out[lane] = p;
-      if (p >= 0) srank[job * K + lane] = atomicAdd(count + ((bh * nchunks + (t >> chunk_shift)) * M2 + p), 1);
+      if (p >= 0) srank[job * K + lane] = atomicAdd(count + (((long long)(t >> chunk_shift) * gridDim.y + bh) * M2 + p), 1);
     }
     __syncwarp();
   }
@@ -539,7 +539,7 @@ template <int NT, int MODE>
 __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
     const __nv_bfloat16* __restrict__ Q, const unsigned char* __restrict__ table, Levels lv, RowOffsets ro,
     LevelTail tail, long long rows_per_bh, int N, int Hq, int Hkv, int K, int causal, int l_start, int l_lo,
-    int32_t* __restrict__ surv, int32_t* __restrict__ srank, int* __restrict__ count, int nchunks, int chunk_shift,
+    int32_t* __restrict__ surv, int32_t* __restrict__ srank, int* __restrict__ count, int t0, int t1, int chunk_shift,
     int M2) {
   extern __shared__ __align__(16) unsigned char wsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -586,12 +586,12 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
   const unsigned lt = (1u << lane) - 1u;
   constexpr unsigned kLo = 0x11111111u, kHi = 0x22222222u;  // lanes owning candidates 0..7 / 8..15 (j = 0 / 1)
 
-  for (int t = blockIdx.x + gridDim.x * warp; t < N; t += gridDim.x * kWalkWarps) {
+  for (int t = t0 + blockIdx.x + gridDim.x * warp; t < t1; t += gridDim.x * kWalkWarps) {
     __syncwarp();  // the previous query's reads of the candidate buffers are done
     const long long job = bh * N + t;
     int32_t* out = surv + job * K;
     int32_t* rk = srank + job * K;  // a survivor's rank in its bucket: the count before it
-    int* cnt = count + (bh * nchunks + (t >> chunk_shift)) * M2;
+    int* cnt = count + ((long long)(t >> chunk_shift) * gridDim.y + bh) * M2;  // chunk-major buckets
     if (l_start < 2) {
       // at most K nodes at level 2: every eligible level-2 node survives unscored
       const int m2 = lv.L >= 2 ? lv.M[2] : 1;
@@ -815,12 +815,16 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
       l_start = l;
       break;
     }
-  const long long thr = (long long)BH * rows * 32;
-  route_table_kernel<<<(unsigned)((thr + 255) / 256), 256, 0, s>>>(W.summ, lv, W.N, BH, rows, ro, l_start, W.table);
-  note_launch();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  mark_phase(1, s);
+  cudaError_t e = cudaSuccess;
+  if (W.build_table) {
+    const long long thr = (long long)BH * rows * 32;
+    route_table_kernel<<<(unsigned)((thr + 255) / 256), 256, 0, s>>>(W.summ, lv, W.N, BH, rows, ro, l_start, W.table);
+    note_launch();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    mark_phase(1, s);
+  }
+  if (W.t1 <= W.t0) return cudaSuccess;
   // the rows of levels [l_lo, l_start] (at most kCacheRows) are cached in shared memory
   int l_lo = l_start + 1, crows = 0;
   while (l_start >= 2 && l_lo - 1 >= 2 && crows + lv.M[l_lo - 1] <= kCacheRows) {
@@ -829,7 +833,7 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
   }
   // CTAs per (b, kv): about 3 resident CTAs per SM over the whole grid
   int per_bh = (int)((3LL * 152 + BH - 1) / BH);
-  if (per_bh > W.N) per_bh = (int)W.N;
+  if (per_bh > W.t1 - W.t0) per_bh = (int)(W.t1 - W.t0);
   if (per_bh < 1) per_bh = 1;
   dim3 grid((unsigned)per_bh, (unsigned)BH);
   const int G = W.Hq / W.Hkv;
@@ -866,8 +870,8 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
       }
     }
     kern<<<grid, kWalkWarps * 32, smem, s>>>(W.Q, W.table, lv, ro, tail, rows, (int)W.N, W.Hq, W.Hkv, W.K, W.causal,
-                                              l_start, l_lo, W.surv, W.srank, W.count, W.nchunks, W.chunk_shift,
-                                              W.M2);
+                                              l_start, l_lo, W.surv, W.srank, W.count, (int)W.t0, (int)W.t1,
+                                              W.chunk_shift, W.M2);
     note_launch();
     return cudaGetLastError();
   }
@@ -884,7 +888,7 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
   }
   walk_mma_kernel<<<grid, kWalkWarps * 32, smem, s>>>(W.Q, W.summ, W.table, lv, ro, rows, (int)W.N, W.Hq, W.Hkv, W.K,
                                                        W.causal, l_start, l_lo, W.surv, W.srank, W.count,
-                                                       W.nchunks, W.chunk_shift, W.M2, W.mode);
+                                                       (int)W.t0, (int)W.t1, W.chunk_shift, W.M2, W.mode);
   note_launch();
   return cudaGetLastError();
 }
