@@ -485,30 +485,38 @@ __global__ void leaf_scatter_kernel(const int32_t* __restrict__ surv, long long 
 // Exclusive scans of the bucket sizes (entries) and of their tile counts
 // ceil(size / R) over buckets [0, nb) of the pointers given, continuing from the
 // offsets already at bucket_off[0] / tile_off[0] (zero when `first`).  One CTA of
-// 1024 threads sweeps the buckets in tiles of 4096, each thread four consecutive
-// buckets (coalesced), warp shuffles and one shared array for the in-tile scan, a
-// running carry between tiles.
+// 1024 threads sweeps the buckets in tiles of 1024 * kScanItems, each thread
+// kScanItems consecutive buckets (coalesced), warp shuffles and one shared array
+// for the in-tile scan, a running carry between tiles; each tile's counts are
+// loaded while the previous tile is scanned.
+constexpr int kScanItems = 4;
 __global__ void __launch_bounds__(1024) leaf_scan_kernel(const int* __restrict__ count, int nb, int R, int first,
                                                           int* __restrict__ bucket_off, int* __restrict__ tile_off) {
   __shared__ int we[32], wt[32];
   __shared__ int carry[2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lgR = __ffs(R) - 1;  // R = 128 / max(G, 8) is a power of two
   if (tid == 0) {
     carry[0] = first ? 0 : bucket_off[0];
     carry[1] = first ? 0 : tile_off[0];
   }
   __syncthreads();
-  for (int base = 0; base < nb; base += 4096) {
-    const int i = base + 4 * tid;
-    int c[4], t[4];
+  int cn[kScanItems];
+#pragma unroll
+  for (int q = 0; q < kScanItems; ++q) cn[q] = kScanItems * tid + q < nb ? count[kScanItems * tid + q] : 0;
+  for (int base = 0; base < nb; base += 1024 * kScanItems) {
+    const int i = base + kScanItems * tid;
+    int c[kScanItems];  // (tile counts are recomputed from c where needed)
     int se = 0, st = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      c[q] = i + q < nb ? count[i + q] : 0;
-      t[q] = (c[q] + R - 1) / R;
+    for (int q = 0; q < kScanItems; ++q) {
+      c[q] = cn[q];
       se += c[q];
-      st += t[q];
+      st += (c[q] + R - 1) >> lgR;
     }
+    const int inext = i + 1024 * kScanItems;
+#pragma unroll
+    for (int q = 0; q < kScanItems; ++q) cn[q] = inext + q < nb ? count[inext + q] : 0;
     int ie = se, it = st;  // inclusive scan over the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -540,13 +548,13 @@ __global__ void __launch_bounds__(1024) leaf_scan_kernel(const int* __restrict__
     int oe = carry[0] + (warp ? we[warp - 1] : 0) + ie - se;
     int ot = carry[1] + (warp ? wt[warp - 1] : 0) + it - st;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < kScanItems; ++q) {
       if (i + q < nb) {
         bucket_off[i + q] = oe;
         tile_off[i + q] = ot;
       }
       oe += c[q];
-      ot += t[q];
+      ot += (c[q] + R - 1) >> lgR;
     }
     __syncthreads();
     if (tid == 0) {
@@ -576,6 +584,75 @@ __global__ void leaf_tile_desc_kernel(const int* __restrict__ tile_off, const in
 
 // Final Top-K per (b, kv, t) over the leaf candidates (children of the level-2
 // survivors, ascending); ineligible children carry -inf and are skipped.
+// The same for K <= 8, in registers: candidate slot q = 2 j + child (child 0 is
+// the left leaf of survivor j); a slot counts if its survivor exists and, for a
+// right child, its score is not -inf.  The compacted order of the generic kernel
+// is the slot order, so its tie rule (earlier candidate first) is the lower slot.
+__global__ void leaf_final8_kernel(const int32_t* __restrict__ surv, const float* __restrict__ leaf_scores,
+                                   long long t0, long long t1, int BH, long long N, int32_t* __restrict__ idx,
+                                   float* __restrict__ scores) {
+  constexpr int K = 8;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (t1 - t0) * BH) return;
+  const long long job = (i / (t1 - t0)) * N + t0 + i % (t1 - t0);
+  const int4* s4 = reinterpret_cast<const int4*>(surv + job * K);
+  const int4 pa = __ldg(s4), pb = __ldg(s4 + 1);
+  const int p[K] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+  const float4* l4 = reinterpret_cast<const float4*>(leaf_scores + job * 2 * K);
+  float sc[2 * K];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 v = __ldg(l4 + q);
+    sc[4 * q] = v.x;
+    sc[4 * q + 1] = v.y;
+    sc[4 * q + 2] = v.z;
+    sc[4 * q + 3] = v.w;
+  }
+  unsigned valid = 0;
+  bool alive = true;  // survivors are ascending with -1 padding at the end
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    alive = alive && p[j] >= 0;
+    if (alive) valid |= (1u << (2 * j)) | (sc[2 * j + 1] != -INFINITY ? 1u << (2 * j + 1) : 0u);
+  }
+  const int nC = __popc(valid);
+  int out_i[K];
+  float out_s[K];
+  int w = 0;
+#pragma unroll
+  for (int q = 0; q < 2 * K; ++q) {
+    bool keep = (valid >> q) & 1;
+    if (keep && nC > K) {
+      int rank = 0;
+#pragma unroll
+      for (int r = 0; r < 2 * K; ++r)
+        rank += ((valid >> r) & 1) && (sc[r] > sc[q] || (sc[r] == sc[q] && r < q));
+      keep = rank < K;
+    }
+#pragma unroll
+    for (int o = 0; o < K; ++o)  // out[w] = candidate q, with register-resident outputs
+      if (keep && o == w) {
+        out_i[o] = 2 * p[q >> 1] + (q & 1);
+        out_s[o] = sc[q];
+      }
+    w += keep;
+  }
+#pragma unroll
+  for (int o = 0; o < K; ++o)
+    if (o >= w) {
+      out_i[o] = -1;
+      out_s[o] = -INFINITY;
+    }
+  int4* io = reinterpret_cast<int4*>(idx + job * K);
+  io[0] = make_int4(out_i[0], out_i[1], out_i[2], out_i[3]);
+  io[1] = make_int4(out_i[4], out_i[5], out_i[6], out_i[7]);
+  if (scores) {
+    float4* so = reinterpret_cast<float4*>(scores + job * K);
+    so[0] = make_float4(out_s[0], out_s[1], out_s[2], out_s[3]);
+    so[1] = make_float4(out_s[4], out_s[5], out_s[6], out_s[7]);
+  }
+}
+
 // Jobs (b * Hkv + kv) * N + t for t in [t0, t1).
 __global__ void leaf_final_kernel(const int32_t* __restrict__ surv, const float* __restrict__ leaf_scores,
                                   long long t0, long long t1, int BH, long long N, int K, int32_t* __restrict__ idx,
@@ -741,8 +818,15 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
   e = launch_leaf_tc_kernel(L, 0, 0, s);
   if (e != cudaSuccess) return e;
   mark_phase(4, s);
-  leaf_final_kernel<<<(unsigned)((BH * span + 127) / 128), 128, 0, s>>>(L.surv, L.leaf_scores, L.t0, L.t1, BH, L.N,
-                                                                       L.K, L.idx, L.scores);
+  // (the K = 8 kernel's vector accesses need 16-byte aligned idx / scores: true for the
+  // torch allocations the binding makes, checked here for any caller)
+  const bool vec = L.K == 8 && ((reinterpret_cast<uintptr_t>(L.idx) | reinterpret_cast<uintptr_t>(L.scores)) & 15) == 0;
+  if (vec)
+    leaf_final8_kernel<<<(unsigned)((BH * span + 127) / 128), 128, 0, s>>>(L.surv, L.leaf_scores, L.t0, L.t1, BH,
+                                                                          L.N, L.idx, L.scores);
+  else
+    leaf_final_kernel<<<(unsigned)((BH * span + 127) / 128), 128, 0, s>>>(L.surv, L.leaf_scores, L.t0, L.t1, BH, L.N,
+                                                                         L.K, L.idx, L.scores);
   note_launch();
   e = cudaGetLastError();
   mark_phase(5, s);

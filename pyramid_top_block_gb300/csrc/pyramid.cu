@@ -14,6 +14,8 @@
 //       leaves up log2(LPB) levels in shared memory.
 //   pyramid_top_kernel    : one CTA per (b, kv) merges the remaining levels up
 //       to the root.
+#include <mutex>
+
 #include "api.cuh"
 
 namespace pisa {
@@ -127,6 +129,56 @@ __global__ void __launch_bounds__(256) pyramid_top_kernel(float* __restrict__ su
   }
 }
 
+// The same levels when level first_level - 1 holds at most kTopNodes nodes: that
+// level is staged in shared memory once and every level above is merged there
+// (children read into registers, a barrier, parents written in place and to
+// global memory), so the chain of levels costs no global round trips.  Same
+// merge arithmetic, same bits.
+constexpr int kTopNodes = 256;                            // 64 KB of fp32 rows
+constexpr int kTopThreads = 1024;
+constexpr int kTopPer = (kTopNodes / 2) * kD / kTopThreads;  // outputs per thread at the first level
+__global__ void __launch_bounds__(kTopThreads) pyramid_top_smem_kernel(float* __restrict__ summ, Levels lv,
+                                                                      long long N, int Hkv, int first_level,
+                                                                      const int32_t* __restrict__ lens,
+                                                                      long long n_cap) {
+  extern __shared__ float4 sm4[];
+  float* sm = reinterpret_cast<float*>(sm4);
+  const int b = blockIdx.x / Hkv, kv = blockIdx.x % Hkv;
+  if (lens) N = min((long long)max(lens[b], 0), n_cap);
+  float* blk = summ + ((long long)b * Hkv + kv) * lv.total * kD;
+  const long long Mc0 = level_size_for(N, first_level - 1);  // <= kTopNodes (checked by the host)
+  const float4* src = reinterpret_cast<const float4*>(blk + lv.off[first_level - 1] * kD);
+  for (long long w = threadIdx.x; w < Mc0 * (kD / 4); w += kTopThreads) sm4[w] = src[w];
+  __syncthreads();
+  for (int l = first_level; l <= lv.L; ++l) {
+    const long long M = level_size_for(N, l), Mc = level_size_for(N, l - 1);
+    float out[kTopPer];
+#pragma unroll
+    for (int r = 0; r < kTopPer; ++r) {
+      const int w = threadIdx.x + r * kTopThreads;
+      out[r] = 0.f;
+      if (w < M * kD) {
+        const long long i = w / kD;
+        const int e = w % kD;
+        const long long c0 = 2 * i, c1 = 2 * i + 1;
+        const int n0 = node_count(l - 1, c0, N);
+        const int n1 = c1 < Mc ? node_count(l - 1, c1, N) : 0;
+        out[r] = merge_mean(sm[c0 * kD + e], n0, n1 > 0 ? sm[c1 * kD + e] : 0.f, n1);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kTopPer; ++r) {
+      const int w = threadIdx.x + r * kTopThreads;
+      if (w < M * kD) {
+        sm[w] = out[r];
+        blk[lv.off[l] * kD + w] = out[r];
+      }
+    }
+    __syncthreads();
+  }
+}
+
 __global__ void fill_lengths_kernel(int32_t* lengths, int B, int value) {
   int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < B) lengths[i] = value;
@@ -150,7 +202,17 @@ cudaError_t launch_build_pyramid(const __nv_bfloat16* keys, float* summ, const L
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (merge_levels + 2 <= lv.L) {
-    pyramid_top_kernel<<<B * Hkv, 256, 0, s>>>(summ, lv, N, Hkv, merge_levels + 2, lens, n_cap);
+    const int first = merge_levels + 2;
+    if (lv.M[first - 1] <= kTopNodes) {
+      const size_t smem = (size_t)kTopNodes * kD * sizeof(float);
+      static std::once_flag once;
+      std::call_once(once, [smem] {
+        cudaFuncSetAttribute(pyramid_top_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      });
+      pyramid_top_smem_kernel<<<B * Hkv, kTopThreads, smem, s>>>(summ, lv, N, Hkv, first, lens, n_cap);
+    } else {
+      pyramid_top_kernel<<<B * Hkv, 256, 0, s>>>(summ, lv, N, Hkv, first, lens, n_cap);
+    }
     note_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
