@@ -40,9 +40,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
                   "walk": ["walk_mma.cu", "tc.cuh", "common.cuh", "api.cuh"]}
 NCU_TRAFFIC = {
-    ("leaf", "latency-256k"): {"bytes": 1665541000 + 35650048, "src_sha1": "f332ea7cd4719a4dd8d50adacfef0f500bbc3610",
+    ("leaf", "latency-256k"): {"bytes": 1888564000 + 35622912, "src_sha1": "47f52060777a4a22b17718b418057aac2d48f4cc",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
-    ("walk", "latency-256k"): {"bytes": 1076188000 + 35827456, "src_sha1": "47d708aa450c87ad3ae24699c7919e6c9d506aa0",
+    ("walk", "latency-256k"): {"bytes": 1077004000 + 35866880, "src_sha1": "c8b305e0f887ca14f55fb36c1e24caf5af90f580",
                                "profile": "profiles/walk_k8_kernel_latency-256k.md"},
 }
 
