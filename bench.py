@@ -368,6 +368,17 @@ def run_ours(args):
             pisa.select_prefill_host(qh, kh, pyr, K, causal=True, idx_host=idx_h, q_dev=qd, idx_dev=idx,
                                      workspace=ws, stream=stream)
 
+        # this box's plain pinned host->device rate (it differs between boxes), for the floor
+        # that the transfers alone put under the end-to-end step
+        qd.copy_(qh, non_blocking=True)
+        torch.cuda.synchronize()
+        hs, he = mk(), mk()
+        hs.record(stream)
+        for _ in range(3):
+            qd.copy_(qh, non_blocking=True)
+        he.record(stream)
+        torch.cuda.synchronize()
+        h2d_gbs = 3 * qh.numel() * 2 / (hs.elapsed_time(he) * 1e6)
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize()
@@ -386,6 +397,8 @@ def run_ours(args):
         e_ms = max_over_ranks(es.elapsed_time(ee) / ne, dist, dev)
         e2e = {"value": job_rows_per_s(world, B * N, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "wall_ms_per_step": wall_ms, "api": "pisa_select_prefill_host",
+               "h2d_gbs_measured": h2d_gbs,
+               "transfer_floor_ms": (qh.numel() * 2 + kh.numel() * 2) / (h2d_gbs * 1e6),
                "h2d_bytes_per_step": qh.numel() * 2 + kh.numel() * 2,
                "d2h_bytes_per_step": idx_h.numel() * 4}
 
