@@ -9,18 +9,21 @@
 //
 // After the intermediate levels every query holds <= K level-2 survivors p; its
 // leaf candidates are the two children 2p, 2p+1 of each, i.e. the 128 keys
-// [128p, 128p+128).  Pipeline (all on one stream):
+// [128p, 128p+128).  Pipeline (on one stream, for a run of whole query chunks):
 //   (the walk kernel)   counts (query, survivor) pairs per bucket, a bucket being
-//                       (b, kv, query chunk, p); a chunk of 2^chunk_shift query
-//                       positions keeps the gathered query rows L2-resident
+//                       (query chunk, b * Hkv + kv, p), chunk-major so that a run
+//                       of chunks owns one contiguous range of buckets and tiles;
+//                       a chunk of 2^chunk_shift query positions keeps the
+//                       gathered query rows L2-resident
 //   leaf_scan_kernel    exclusive scans: entry offsets and tile offsets
 //   leaf_scatter_kernel write each pair (t << 5 | slot) into its bucket
+//   leaf_tile_desc_kernel  one descriptor per tile {first entry, rows, p, b*Hkv+kv}
 //   leaf_tc_kernel      persistent, warp-specialised: per tile of R = 128/max(G,8)
 //                       queries of one bucket, D[128 x 128] = Q_rows[128 x 64] x
 //                       K_block[128 x 64]^T on tcgen05 (bf16 in, fp32 in TMEM),
 //                       then per row two masked log-sum-exps and a sum over the
 //                       group's heads
-//   leaf_final_kernel   Top-K of the <= 2K leaf scores per query
+//   leaf_final(8)_kernel  Top-K of the <= 2K leaf scores per query
 #include <cudaTypedefs.h>
 
 #include <mutex>
