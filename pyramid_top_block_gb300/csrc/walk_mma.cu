@@ -789,6 +789,273 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// The K <= 8 walk for G = 16 with the operands of the MMA swapped: the query's 16
+// heads are the A operand (rows g and g + 8 of the fragment, loaded once per
+// query) and the candidates' rows are the B operand (n = g of each 8-candidate
+// tile).  A lane's B pair for k-step ks is two adjacent words of one row in the
+// table's layout, so the rows feed the MMA straight from their 16-byte loads
+// (with candidates as the A operand every A quad mixes two rows and has to be
+// assembled by register moves).  After the MMAs lane (g, j) holds u for heads g,
+// g + 8 and candidates 8 ct + 2 j + e (ct, e in {0, 1}); the head sums run as a
+// three-step butterfly over g that leaves candidate oc = 8 b4 + 2 j + b3 (bN =
+// lane bit N) on the two lanes that differ in bit 2.  Same arithmetic per
+// (candidate, head) as walk_k8_kernel; head sums associate differently.
+
+// Keeps the value of candidate `hi` (if the lane bit is set) or `lo` and adds
+// (or multiplies) the partner's copy of the same candidate.
+__device__ __forceinline__ float bfly_add(float lo, float hi, int bit, int mask) {
+  const float send = bit ? lo : hi, mine = bit ? hi : lo;
+  return mine + __shfl_xor_sync(kFull, send, mask);
+}
+
+// q . row for this lane's two B rows (ra: candidate g, rb: candidate g + 8) against
+// the query's heads: u[ct][0..1] = head g, candidates 8 ct + 2 j + {0, 1};
+// u[ct][2..3] = head g + 8, the same candidates.  The B pair of k-step ks is the
+// word pair (2 (ks & 1), +1) of ra / rb [ks >> 1] (hi) and [2 + (ks >> 1)] (lo).
+__device__ __forceinline__ void tile_dots_s(const uint32_t (&A)[4][4], const uint4 (&ra)[4], const uint4 (&rb)[4],
+                                            float (&u)[2][4]) {
+  float dh[2][4], dl[2][4];
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) {
+    const uint4& Ha = ra[ks >> 1];
+    const uint4& La = ra[2 + (ks >> 1)];
+    const uint4& Hb = rb[ks >> 1];
+    const uint4& Lb = rb[2 + (ks >> 1)];
+    const bool hw = ks & 1;
+    if (ks == 0) {
+      mma_bf16_16816_z(dh[0], A[ks], Ha.x, Ha.y);
+      mma_bf16_16816_z(dl[0], A[ks], La.x, La.y);
+      mma_bf16_16816_z(dh[1], A[ks], Hb.x, Hb.y);
+      mma_bf16_16816_z(dl[1], A[ks], Lb.x, Lb.y);
+    } else {
+      mma_bf16_16816(dh[0], A[ks], hw ? Ha.z : Ha.x, hw ? Ha.w : Ha.y);
+      mma_bf16_16816(dl[0], A[ks], hw ? La.z : La.x, hw ? La.w : La.y);
+      mma_bf16_16816(dh[1], A[ks], hw ? Hb.z : Hb.x, hw ? Hb.w : Hb.y);
+      mma_bf16_16816(dl[1], A[ks], hw ? Lb.z : Lb.x, hw ? Lb.w : Lb.y);
+    }
+  }
+#pragma unroll
+  for (int ct = 0; ct < 2; ++ct)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[ct][i] = dh[ct][i] + dl[ct][i];
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8s_kernel(
+    const __nv_bfloat16* __restrict__ Q, const unsigned char* __restrict__ table, Levels lv, RowOffsets ro,
+    LevelTail tail, long long rows_per_bh, int N, int Hq, int Hkv, int K, int causal, int l_start, int l_lo,
+    int32_t* __restrict__ surv, int32_t* __restrict__ srank, int* __restrict__ count, int t0, int t1, int chunk_shift,
+    int M2) {
+  extern __shared__ __align__(16) unsigned char wsm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, j = lane & 3;
+  const int b2 = (lane >> 2) & 1, b3 = (lane >> 3) & 1, b4 = (lane >> 4) & 1;
+  const int oc = 8 * b4 + 2 * j + b3;  // the candidate this lane owns after the head sums
+  // first-copy lane of candidate c: 16 (c >> 3) + 8 (c & 1) + ((c >> 1) & 3); `below` marks
+  // those of the candidates before oc, kOwn all first copies (lane bit 2 clear)
+  unsigned below = 0;
+  for (int c = 0; c < oc; ++c) below |= 1u << (16 * (c >> 3) + 8 * (c & 1) + ((c >> 1) & 3));
+  constexpr unsigned kOwn = 0x0F0F0F0Fu;
+  constexpr int G = 16;  // the launcher's condition (Hq / Hkv == 16)
+  const long long bh = blockIdx.y;
+  const int kv = (int)(bh % Hkv);
+  const long long b = bh / Hkv;
+  const long long zrow0 = ro.o[lv.L + 1] + 1;
+  const int crow0 = (l_start >= 2) ? (int)ro.o[l_lo] : 0;
+  const int ncache = (l_start >= 2) ? (int)(ro.o[l_start + 1] - ro.o[l_lo]) : 0;
+  unsigned char* czr = wsm;
+  unsigned char* cdr = wsm + 16 * kCacheRowBytes;
+  int* cbuf = reinterpret_cast<int*>(cdr + (size_t)ncache * kCacheRowBytes) + warp * kCandBuf;
+  __shared__ int4 lvt[kMaxLevels + 2];
+  if (threadIdx.x >= 2 && threadIdx.x <= lv.L) {
+    const int l = threadIdx.x;
+    const bool cached = l >= l_lo && l <= l_start;
+    lvt[l] = make_int4(cached ? (int)((ro.o[l] - crow0) * kCacheRowBytes) : (int)ro.o[l], lv.M[l - 1] - 1,
+                       tail.node[l], __float_as_int(tail.nr[l]));
+  }
+  const unsigned char* tb = table + bh * rows_per_bh * kRowBytes;
+  if (l_start >= 2) {
+    for (int e = threadIdx.x; e < 16 * 16; e += blockDim.x)
+      *reinterpret_cast<uint4*>(czr + (e >> 4) * kCacheRowBytes + (e & 15) * 16) =
+          __ldg(reinterpret_cast<const uint4*>(tb + zrow0 * kRowBytes) + e);
+    for (int e = threadIdx.x; e < ncache * 16; e += blockDim.x)
+      *reinterpret_cast<uint4*>(cdr + (e >> 4) * kCacheRowBytes + (e & 15) * 16) =
+          __ldg(reinterpret_cast<const uint4*>(tb + (long long)crow0 * kRowBytes) + e);
+  }
+  __syncthreads();
+  for (int t = t0 + blockIdx.x + gridDim.x * warp; t < t1; t += gridDim.x * kWalkWarps) {
+    __syncwarp();  // the previous query's reads of the candidate buffers are done
+    const long long job = bh * N + t;
+    if (l_start < 2) {
+      int32_t* out = surv + job * K;
+      int32_t* rk = srank + job * K;
+      int* cnt = count + ((long long)(t >> chunk_shift) * gridDim.y + bh) * M2;  // chunk-major buckets
+      const int m2 = lv.L >= 2 ? lv.M[2] : 1;
+      const int el = causal ? min(m2, (t >> (kLog2C + 1)) + 1) : m2;
+      if (lane < K) {
+        const int p = lane < el ? lane : -1;
+        out[lane] = p;
+        if (p >= 0) rk[lane] = atomicAdd(cnt + p, 1);
+      }
+      continue;
+    }
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + ((b * N + t) * Hq + (long long)kv * G) * kD);
+    // Q as the A operand: [ks] = {head g word 8ks + j, head g + 8 same word, head g word
+    // 8ks + j + 4, head g + 8 same word} (all 16 heads are real: G = 16)
+    uint32_t A[4][4];
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const int w0 = 8 * ks + j;
+      A[ks][0] = __ldg(q0 + g * 32 + w0);
+      A[ks][2] = __ldg(q0 + g * 32 + w0 + 4);
+      A[ks][1] = __ldg(q0 + (g + 8) * 32 + w0);
+      A[ks][3] = __ldg(q0 + (g + 8) * 32 + w0 + 4);
+    }
+    int nC;
+    {
+      const int ml = lv.M[l_start];
+      nC = causal ? min(ml, (t >> (kLog2C + l_start - 1)) + 1) : ml;
+    }
+    int c = oc;            // node id of the owned candidate
+    int na = g, nb = g + 8;  // node ids of this lane's B rows (candidates g and g + 8)
+    float Z;
+    {
+      uint4 ra[4], rb[4];
+      ld_row(czr + g * kCacheRowBytes + 32 * j, true, ra[0], ra[1], ra[2], ra[3]);
+      ld_row(czr + (g + 8) * kCacheRowBytes + 32 * j, true, rb[0], rb[1], rb[2], rb[3]);
+      float u[2][4];
+      tile_dots_s(A, ra, rb, u);
+      // sum over the lane's two heads, then over g
+      const float z0 = u[0][0] + u[0][2], z1 = u[0][1] + u[0][3], z2 = u[1][0] + u[1][2], z3 = u[1][1] + u[1][3];
+      float ze = bfly_add(z0, z2, b4, 16), zo = bfly_add(z1, z3, b4, 16);
+      Z = bfly_add(ze, zo, b3, 8);
+      Z += __shfl_xor_sync(kFull, Z, 4);
+    }
+    for (int l = l_start;; --l) {
+      const bool scoring = nC > K;
+      const int4 lt4 = lvt[l];
+      const int lim = causal ? min(lt4.y, t >> (l + 4)) : lt4.y;  // last eligible second child
+      const int rag = lt4.z;
+      const float rnr = __int_as_float(lt4.w);
+      const bool va = g < nC, vb = g + 8 < nC;
+      const int ra_row = va ? na : 0, rb_row = vb ? nb : 0;  // (rows >= nC: never kept)
+      uint4 ra[4], rb[4];
+      if (l >= l_lo) {
+        const unsigned char* base = cdr + lt4.x + 32 * j;
+        ld_row(base + ra_row * kCacheRowBytes, true, ra[0], ra[1], ra[2], ra[3]);
+        ld_row(base + rb_row * kCacheRowBytes, true, rb[0], rb[1], rb[2], rb[3]);
+      } else {
+        const unsigned char* base = tb + (long long)lt4.x * kRowBytes + 32 * j;
+        ld_row(base + ra_row * kRowBytes, false, ra[0], ra[1], ra[2], ra[3]);
+        ld_row(base + rb_row * kRowBytes, false, rb[0], rb[1], rb[2], rb[3]);
+      }
+      float u[2][4];
+      tile_dots_s(A, ra, rb, u);
+      // per candidate 8 ct + 2 j + e over the lane's two heads: sum of u, and the
+      // LSE excess over z (MODE 0) or the sum of u^2 (MODE 2)
+      float su[2][2], pt[2][2];
+      const bool any_rag = MODE == 0 && rag >= 0 && __any_sync(kFull, (va && na == rag) || (vb && nb == rag));
+      const int* cur = cbuf + (((l + 1) & 1) << 5);  // this level's candidate node ids
+#pragma unroll
+      for (int ct = 0; ct < 2; ++ct) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float ua = u[ct][e], ub = u[ct][2 + e];  // heads g and g + 8
+          su[ct][e] = ua + ub;
+          if (MODE == 2) pt[ct][e] = fmaf(ua, ua, ub * ub);
+          if (MODE == 0 && !any_rag) {  // r = 1: max(u, -u) = |u|, exponent -2 |u|
+            const float aa = fabsf(ua), ab = fabsf(ub);
+            const float ea = ex2_approx(-2.f * aa), eb = ex2_approx(-2.f * ab);
+            pt[ct][e] = (aa + ab) + lg2_approx(fmaf(ea, 1.f + eb, 1.f + eb));
+          } else if (MODE == 0) {
+            float nr = -1.f;
+            {
+              const int ci = 8 * ct + 2 * j + e;
+              const int nd = l == l_start ? ci : cur[ci];
+              if (ci < nC && nd == rag) nr = rnr;
+            }
+            // max(u, nr u) + log2(1 + 2^(min - max)) per head, summed over the two
+            const float tax = nr * ua, tbx = nr * ub;
+            const float mxa = fmaxf(ua, tax), mxb = fmaxf(ub, tbx);
+            const float ea = ex2_approx(fminf(ua, tax) - mxa), eb = ex2_approx(fminf(ub, tbx) - mxb);
+            pt[ct][e] = (mxa + mxb) + lg2_approx(fmaf(ea, 1.f + eb, 1.f + eb));
+          }
+        }
+      }
+      // butterfly over g: keep tile b4, then parity b3, then add the copy on lane ^ 4
+      float sum_u = bfly_add(bfly_add(su[0][0], su[1][0], b4, 16), bfly_add(su[0][1], su[1][1], b4, 16), b3, 8);
+      sum_u += __shfl_xor_sync(kFull, sum_u, 4);
+      float part = 0.f;
+      if (MODE != 1) {
+        part = bfly_add(bfly_add(pt[0][0], pt[1][0], b4, 16), bfly_add(pt[0][1], pt[1][1], b4, 16), b3, 8);
+        part += __shfl_xor_sync(kFull, part, 4);
+      }
+      const bool valid = oc < nC;
+      const bool two = 2 * c + 1 <= lim;
+      const bool ref1 = c == rag;
+      const float nr = ref1 ? rnr : -1.f;
+      bool keep = valid;
+      if (scoring) {
+        float two_sc = part;
+        if (MODE == 1) two_sc = 0.5f * (1.f + nr) * sum_u;
+        if (MODE == 2) two_sc = 0.5f * (1.f + nr) * sum_u + 0.69314718055994531f * 0.125f * (1.f - nr) * (1.f - nr) * part;
+        const float sc = Z + (two ? two_sc : (ref1 ? nr : 1.f) * sum_u);
+        const unsigned fb = __float_as_uint(sc);
+        unsigned key = fb ^ ((unsigned)((int)fb >> 31) | 0x80000000u);
+        key = valid ? ((key & ~15u) | (unsigned)(15 - oc)) : 0u;
+        // rank = number of larger keys: lanes with bit 2 clear count among candidates 0..7,
+        // the others among 8..15
+        unsigned* keys = reinterpret_cast<unsigned*>(cbuf) + 64;
+        if (b2 == 0) keys[oc] = key;
+        __syncwarp();
+        const uint4* kq = reinterpret_cast<const uint4*>(keys + 8 * b2);
+        const uint4 k0 = kq[0], k1 = kq[1];
+        int rank = (k0.x > key) + (k0.y > key) + (k0.z > key) + (k0.w > key) + (k1.x > key) + (k1.y > key) +
+                   (k1.z > key) + (k1.w > key);
+        rank += __shfl_xor_sync(kFull, rank, 4);
+        keep = valid && rank < K;
+      }
+      const unsigned bk = __ballot_sync(kFull, keep), b2k = __ballot_sync(kFull, keep && two);
+      const int before = __popc(bk & below);
+      if (l == 2) {
+        int32_t* out = surv + job * K;
+        int32_t* rk = srank + job * K;
+        int* cnt = count + ((long long)(t >> chunk_shift) * gridDim.y + bh) * M2;  // chunk-major buckets
+        if (b2 == 0 && keep) {
+          out[before] = c;
+          rk[before] = atomicAdd(cnt + c, 1);
+        }
+        const int nS = __popc(bk & kOwn);
+        if (lane < K && lane >= nS) out[lane] = -1;
+        break;
+      }
+      {
+        const float zr = Z + sum_u, zo = fmaf(nr, sum_u, Z);
+        int* buf = cbuf + ((l & 1) << 5);
+        if (b2 == 0 && keep) {
+          const int pos = before + __popc(b2k & below);
+          buf[pos] = 2 * c;
+          buf[16 + pos] = __float_as_int(ref1 ? zo : zr);
+          if (two) {
+            buf[pos + 1] = 2 * c + 1;
+            buf[16 + pos + 1] = __float_as_int(ref1 ? zr : zo);
+          }
+        }
+        nC = __popc(bk & kOwn) + __popc(b2k & kOwn);
+        __syncwarp();
+        if (oc < nC) {
+          c = buf[oc];
+          Z = __int_as_float(buf[16 + oc]);
+        }
+        na = g < nC ? buf[g] : 0;
+        nb = g + 8 < nC ? buf[g + 8] : 0;
+      }
+    }
+  }
+}
+
 // Host side: table size and launches.
 long long route_rows_per_bh(const Levels& lv) {
   long long r = 1 + kZRows;  // the zero row and the mean rows
@@ -858,7 +1125,12 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
       constexpr int NT = decltype(nt)::value;
       return W.mode == 1 ? walk_k8_kernel<NT, 1> : W.mode == 2 ? walk_k8_kernel<NT, 2> : walk_k8_kernel<NT, 0>;
     };
-    auto kern = G > 8 ? pick(std::integral_constant<int, 2>()) : pick(std::integral_constant<int, 1>());
+    auto pick_s = [&]() {
+      return W.mode == 1 ? walk_k8s_kernel<1> : W.mode == 2 ? walk_k8s_kernel<2> : walk_k8s_kernel<0>;
+    };
+    // G = 16: the swapped-operand walk; smaller groups (one 8-head tile) keep the
+    // candidates as the A operand
+    auto kern = G == 16 ? pick_s() : pick(std::integral_constant<int, 1>());
     {
       static std::mutex mu;
       static size_t attr[2][3] = {};
