@@ -42,8 +42,8 @@ KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
 NCU_TRAFFIC = {
     ("leaf", "latency-256k"): {"bytes": 1888564000 + 35622912, "src_sha1": "c98ce3d8da7128f0c2e53308cf5d2f696a1390e7",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
-    ("walk", "latency-256k"): {"bytes": 1077004000 + 35866880, "src_sha1": "c8b305e0f887ca14f55fb36c1e24caf5af90f580",
-                               "profile": "profiles/walk_k8_kernel_latency-256k.md"},
+    ("walk", "latency-256k"): {"bytes": 1076219000 + 34968064, "src_sha1": "24dbfbe0de7c58e3127c7193c55b0a7f56142c6e",
+                               "profile": "profiles/walk_k8s_kernel_latency-256k.md"},
 }
 
 
