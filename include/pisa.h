@@ -226,6 +226,7 @@ size_t pisa_decode_workspace_bytes(int B, int Hq, int Hkv, int K);
  * keeps the mean pyramid cached, updates only the new token's leaf mean and its
  * ancestor path, then walks for the new query).
  *   q_new  : device bf16 [B, Hq, d], the query of the token being appended
+ *            (16-byte aligned)
  *   k_new  : device bf16 [B, Hkv, d], its key
  *   pyr    : pyramid with keys [B, n_cap, Hkv, d], summaries and lengths (all
  *            required); for each b the key is written at position

@@ -7,8 +7,9 @@
 //
 // One CTA of kDecWarps warps per (b, kv).  Threads 0..63 update the path (one
 // feature each); then every level's candidates are scored one warp per candidate
-// (lanes = child x head for an intermediate node, lanes = keys for a leaf) and
-// warp 0 keeps the Top-K and expands the survivors.
+// (lanes = child x head for an intermediate node; for a leaf, the exact score on
+// mma.sync with the query heads as rows and the leaf's 64 keys as 8 column tiles)
+// and warp 0 keeps the Top-K and expands the survivors.
 #include "api.cuh"
 #include "walk.cuh"
 
@@ -30,16 +31,16 @@ __device__ __forceinline__ float warp_node_score(const float* blk, const Levels&
   if (h < G && (ch == 0 || two)) {
     const float4* r = reinterpret_cast<const float4*>(blk + (lv.off[l - 1] + node) * kD);
     const float4* qv = reinterpret_cast<const float4*>(qs + h * kQStride);
-    float a = 0.f;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // four chains for latency
 #pragma unroll
     for (int j = 0; j < kD / 4; ++j) {
       const float4 k = r[j], q = qv[j];
-      a = fmaf(q.x, k.x, a);
-      a = fmaf(q.y, k.y, a);
-      a = fmaf(q.z, k.z, a);
-      a = fmaf(q.w, k.w, a);
+      a0 = fmaf(q.x, k.x, a0);
+      a1 = fmaf(q.y, k.y, a1);
+      a2 = fmaf(q.z, k.z, a2);
+      a3 = fmaf(q.w, k.w, a3);
     }
-    z = a * kScale;
+    z = ((a0 + a1) + (a2 + a3)) * kScale;
   }
   const float z1 = __shfl_xor_sync(kFull, z, 16);
   float v = (ch == 0 && h < G) ? (two ? lse2(z, z1) : z) : 0.f;
@@ -48,51 +49,104 @@ __device__ __forceinline__ float warp_node_score(const float* blk, const Levels&
   return v;
 }
 
-// Exact leaf score: sum over heads of log sum exp over the raw keys of leaf c
-// below n (all present keys); lane j holds keys 64c + j and 64c + j + 32.
+// bf16 m16n8k16 MMA with fp32 accumulation (D = A B + C).
+__device__ __forceinline__ void dec_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The query heads of this (b, kv) as the A operand of q . k: rows g and g + 8 of
+// the fragment are heads g and g + 8 (zero beyond G); k-step ks takes the bf16
+// pairs (words) 8 j + 2 ks and 8 j + 2 ks + 1 of a row, so a lane's words of every
+// k-step are one contiguous 32-byte slice of each row.
 template <int G>
-__device__ __forceinline__ float warp_leaf_exact(const __nv_bfloat16* keys_b, int Hkv, int kv, long long c,
-                                                 long long n, const float* qs, int lane) {
-  float total = 0.f;
-  float z0[G], z1[G];
-  const long long r0 = c * kC + lane, r1 = r0 + 32;
-  const bool a0 = r0 < n, a1 = r1 < n;
+__device__ __forceinline__ void leaf_q_frags(const __nv_bfloat16* q_bkv, int lane, uint32_t (&A)[4][4]) {
+  const int g = lane >> 2, j = lane & 3;
+  uint4 h0[2] = {}, h1[2] = {};
+  if (g < G) {
+    const uint4* r = reinterpret_cast<const uint4*>(q_bkv + g * kD) + 2 * j;
+    h0[0] = r[0];
+    h0[1] = r[1];
+  }
+  if (g + 8 < G) {
+    const uint4* r = reinterpret_cast<const uint4*>(q_bkv + (g + 8) * kD) + 2 * j;
+    h1[0] = r[0];
+    h1[1] = r[1];
+  }
+  const uint32_t w0[8] = {h0[0].x, h0[0].y, h0[0].z, h0[0].w, h0[1].x, h0[1].y, h0[1].z, h0[1].w};
+  const uint32_t w1[8] = {h1[0].x, h1[0].y, h1[0].z, h1[0].w, h1[1].x, h1[1].y, h1[1].z, h1[1].w};
 #pragma unroll
-  for (int w = 0; w < 2; ++w) {
-    const long long r = w ? r1 : r0;
-    float* z = w ? z1 : z0;
-    if (w ? a1 : a0) {
-      float k[kD];
-      const uint4* r4 = reinterpret_cast<const uint4*>(keys_b + (r * Hkv + kv) * kD);
+  for (int ks = 0; ks < 4; ++ks) {
+    A[ks][0] = w0[2 * ks];
+    A[ks][1] = w1[2 * ks];
+    A[ks][2] = w0[2 * ks + 1];
+    A[ks][3] = w1[2 * ks + 1];
+  }
+}
+
+// Exact leaf score on the tensor cores: sum over heads of log sum exp over the raw
+// keys of leaf c below n.  S[16 heads x 64 keys] = Q K^T in 8 tiles of 8 keys (the
+// B operand of tile nt: key 8 nt + g, the lane's 32-byte slice of its row), fp32
+// accumulation of the exact bf16 products; then per head a max / sum over the
+// lane's 16 keys and the lane quad, and the head sum over g.
+template <int G>
+__device__ __forceinline__ float warp_leaf_mma(const __nv_bfloat16* keys_b, int Hkv, int kv, long long c, long long n,
+                                               const uint32_t (&A)[4][4], int lane) {
+  const int g = lane >> 2, j = lane & 3;
+  float z[8][4];
 #pragma unroll
-      for (int j = 0; j < kD / 8; ++j) unpack8(r4[j], k + 8 * j);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float4* qv = reinterpret_cast<const float4*>(qs + h * kQStride);
-        float a = 0.f;
-#pragma unroll
-        for (int j = 0; j < kD / 4; ++j) {
-          const float4 q = qv[j];
-          a = fmaf(q.x, k[4 * j], a);
-          a = fmaf(q.y, k[4 * j + 1], a);
-          a = fmaf(q.z, k[4 * j + 2], a);
-          a = fmaf(q.w, k[4 * j + 3], a);
-        }
-        z[h] = a * kScale;
-      }
+  for (int nt = 0; nt < 8; ++nt) {
+    const long long r = c * kC + 8 * nt + g;
+    uint4 k0 = make_uint4(0, 0, 0, 0), k1 = k0;
+    if (r < n) {
+      const uint4* kp = reinterpret_cast<const uint4*>(keys_b + (r * Hkv + kv) * kD) + 2 * j;
+      k0 = kp[0];
+      k1 = kp[1];
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) z[nt][i] = 0.f;
+    dec_mma(z[nt], A[0], k0.x, k0.y);
+    dec_mma(z[nt], A[1], k0.z, k0.w);
+    dec_mma(z[nt], A[2], k1.x, k1.y);
+    dec_mma(z[nt], A[3], k1.z, k1.w);
   }
+  // z[nt][e] = head g, key 8 nt + 2 j + e; z[nt][2 + e] = head g + 8, same key
+  float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float m = fmaxf(a0 ? z0[h] : -INFINITY, a1 ? z1[h] : -INFINITY);
+  for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    float e = (a0 ? expf(z0[h] - m) : 0.f) + (a1 ? expf(z1[h] - m) : 0.f);
+    for (int e = 0; e < 2; ++e) {
+      const bool in = c * kC + 8 * nt + 2 * j + e < n;
+      z[nt][e] = in ? z[nt][e] * kScale : -INFINITY;
+      z[nt][2 + e] = in ? z[nt][2 + e] * kScale : -INFINITY;
+      m0 = fmaxf(m0, z[nt][e]);
+      m1 = fmaxf(m1, z[nt][2 + e]);
+    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(kFull, e, o);
-    total += m + logf(e);
+  for (int o = 1; o < 4; o <<= 1) {
+    m0 = fmaxf(m0, __shfl_xor_sync(kFull, m0, o));
+    m1 = fmaxf(m1, __shfl_xor_sync(kFull, m1, o));
   }
-  return total;
+  float e0 = 0.f, e1 = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      e0 += expf(z[nt][e] - m0);
+      e1 += expf(z[nt][2 + e] - m1);
+    }
+#pragma unroll
+  for (int o = 1; o < 4; o <<= 1) {
+    e0 += __shfl_xor_sync(kFull, e0, o);
+    e1 += __shfl_xor_sync(kFull, e1, o);
+  }
+  float v = (g < G ? m0 + logf(e0) : 0.f) + (g + 8 < G ? m1 + logf(e1) : 0.f);
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
 }
 
 // One decode step for one (b, kv): append k_new at position p = lengths[b],
@@ -136,13 +190,17 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
   if (tid < kD) {
     // siblings of the path nodes (levels 1..L-1), fetched together before the new token
     // changes anything they depend on: none of them is on the path
+    // (all loads issued before any store, so their latencies overlap)
     const int e = tid;
-    long long i = leaf;
-    for (int l = 2; l <= lv.L; ++l) {
-      const long long s = i ^ 1;
-      sib[l][e] = s < lv.M[l - 1] ? blk[(lv.off[l - 1] + s) * kD + e] : 0.f;
-      i >>= 1;
+    float v[kMaxLevels + 1];
+#pragma unroll
+    for (int l = 2; l <= kMaxLevels; ++l) {
+      const long long s = (leaf >> (l - 2)) ^ 1;
+      v[l] = (l <= lv.L && s < lv.M[l - 1]) ? blk[(lv.off[l - 1] + s) * kD + e] : 0.f;
     }
+#pragma unroll
+    for (int l = 2; l <= kMaxLevels; ++l)
+      if (l <= lv.L) sib[l][e] = v[l];
   } else if (tid >= 64 && tid < 64 + G * kD) {
     for (int i = tid - 64; i < G * kD; i += kDecWarps * 32 - 64)
       qs[(i / kD) * kQStride + (i % kD)] = bf2f(q_new[((long long)b * Hq + (long long)kv * G) * kD + i]);
@@ -218,8 +276,10 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
   __syncthreads();
   const int nC = nC_s;
   if (nC > K || so != nullptr) {
+    uint32_t qa[4][4];
+    leaf_q_frags<G>(q_new + ((long long)b * Hq + (long long)kv * G) * kD, lane, qa);
     for (int ci = warp; ci < nC; ci += kDecWarps) {
-      const float sc = warp_leaf_exact<G>(keys_b, Hkv, kv, ws.cand[ci], n, qs, lane);
+      const float sc = warp_leaf_mma<G>(keys_b, Hkv, kv, ws.cand[ci], n, qa, lane);
       if (lane == 0) ws.score[ci] = sc;
     }
     __syncthreads();

@@ -529,6 +529,7 @@ int pisa_decode_append_and_select(const void* q_new, const void* k_new, int Hq, 
   st = check_geometry(pyr->B, pyr->n_cap, Hq, pyr->Hkv, pyr->d, pyr->C, pyr->g, K);
   if (st) return st;
   if (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) return PISA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(q_new) & 15) return PISA_ERR_INVALID_ARG;  // read 16 bytes at a time
   if (ws_bytes < align_up(kStatusBytes)) return PISA_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes, s);
