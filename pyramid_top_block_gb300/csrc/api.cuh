@@ -78,6 +78,6 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s);
 cudaError_t launch_decode_warp(const __nv_bfloat16* q_new, const __nv_bfloat16* k_new,
                                __nv_bfloat16* keys, float* summ, int32_t* lengths,
                                const Levels& cap_lv, long long n_cap, int B, int Hq, int Hkv, int K,
-                               int32_t* idx, float* scores, int* status, cudaStream_t s);
+                               int32_t* idx, float* scores, int* status, int* arrivals, cudaStream_t s);
 
 }  // namespace pisa

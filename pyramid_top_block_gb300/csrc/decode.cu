@@ -19,17 +19,27 @@ constexpr int kDecWarps = 16;
 constexpr int kQStride = kD + 4;  // padded row of the query heads in shared memory (conflict-free float4 reads)
 
 // Head-summed LSE score of candidate c at level l >= 2 over its children's
-// summaries; lane = (child lane >> 4, head lane & 15).  In decode the query is the
-// newest token, so every existing child is eligible.  Lanes 0..15 return it.
+// summaries (level l - 1: row offset off1, size M1); lane = (child lane >> 4, head
+// lane & 15).  In decode the query is the newest token, so every existing child is
+// eligible.  Lanes 0..15 return it.  While the rows are in flight, lanes 0..7 ask L1
+// for the rows of c's grandchildren (level l - 2: offset off2, size M2), which are
+// the rows the next level reads for whichever of c's children it keeps.
 template <int G>
-__device__ __forceinline__ float warp_node_score(const float* blk, const Levels& lv, int l, int c, const float* qs,
-                                                 int lane) {
+__device__ __forceinline__ float warp_node_score(const float* blk, long long off1, long long M1, long long off2,
+                                                 long long M2, int l, int c, const float* qs, int lane) {
   const int ch = lane >> 4, h = lane & 15;
   const long long node = 2LL * c + ch;
-  const bool two = 2LL * c + 1 < lv.M[l - 1];
+  const bool two = 2LL * c + 1 < M1;
   float z = 0.f;
+  if (l >= 3 && lane < 8) {
+    const long long gc = 4LL * c + (lane >> 1);
+    if (gc < M2) {
+      const float* a = blk + (off2 + gc) * kD + (lane & 1) * (kD / 2);
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
+    }
+  }
   if (h < G && (ch == 0 || two)) {
-    const float4* r = reinterpret_cast<const float4*>(blk + (lv.off[l - 1] + node) * kD);
+    const float4* r = reinterpret_cast<const float4*>(blk + (off1 + node) * kD);
     const float4* qv = reinterpret_cast<const float4*>(qs + h * kQStride);
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // four chains for latency
 #pragma unroll
@@ -155,9 +165,9 @@ __device__ __forceinline__ float warp_leaf_mma(const __nv_bfloat16* keys_b, int 
 template <int G>
 __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
     const __nv_bfloat16* __restrict__ q_new, const __nv_bfloat16* __restrict__ k_new,
-    __nv_bfloat16* keys, float* summ, const int32_t* __restrict__ lengths, Levels cap_lv,
+    __nv_bfloat16* keys, float* summ, int32_t* lengths, Levels cap_lv,
     long long n_cap, int Hq, int Hkv, int K, int32_t* __restrict__ idx, float* __restrict__ scores,
-    int* status) {
+    int* status, int* arrivals) {
   __shared__ __align__(16) float qs[G * kQStride];
   __shared__ float sib[kMaxLevels + 1][kD];  // siblings along the new token's path
   __shared__ __align__(16) __nv_bfloat16 lk[kC * kD];  // the earlier keys of the new token's leaf
@@ -240,6 +250,12 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
   }
   __threadfence_block();
   __syncthreads();
+  if (tid == 0) {
+    // every thread of this CTA has read lengths[b]; the last of the sequence's Hkv CTAs
+    // to get here advances it (none of them reads it again)
+    __threadfence();
+    if (atomicAdd(arrivals + b, 1) == Hkv - 1) lengths[b] = (int32_t)(p + 1);
+  }
 
   // intermediate levels L-1 .. 2 (levels with at most K candidates are kept whole)
   int nS = 1, myS = 0;  // survivors, held by warp 0 (lane j < nS holds the j-th)
@@ -251,8 +267,10 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
     __syncthreads();
     const int nC = nC_s;
     if (nC > K) {
+      const long long off1 = lv.off[l - 1], M1 = lv.M[l - 1];
+      const long long off2 = l >= 3 ? lv.off[l - 2] : 0, M2 = l >= 3 ? lv.M[l - 2] : 0;
       for (int ci = warp; ci < nC; ci += kDecWarps) {
-        const float sc = warp_node_score<G>(blk, lv, l, ws.cand[ci], qs, lane);
+        const float sc = warp_node_score<G>(blk, off1, M1, off2, M2, l, ws.cand[ci], qs, lane);
         if (lane == 0) ws.score[ci] = sc;
       }
       __syncthreads();
@@ -306,24 +324,15 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
   }
 }
 
-__global__ void bump_lengths_kernel(int32_t* lengths, int B, long long n_cap) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b < B && lengths[b] >= 0 && lengths[b] < n_cap) lengths[b] += 1;
-}
-
 // ---------------------------------------------------------------- launchers
 
 template <int G>
 static cudaError_t launch_decode_G(const __nv_bfloat16* q_new, const __nv_bfloat16* k_new,
                                    __nv_bfloat16* keys, float* summ, int32_t* lengths,
                                    const Levels& cap_lv, long long n_cap, int B, int Hq, int Hkv,
-                                   int K, int32_t* idx, float* scores, int* status, cudaStream_t s) {
+                                   int K, int32_t* idx, float* scores, int* status, int* arrivals, cudaStream_t s) {
   decode_kernel<G><<<B * Hkv, kDecWarps * 32, 0, s>>>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, Hq, Hkv,
-                                          K, idx, scores, status);
-  note_launch();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  bump_lengths_kernel<<<(B + 127) / 128, 128, 0, s>>>(lengths, B, n_cap);
+                                          K, idx, scores, status, arrivals);
   note_launch();
   return cudaGetLastError();
 }
@@ -331,13 +340,13 @@ static cudaError_t launch_decode_G(const __nv_bfloat16* q_new, const __nv_bfloat
 cudaError_t launch_decode_warp(const __nv_bfloat16* q_new, const __nv_bfloat16* k_new,
                                __nv_bfloat16* keys, float* summ, int32_t* lengths,
                                const Levels& cap_lv, long long n_cap, int B, int Hq, int Hkv, int K,
-                               int32_t* idx, float* scores, int* status, cudaStream_t s) {
+                               int32_t* idx, float* scores, int* status, int* arrivals, cudaStream_t s) {
   switch (Hq / Hkv) {
-    case 1: return launch_decode_G<1>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, s);
-    case 2: return launch_decode_G<2>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, s);
-    case 4: return launch_decode_G<4>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, s);
-    case 8: return launch_decode_G<8>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, s);
-    case 16: return launch_decode_G<16>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, s);
+    case 1: return launch_decode_G<1>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, arrivals, s);
+    case 2: return launch_decode_G<2>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, arrivals, s);
+    case 4: return launch_decode_G<4>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, arrivals, s);
+    case 8: return launch_decode_G<8>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, arrivals, s);
+    case 16: return launch_decode_G<16>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, B, Hq, Hkv, K, idx, scores, status, arrivals, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -515,9 +515,10 @@ int pisa_select_flat_ex(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t 
   return select_flat_impl(Q, Hq, pyr, N, K, causal, idx, scores, ws, ws_bytes, stream, score_mode);
 }
 
+// Decode workspace: [status 256 B][one arrival counter per sequence], zeroed per call.
 size_t pisa_decode_workspace_bytes(int B, int Hq, int Hkv, int K) {
   if (check_geometry(B, 1, Hq, Hkv, kD, kC, 2, K) != PISA_OK) return 0;
-  return align_up(kStatusBytes);
+  return align_up(kStatusBytes + sizeof(int) * (size_t)B);
 }
 
 int pisa_decode_append_and_select(const void* q_new, const void* k_new, int Hq, const pisa_pyramid* pyr,
@@ -530,14 +531,16 @@ int pisa_decode_append_and_select(const void* q_new, const void* k_new, int Hq, 
   if (st) return st;
   if (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) return PISA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(q_new) & 15) return PISA_ERR_INVALID_ARG;  // read 16 bytes at a time
-  if (ws_bytes < align_up(kStatusBytes)) return PISA_ERR_WORKSPACE_TOO_SMALL;
+  const size_t zero = kStatusBytes + sizeof(int) * (size_t)pyr->B;
+  if (ws_bytes < align_up(zero)) return PISA_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes, s);
+  cudaError_t e = cudaMemsetAsync(ws, 0, zero, s);
   if (e != cudaSuccess) return PISA_ERR_CUDA;
   const Levels cap_lv = make_levels(pyr->n_cap, pyr->n_cap);
   e = launch_decode_warp(static_cast<const __nv_bfloat16*>(q_new), static_cast<const __nv_bfloat16*>(k_new),
                          static_cast<__nv_bfloat16*>(pyr->keys), pyr->summaries, pyr->lengths, cap_lv,
-                         pyr->n_cap, pyr->B, Hq, pyr->Hkv, K, idx, scores, static_cast<int*>(ws), s);
+                         pyr->n_cap, pyr->B, Hq, pyr->Hkv, K, idx, scores, static_cast<int*>(ws),
+                         reinterpret_cast<int*>(static_cast<char*>(ws) + kStatusBytes), s);
   return cuda_status(e);
 }
 

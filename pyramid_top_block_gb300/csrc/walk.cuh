@@ -19,7 +19,7 @@
 
 namespace pisa {
 
-struct WarpScratch {
+struct __align__(16) WarpScratch {
   int cand[2 * kMaxK];
   float score[2 * kMaxK];
   int next[kMaxK];
@@ -38,9 +38,14 @@ __device__ __forceinline__ void warp_topk(WarpScratch& ws, int nC, int K, int la
     if (ci < nC) {
       const float sc = ws.score[ci];
       int rank = 0;
-      for (int j = 0; j < nC; ++j) {
-        const float o = ws.score[j];
-        rank += (o > sc) || (o == sc && j < ci);
+      const float4* s4 = reinterpret_cast<const float4*>(ws.score);  // 4 scores per load
+      for (int q4 = 0; 4 * q4 < nC; ++q4) {
+        const float4 o = s4[q4];
+        const int q = 4 * q4;
+        rank += (q < nC && (o.x > sc || (o.x == sc && q < ci)));
+        rank += (q + 1 < nC && (o.y > sc || (o.y == sc && q + 1 < ci)));
+        rank += (q + 2 < nC && (o.z > sc || (o.z == sc && q + 2 < ci)));
+        rank += (q + 3 < nC && (o.w > sc || (o.w == sc && q + 3 < ci)));
       }
       sel[s] = rank < K;
     }
