@@ -40,9 +40,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
                   "walk": ["walk_mma.cu", "tc.cuh", "common.cuh", "api.cuh"]}
 NCU_TRAFFIC = {
-    ("leaf", "latency-256k"): {"bytes": 1888564000 + 35622912, "src_sha1": "c98ce3d8da7128f0c2e53308cf5d2f696a1390e7",
+    ("leaf", "latency-256k"): {"bytes": 1888564000 + 35622912, "src_sha1": "5dcf7bbc21ce5ed0c429865bc63dd6c1d2a5cc25",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
-    ("walk", "latency-256k"): {"bytes": 1076219000 + 34968064, "src_sha1": "24dbfbe0de7c58e3127c7193c55b0a7f56142c6e",
+    ("walk", "latency-256k"): {"bytes": 1076219000 + 34968064, "src_sha1": "d565c194f561ff8c9f0d56ee5c7f476a44613729",
                                "profile": "profiles/walk_k8s_kernel_latency-256k.md"},
 }
 
