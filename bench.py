@@ -40,9 +40,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
                   "walk": ["walk_mma.cu", "tc.cuh", "common.cuh", "api.cuh"]}
 NCU_TRAFFIC = {
-    ("leaf", "latency-256k"): {"bytes": 1888564000 + 35622912, "src_sha1": "5dcf7bbc21ce5ed0c429865bc63dd6c1d2a5cc25",
+    ("leaf", "latency-256k"): {"bytes": 1888564000 + 35622912, "src_sha1": "254c9572eea6b39af6276a5a22a5cfa9632af98b",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
-    ("walk", "latency-256k"): {"bytes": 1076219000 + 34968064, "src_sha1": "d565c194f561ff8c9f0d56ee5c7f476a44613729",
+    ("walk", "latency-256k"): {"bytes": 1076219000 + 34968064, "src_sha1": "0c764edecc6a81da6b9154e4357f1362cd3de62c",
                                "profile": "profiles/walk_k8s_kernel_latency-256k.md"},
 }
 

@@ -64,21 +64,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// 16-byte asynchronous global -> shared copy (L2 only), grouped per thread.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-// Makes this thread's generic-proxy shared-memory writes visible to the async
-// proxy (tensor-core operand reads).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // UMMA shared-memory descriptor: K-major operand, 128-byte swizzle, rows of
 // 128 bytes (64 bf16), 8-row groups 1024 bytes apart (SBO), descriptor version 1.
 __device__ __forceinline__ uint64_t umma_desc_sw128(const void* p) {
@@ -91,14 +76,8 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(
-          tmem_d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-
-// The same MMA with the accumulate flag fixed: D = A*B (first k-step) or D += A*B.
+// tcgen05.mma kind::f16 (bf16 A and B from shared memory, fp32 D in TMEM): D = A*B
+// (first k-step) or D += A*B.
 __device__ __forceinline__ void umma_bf16_first(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc) {
   asm volatile(
       "{ .reg .pred p; setp.ne.b32 p, 0, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(tmem_d),
