@@ -40,9 +40,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
                   "walk": ["walk_mma.cu", "tc.cuh", "common.cuh", "api.cuh"]}
 NCU_TRAFFIC = {
-    ("leaf", "latency-256k"): {"bytes": 1888564000 + 35622912, "src_sha1": "254c9572eea6b39af6276a5a22a5cfa9632af98b",
+    ("leaf", "latency-256k"): {"bytes": 1888564000 + 35622912, "src_sha1": "71983897ed7c4f0236c161bd056afafd194423cc",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
-    ("walk", "latency-256k"): {"bytes": 1076219000 + 34968064, "src_sha1": "0c764edecc6a81da6b9154e4357f1362cd3de62c",
+    ("walk", "latency-256k"): {"bytes": 1076219000 + 34968064, "src_sha1": "0f2bba68dbade201e7831b7f18bf2ac6283b2387",
                                "profile": "profiles/walk_k8s_kernel_latency-256k.md"},
 }
 

@@ -32,6 +32,7 @@ struct LeafTcLaunch {
   const int32_t* srank;  // rank of each survivor inside its bucket (from the walk)
   int* bucket_off;
   int* tile_off;
+  int* scan_part;  // 2 + 2 * ceil(buckets / 4096) ints of scan scratch
   int4* tile_desc;      // [max_tiles] {first entry, rows, level-2 survivor p, b * Hkv + kv}
   long long max_tiles;  // upper bound on the number of tiles
   uint32_t* list;

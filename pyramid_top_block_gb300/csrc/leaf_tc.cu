@@ -487,88 +487,123 @@ __global__ void leaf_scatter_kernel(const int32_t* __restrict__ surv, long long 
 
 // Exclusive scans of the bucket sizes (entries) and of their tile counts
 // ceil(size / R) over buckets [0, nb) of the pointers given, continuing from the
-// offsets already at bucket_off[0] / tile_off[0] (zero when `first`).  One CTA of
-// 1024 threads sweeps the buckets in tiles of 1024 * kScanItems, each thread
-// kScanItems consecutive buckets (coalesced), warp shuffles and one shared array
-// for the in-tile scan, a running carry between tiles; each tile's counts are
-// loaded while the previous tile is scanned.
+// offsets already at bucket_off[0] / tile_off[0] (zero when `first`), in two
+// passes over tiles of kScanTile buckets, one CTA of 1024 threads per tile, each
+// thread kScanItems consecutive buckets (coalesced): the tiles' sums, then each
+// tile's scan from the carry-in plus the sums of the tiles before it.  part[0..1]
+// holds the carry-in, part[2 + 2x .. 3 + 2x] the sums of tile x.
 constexpr int kScanItems = 4;
-__global__ void __launch_bounds__(1024) leaf_scan_kernel(const int* __restrict__ count, int nb, int R, int first,
-                                                          int* __restrict__ bucket_off, int* __restrict__ tile_off) {
-  __shared__ int we[32], wt[32];
-  __shared__ int carry[2];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int lgR = __ffs(R) - 1;  // R = 128 / max(G, 8) is a power of two
-  if (tid == 0) {
-    carry[0] = first ? 0 : bucket_off[0];
-    carry[1] = first ? 0 : tile_off[0];
+constexpr int kScanTile = 1024 * kScanItems;
+
+// Block-wide sum of two values (every thread gets both).
+__device__ __forceinline__ int2 block_sum2(int a, int b, int2* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(kFull, a, o);
+    b += __shfl_xor_sync(kFull, b, o);
+  }
+  if (lane == 0) sh[warp] = make_int2(a, b);
+  __syncthreads();
+  int2 v = lane < (int)(blockDim.x >> 5) ? sh[lane] : make_int2(0, 0);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    v.x += __shfl_xor_sync(kFull, v.x, o);
+    v.y += __shfl_xor_sync(kFull, v.y, o);
   }
   __syncthreads();
-  int cn[kScanItems];
+  return v;
+}
+
+__global__ void __launch_bounds__(1024) leaf_scan_sums_kernel(const int* __restrict__ count, int nb, int R, int first,
+                                                               const int* __restrict__ bucket_off,
+                                                               const int* __restrict__ tile_off, int* __restrict__ part) {
+  __shared__ int2 sh[32];
+  const int lgR = __ffs(R) - 1;  // R = 128 / max(G, 8) is a power of two
+  const int i = blockIdx.x * kScanTile + kScanItems * threadIdx.x;
+  int se = 0, st = 0;
 #pragma unroll
-  for (int q = 0; q < kScanItems; ++q) cn[q] = kScanItems * tid + q < nb ? count[kScanItems * tid + q] : 0;
-  for (int base = 0; base < nb; base += 1024 * kScanItems) {
-    const int i = base + kScanItems * tid;
-    int c[kScanItems];  // (tile counts are recomputed from c where needed)
-    int se = 0, st = 0;
-#pragma unroll
-    for (int q = 0; q < kScanItems; ++q) {
-      c[q] = cn[q];
-      se += c[q];
-      st += (c[q] + R - 1) >> lgR;
+  for (int q = 0; q < kScanItems; ++q) {
+    const int c = i + q < nb ? count[i + q] : 0;
+    se += c;
+    st += (c + R - 1) >> lgR;
+  }
+  const int2 tot = block_sum2(se, st, sh);
+  if (threadIdx.x == 0) {
+    part[2 + 2 * blockIdx.x] = tot.x;
+    part[3 + 2 * blockIdx.x] = tot.y;
+    if (blockIdx.x == 0) {
+      part[0] = first ? 0 : bucket_off[0];
+      part[1] = first ? 0 : tile_off[0];
     }
-    const int inext = i + 1024 * kScanItems;
+  }
+}
+
+__global__ void __launch_bounds__(1024) leaf_scan_kernel(const int* __restrict__ count, int nb, int R,
+                                                          const int* __restrict__ part, int* __restrict__ bucket_off,
+                                                          int* __restrict__ tile_off) {
+  __shared__ int2 sh[32];
+  __shared__ int we[32], wt[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lgR = __ffs(R) - 1;
+  // carry-in of this tile: the stage's carry plus the sums of the tiles before it
+  int pe = 0, pt = 0;
+  for (int y = tid; y < (int)blockIdx.x; y += blockDim.x) {
+    pe += part[2 + 2 * y];
+    pt += part[3 + 2 * y];
+  }
+  const int2 carry = block_sum2(pe, pt, sh);
+  const int i = blockIdx.x * kScanTile + kScanItems * tid;
+  int c[kScanItems];
+  int se = 0, st = 0;
 #pragma unroll
-    for (int q = 0; q < kScanItems; ++q) cn[q] = inext + q < nb ? count[inext + q] : 0;
-    int ie = se, it = st;  // inclusive scan over the warp
+  for (int q = 0; q < kScanItems; ++q) {
+    c[q] = i + q < nb ? count[i + q] : 0;
+    se += c[q];
+    st += (c[q] + R - 1) >> lgR;
+  }
+  int ie = se, it = st;  // inclusive scan over the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ve = __shfl_up_sync(kFull, ie, o), vt = __shfl_up_sync(kFull, it, o);
+    if (lane >= o) {
+      ie += ve;
+      it += vt;
+    }
+  }
+  if (lane == 31) {
+    we[warp] = ie;
+    wt[warp] = it;
+  }
+  __syncthreads();
+  if (warp == 0) {  // scan of the 32 warp totals
+    int xe = we[lane], xt = wt[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int ve = __shfl_up_sync(kFull, ie, o), vt = __shfl_up_sync(kFull, it, o);
+      const int ve = __shfl_up_sync(kFull, xe, o), vt = __shfl_up_sync(kFull, xt, o);
       if (lane >= o) {
-        ie += ve;
-        it += vt;
+        xe += ve;
+        xt += vt;
       }
     }
-    if (lane == 31) {
-      we[warp] = ie;
-      wt[warp] = it;
-    }
-    __syncthreads();
-    if (warp == 0) {  // scan of the 32 warp totals
-      int xe = we[lane], xt = wt[lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int ve = __shfl_up_sync(kFull, xe, o), vt = __shfl_up_sync(kFull, xt, o);
-        if (lane >= o) {
-          xe += ve;
-          xt += vt;
-        }
-      }
-      we[lane] = xe;
-      wt[lane] = xt;
-    }
-    __syncthreads();
-    int oe = carry[0] + (warp ? we[warp - 1] : 0) + ie - se;
-    int ot = carry[1] + (warp ? wt[warp - 1] : 0) + it - st;
-#pragma unroll
-    for (int q = 0; q < kScanItems; ++q) {
-      if (i + q < nb) {
-        bucket_off[i + q] = oe;
-        tile_off[i + q] = ot;
-      }
-      oe += c[q];
-      ot += (c[q] + R - 1) >> lgR;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      carry[0] += we[31];
-      carry[1] += wt[31];
-    }
-    __syncthreads();
+    we[lane] = xe;
+    wt[lane] = xt;
   }
-  if (tid == 0) {
-    bucket_off[nb] = carry[0];
-    tile_off[nb] = carry[1];
+  __syncthreads();
+  int oe = part[0] + carry.x + (warp ? we[warp - 1] : 0) + ie - se;
+  int ot = part[1] + carry.y + (warp ? wt[warp - 1] : 0) + it - st;
+#pragma unroll
+  for (int q = 0; q < kScanItems; ++q) {
+    if (i + q < nb) {
+      bucket_off[i + q] = oe;
+      tile_off[i + q] = ot;
+    }
+    oe += c[q];
+    ot += (c[q] + R - 1) >> lgR;
+  }
+  if (blockIdx.x == gridDim.x - 1 && tid == 0) {
+    bucket_off[nb] = part[0] + carry.x + we[31];
+    tile_off[nb] = part[1] + carry.y + wt[31];
   }
 }
 
@@ -803,9 +838,16 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
   const int Gp = G < 8 ? 8 : G;
   const int R = 128 / Gp;
   // bucket sizes were counted by the walk kernel as it wrote the survivors
-  leaf_scan_kernel<<<1, 1024, 0, s>>>(L.count + L.b0, L.b1 - L.b0, R, L.b0 == 0, L.bucket_off + L.b0,
-                                      L.tile_off + L.b0);
-  note_launch();
+  const int nbs = L.b1 - L.b0;
+  const unsigned tiles = (unsigned)((nbs + kScanTile - 1) / kScanTile);
+  if (tiles > 0) {
+    leaf_scan_sums_kernel<<<tiles, 1024, 0, s>>>(L.count + L.b0, nbs, R, L.b0 == 0, L.bucket_off + L.b0,
+                                                 L.tile_off + L.b0, L.scan_part);
+    note_launch();
+    leaf_scan_kernel<<<tiles, 1024, 0, s>>>(L.count + L.b0, nbs, R, L.scan_part, L.bucket_off + L.b0,
+                                            L.tile_off + L.b0);
+    note_launch();
+  }
   leaf_scatter_kernel<<<(unsigned)((entries + 255) / 256), 256, 0, s>>>(
       L.surv, L.t0, L.t1, BH, L.K, L.N, L.chunk_shift, L.M2, L.bucket_off, L.srank, L.list);
   note_launch();

@@ -86,6 +86,7 @@ int chunk_shift_for(long long N) {
 // Workspace of the prefill selection (every slice 256-byte aligned):
 //   [status 256 B][count nb]                  zeroed at every call
 //   [bucket_off nb+1][tile_off nb+1]           scans of the bucket sizes
+//   [scan_part 2 + 2 ceil(nb/4096)]            the scan's carry-in and per-tile sums
 //   [tile_desc: max_tiles int4]                first entry, rows, p, b*Hkv+kv of each leaf tile
 //   [surv2: B*Hkv*N*K int32]                   level-2 survivors
 //   [srank: B*Hkv*N*K int32]                   rank of each survivor inside its bucket
@@ -94,7 +95,7 @@ int chunk_shift_for(long long N) {
 //   [route table: B*Hkv*rows x 256 B]          per-node logit-step rows of the walk
 // with nb = B * Hkv * nchunks * M2 buckets (chunk of queries, level-2 node).
 struct PrefillWs {
-  size_t status, count, srank, bucket_off, tile_off, tile_desc, surv, list, leaf, table, total, zero_bytes;
+  size_t status, count, srank, bucket_off, tile_off, scan_part, tile_desc, surv, list, leaf, table, total, zero_bytes;
   long long max_tiles;
   long long nb;
   int nchunks, chunk_shift, M2;
@@ -118,6 +119,8 @@ PrefillWs prefill_layout(int B, long long N, int Hkv, int K) {
   o += align_up(sizeof(int) * (size_t)(w.nb + 1));
   w.tile_off = o;
   o += align_up(sizeof(int) * (size_t)(w.nb + 1));
+  w.scan_part = o;  // the bucket scan's carry-in and per-4096-bucket sums
+  o += align_up(sizeof(int) * (size_t)(2 + 2 * ((w.nb + 4095) / 4096)));
   // a tile holds R = 128 / max(G, 8) >= 8 queries: at most entries / 8 + nb tiles
   w.max_tiles = (long long)(entries / 8) + w.nb + 1;
   w.tile_desc = o;
@@ -286,6 +289,7 @@ static void prefill_plan(PrefillPlan& P, const void* Q, int Hq, const pisa_pyram
   L.srank = reinterpret_cast<int32_t*>(base + w.srank);
   L.bucket_off = reinterpret_cast<int*>(base + w.bucket_off);
   L.tile_off = reinterpret_cast<int*>(base + w.tile_off);
+  L.scan_part = reinterpret_cast<int*>(base + w.scan_part);
   L.tile_desc = reinterpret_cast<int4*>(base + w.tile_desc);
   L.max_tiles = w.max_tiles;
   L.list = reinterpret_cast<uint32_t*>(base + w.list);
