@@ -71,6 +71,34 @@ def test_argument_errors_without_launch():
                                              ctypes.c_void_p(0x4000), 1 << 20, None) == 1
 
 
+def test_host_selection_argument_errors_without_launch():
+    """pisa_select_prefill_host rejects bad arguments before it touches a stream."""
+    lib = pisa.load()
+    st = pisa._PyrStruct(0x1000, 0x2000, 0x6000, 1, 2, 64, 64, 2, 128)
+    vp = ctypes.c_void_p
+    good = dict(K_host=vp(0x7000), Q_host=vp(0x8000), Q_dev=vp(0x3000), idx_host=vp(0x9000), idx_dev=vp(0x5000))
+
+    def call(N=128, Hq=32, K=8, ws_bytes=1 << 30, **over):
+        a = dict(good, **over)
+        return lib.pisa_select_prefill_host(ctypes.byref(st), a["K_host"], N, a["Q_host"], a["Q_dev"], Hq, K, 1,
+                                            a["idx_host"], a["idx_dev"], vp(0x4000), ws_bytes, None, None)
+
+    assert call(K_host=None) == 1
+    assert call(Q_host=None) == 1
+    assert call(idx_host=None) == 1
+    assert call(idx_dev=None) == 1
+    assert call(Q_dev=vp(0x3008)) == 1           # device Q not 16-byte aligned
+    assert call(N=129) == 1                     # N > n_cap
+    assert call(K=40) == 2                      # K too large
+    assert call(Hq=6) == 2                      # group of 3
+    assert call(ws_bytes=16) == 3               # workspace too small
+
+
+def test_decode_workspace_counts_one_arrival_slot_per_sequence():
+    assert pisa.decode_workspace_bytes(1, 32, 2, 8) >= 256 + 4
+    assert pisa.decode_workspace_bytes(300, 32, 2, 8) >= 256 + 4 * 300
+
+
 def test_status_strings():
     for s in range(7):
         assert pisa.status_string(s)
