@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 METRIC = "selection ms/pass and query-rows/s at 32K–256K; % of roofline (1×GB300)"
 UNIT = "query-rows/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+MUFU_EX2_PER_CLK_SM = 29.0  # measured ex2.approx throughput per SM and clock on GB300 (probe, 1 GPU)
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # kernels that can dominate a pass, from one ncu capture of the workload named
@@ -350,9 +351,14 @@ def run_ours(args):
     work = {"exps": alg["exps"], "leaf_row_gather_bytes": alg["leaf_row_gather_bytes"],
             "note": "north-star work model (non-causal upper bound); leaf_row_gather_bytes = query rows "
                     "gathered once per (query, KV head, level-2 survivor)"}
+    # informative third bound (not part of the spec roofline): the work model's
+    # exponentials at the exponential unit's rate measured on this GPU (ex2 ~29 per clock
+    # per SM, 152 SMs at 2.07 GHz)
+    t_exp = alg["exps"] / (MUFU_EX2_PER_CLK_SM * 152 * 2.07e9) * 1e3
     pass_roof = {"flops": alg["flops"], "min_bytes": alg["bytes"], "t_tensor_ms": t_tensor, "t_hbm_ms": t_hbm,
                  "t_roofline_ms": max(t_tensor, t_hbm), "frac": max(t_tensor, t_hbm) / ms_step,
-                 "peaks": f"{pk_kind}: {tf_peak} TFLOP/s bf16 burst, {pk['hbm_gbs']} GB/s"}
+                 "peaks": f"{pk_kind}: {tf_peak} TFLOP/s bf16 burst, {pk['hbm_gbs']} GB/s",
+                 "t_exp_ms": t_exp, "frac_with_exp_bound": max(t_tensor, t_hbm, t_exp) / ms_step}
 
     # end to end through the public API with host buffers (pinned): every step copies K and
     # Q in and the indices out (pisa_select_prefill_host overlaps the copies with the
