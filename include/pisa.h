@@ -269,6 +269,19 @@ int pisa_select_prefill_noalloc(const void* Q, int Hq, const pisa_pyramid* pyr, 
                                 int causal, int32_t* idx, float* scores, void* stream);
 
 /*
+ * pisa_selftest_bounded_wait -- the failure path of the kernels' bounded barrier
+ * waits, exercised on the GPU without faulting it: one thread waits on an mbarrier
+ * that nothing arrives on, through the same wait routine the tcgen05 kernels use,
+ * while another warp of its CTA raises the CTA's abort flag after delay_cycles clock
+ * cycles (0 <= delay_cycles <= 2^32); the wait gives up and the kernel records
+ * PISA_ERR_DEVICE_TIMEOUT in the status word of ws (device memory, >= 256 bytes,
+ * 256-byte aligned, zeroed here first) and returns.  Read it with
+ * pisa_check_device_status.  Returns PISA_ERR_INVALID_ARG / _WORKSPACE_TOO_SMALL on
+ * bad arguments, before anything is launched.
+ */
+int pisa_selftest_bounded_wait(void* ws, size_t ws_bytes, int64_t delay_cycles, void* stream);
+
+/*
  * Synchronises `stream` and returns the status word that kernels of the last
  * select / decode call on this workspace left in `ws` (PISA_OK if none).
  */

@@ -68,6 +68,8 @@ def load(path: str | None = None):
     lib.pisa_select_prefill_ex.restype = i32
     lib.pisa_select_prefill_host.argtypes = [vp, vp, i64, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp, vp]
     lib.pisa_select_prefill_host.restype = i32
+    lib.pisa_selftest_bounded_wait.argtypes = [vp, sz, i64, vp]
+    lib.pisa_selftest_bounded_wait.restype = i32
     lib.pisa_select_flat_ex.argtypes = [vp, i32, vp, i64, i32, i32, vp, vp, vp, sz, vp, i32]
     lib.pisa_select_flat_ex.restype = i32
     lib.pisa_sparse_attention.argtypes = [vp, i32, vp, vp, i32, i64, i32, vp, i32, i32, vp, vp]
@@ -415,6 +417,13 @@ def event_elapsed_ms(start, end) -> float:
     _check(load().pisa_event_elapsed_ms(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(end.cuda_event),
                                         ctypes.byref(out)), "pisa_event_elapsed_ms")
     return float(out.value)
+
+
+def selftest_bounded_wait(workspace: torch.Tensor, delay_cycles: int = 2_000_000, stream=None) -> None:
+    """Make a kernel's bounded barrier wait run out (nothing arrives; an abort flag goes
+    up after delay_cycles): its status word in `workspace` then reads the timeout code."""
+    _check(load().pisa_selftest_bounded_wait(_ptr(workspace), workspace.numel(), int(delay_cycles), _stream(stream)),
+           "pisa_selftest_bounded_wait")
 
 
 def check_device_status(workspace: torch.Tensor, stream=None) -> int:

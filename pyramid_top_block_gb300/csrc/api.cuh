@@ -74,6 +74,7 @@ struct WalkLaunch {
 };
 
 long long route_rows_per_bh(const Levels& lv);
+cudaError_t launch_selftest_wait(int* status, long long delay_cycles, cudaStream_t s);
 cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s);
 
 cudaError_t launch_decode_warp(const __nv_bfloat16* q_new, const __nv_bfloat16* k_new,

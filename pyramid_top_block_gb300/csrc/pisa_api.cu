@@ -548,6 +548,15 @@ int pisa_decode_append_and_select(const void* q_new, const void* k_new, int Hq, 
   return cuda_status(e);
 }
 
+int pisa_selftest_bounded_wait(void* ws, size_t ws_bytes, int64_t delay_cycles, void* stream) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return PISA_ERR_INVALID_ARG;
+  if (ws_bytes < kStatusBytes) return PISA_ERR_WORKSPACE_TOO_SMALL;
+  if (delay_cycles < 0 || delay_cycles > (1LL << 32)) return PISA_ERR_INVALID_ARG;  // (about 2 s at most)
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, kStatusBytes, s) != cudaSuccess) return PISA_ERR_CUDA;
+  return cuda_status(launch_selftest_wait(static_cast<int*>(ws), delay_cycles, s));
+}
+
 int pisa_check_device_status(const void* ws, void* stream) {
   if (!ws) return PISA_ERR_INVALID_ARG;
   int h = 0;

@@ -99,6 +99,16 @@ def test_decode_workspace_counts_one_arrival_slot_per_sequence():
     assert pisa.decode_workspace_bytes(300, 32, 2, 8) >= 256 + 4 * 300
 
 
+def test_bounded_wait_selftest_argument_errors_without_launch():
+    lib = pisa.load()
+    vp = ctypes.c_void_p
+    assert lib.pisa_selftest_bounded_wait(None, 256, 1000, None) == 1
+    assert lib.pisa_selftest_bounded_wait(vp(0x4010), 256, 1000, None) == 1     # not 256-byte aligned
+    assert lib.pisa_selftest_bounded_wait(vp(0x4000), 16, 1000, None) == 3      # workspace too small
+    assert lib.pisa_selftest_bounded_wait(vp(0x4000), 256, -1, None) == 1
+    assert lib.pisa_selftest_bounded_wait(vp(0x4000), 256, 1 << 40, None) == 1  # more than about 2 s
+
+
 def test_status_strings():
     for s in range(7):
         assert pisa.status_string(s)
