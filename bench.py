@@ -41,9 +41,9 @@ MUFU_EX2_PER_CLK_SM = 29.0  # measured ex2.approx throughput per SM and clock on
 KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
                   "walk": ["walk_mma.cu", "tc.cuh", "common.cuh", "api.cuh"]}
 NCU_TRAFFIC = {
-    ("leaf", "latency-256k"): {"bytes": 1888564000 + 35622912, "src_sha1": "71983897ed7c4f0236c161bd056afafd194423cc",
+    ("leaf", "latency-256k"): {"bytes": 1888564000 + 35622912, "src_sha1": "8aeb7fc3b48b1c50cc7a64dd8bb9859e1566e793",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
-    ("walk", "latency-256k"): {"bytes": 1076219000 + 34968064, "src_sha1": "0f2bba68dbade201e7831b7f18bf2ac6283b2387",
+    ("walk", "latency-256k"): {"bytes": 1076219000 + 34968064, "src_sha1": "61a3d75e23ddecdda610b81081ec03ce9c552976",
                                "profile": "profiles/walk_k8s_kernel_latency-256k.md"},
 }
 
