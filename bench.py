@@ -41,9 +41,9 @@ MUFU_EX2_PER_CLK_SM = 29.0  # measured ex2.approx throughput per SM and clock on
 KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
                   "walk": ["walk_mma.cu", "tc.cuh", "common.cuh", "api.cuh"]}
 NCU_TRAFFIC = {
-    ("leaf", "latency-256k"): {"bytes": 1888564000 + 35622912, "src_sha1": "8aeb7fc3b48b1c50cc7a64dd8bb9859e1566e793",
+    ("leaf", "latency-256k"): {"bytes": 1888564000 + 35622912, "src_sha1": "0b4fa4031203dddd429dfd661fa75d4ab9d19b73",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
-    ("walk", "latency-256k"): {"bytes": 1076219000 + 34968064, "src_sha1": "61a3d75e23ddecdda610b81081ec03ce9c552976",
+    ("walk", "latency-256k"): {"bytes": 1076219000 + 34968064, "src_sha1": "bb6c12db10106a570e3947e0faea7bd22e02bb79",
                                "profile": "profiles/walk_k8s_kernel_latency-256k.md"},
 }
 

@@ -44,19 +44,24 @@ def _fingerprint() -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
-    stamp = os.path.join(BUILD, "libpisa.stamp")
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          name: str = "libpisa") -> str:
+    """Compile every .cu of csrc/ and link _build/<name>.so.  Another name (with, say,
+    extra_flags=["-DPISA_DEBUG_BOUNDS"]) builds a variant beside the default library."""
+    out_dir = BUILD if name == "libpisa" else os.path.join(BUILD, name)
+    os.makedirs(out_dir, exist_ok=True)
+    lib = os.path.join(BUILD, name + ".so")
+    stamp = os.path.join(BUILD, name + ".stamp")
     fp = _fingerprint() + (" ".join(extra_flags) if extra_flags else "")
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
+    if not force and os.path.exists(lib) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == fp:
-                return LIB
+                return lib
     nvcc = _nvcc()
     extra = list(extra_flags or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -68,15 +73,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stderr)
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp, "w") as f:
         f.write(fp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -71,6 +71,7 @@ struct WalkLaunch {
   int mode;  // block score: 0 LSE, 1 mean of the child logits, 2 mean + variance / 2
   long long t0, t1;  // the query positions walked by this launch
   bool build_table;  // build the route table first (once per pyramid state)
+  int* status;       // the call's status word (debug builds record failed index checks there)
 };
 
 long long route_rows_per_bh(const Levels& lv);

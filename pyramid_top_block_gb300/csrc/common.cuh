@@ -90,6 +90,30 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Debug builds (-DPISA_DEBUG_BOUNDS): every gathered index is range-checked on the
+// device; a failed check records PISA_ERR_DEVICE_BOUNDS in the status word of the
+// call (its address set by the launcher into this translation unit's copy of
+// g_bounds_status) and the access is replaced by a harmless one.  Nothing traps.  In
+// the default build the checks are not compiled.
+#ifdef PISA_DEBUG_BOUNDS
+static __device__ int* g_bounds_status;
+__device__ __forceinline__ bool in_bounds(bool ok) {
+  if (!ok) set_status(g_bounds_status, PISA_ERR_DEVICE_BOUNDS);
+  return ok;
+}
+#define PISA_IN_BOUNDS(cond) (::pisa::in_bounds(cond))
+#define PISA_SET_BOUNDS_STATUS(ptr, stream)                                                              \
+  do {                                                                                                   \
+    int* p_ = (ptr);                                                                                     \
+    cudaMemcpyToSymbolAsync(::pisa::g_bounds_status, &p_, sizeof(p_), 0, cudaMemcpyHostToDevice, stream); \
+  } while (0)
+#else
+#define PISA_IN_BOUNDS(cond) (true)
+#define PISA_SET_BOUNDS_STATUS(ptr, stream) \
+  do {                                      \
+  } while (0)
+#endif
+
 // log(exp(a) + exp(b)) without overflow.
 __device__ __forceinline__ float lse2(float a, float b) {
   float m = fmaxf(a, b);

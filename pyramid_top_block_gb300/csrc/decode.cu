@@ -28,6 +28,7 @@ template <int G>
 __device__ __forceinline__ float warp_node_score(const float* blk, long long off1, long long M1, long long off2,
                                                  long long M2, int l, int c, const float* qs, int lane) {
   const int ch = lane >> 4, h = lane & 15;
+  if (!PISA_IN_BOUNDS(c >= 0 && 2LL * c < M1)) c = 0;
   const long long node = 2LL * c + ch;
   const bool two = 2LL * c + 1 < M1;
   float z = 0.f;
@@ -106,6 +107,7 @@ template <int G>
 __device__ __forceinline__ float warp_leaf_mma(const __nv_bfloat16* keys_b, int Hkv, int kv, long long c, long long n,
                                                const uint32_t (&A)[4][4], int lane) {
   const int g = lane >> 2, j = lane & 3;
+  if (!PISA_IN_BOUNDS(c >= 0 && c * kC < n)) c = 0;
   float z[8][4];
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
@@ -331,6 +333,7 @@ static cudaError_t launch_decode_G(const __nv_bfloat16* q_new, const __nv_bfloat
                                    __nv_bfloat16* keys, float* summ, int32_t* lengths,
                                    const Levels& cap_lv, long long n_cap, int B, int Hq, int Hkv,
                                    int K, int32_t* idx, float* scores, int* status, int* arrivals, cudaStream_t s) {
+  PISA_SET_BOUNDS_STATUS(status, s);
   decode_kernel<G><<<B * Hkv, kDecWarps * 32, 0, s>>>(q_new, k_new, keys, summ, lengths, cap_lv, n_cap, Hq, Hkv,
                                           K, idx, scores, status, arrivals);
   note_launch();

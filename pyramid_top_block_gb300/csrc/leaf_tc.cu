@@ -294,8 +294,9 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
             const int bb = nchg % kKeyBufs;
             if (nchg >= kKeyBufs) w = mbar_wait(&b_empty[bb], ((nchg / kKeyBufs) - 1) & 1, abort);
             if (w) {
+              const int pk = PISA_IN_BOUNDS(p >= 0 && p < P.M2 && 128LL * p < P.n_cap && bh >= 0) ? p : 0;
               mbar_expect_tx(&b_full[bb], kTileBytes);
-              tma_load_3d(sB + bb * kTileBytes, &kmap, 0, bh % P.Hkv, (int)((bh / P.Hkv) * P.n_cap + 128LL * p),
+              tma_load_3d(sB + bb * kTileBytes, &kmap, 0, bh % P.Hkv, (int)((bh / P.Hkv) * P.n_cap + 128LL * pk),
                           &b_full[bb]);
             }
           }
@@ -374,9 +375,11 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
         break;
       }
       __syncwarp();
-      if (lane < d.y)
+      if (lane < d.y) {
+        const long long tq = PISA_IN_BOUNDS((long long)(ent >> 5) < P.N && d.w >= 0) ? (long long)(ent >> 5) : 0;
         tma_load_3d(sA + s * kTileBytes + lane * Gp * 128, &qmap, 0, (d.w % P.Hkv) * G,
-                    (int)((d.w / P.Hkv) * P.N + (ent >> 5)), &a_full[s]);
+                    (int)((d.w / P.Hkv) * P.N + tq), &a_full[s]);
+      }
     }
   } else {
     // ---------------- epilogue (warps 4..15): warpgroup wg takes tiles wg, wg + 3, ...;
@@ -438,7 +441,7 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
         v0 += __shfl_xor_sync(kFull, v0, o);
         v1 += __shfl_xor_sync(kFull, v1, o);
       }
-      if (qvalid && h == 0) {
+      if (qvalid && h == 0 && PISA_IN_BOUNDS(t < P.N && (P.flat || qslot < P.K))) {
         float* out = P.flat ? P.leaf_scores + ((long long)tbh * P.N + t) * P.flat_stride + 2 * tp
                             : P.leaf_scores + ((long long)tbh * P.N + t) * (2 * P.K) + 2 * qslot;
         out[0] = v0;
@@ -482,6 +485,7 @@ __global__ void leaf_scatter_kernel(const int32_t* __restrict__ surv, long long 
   const long long job = e / K;
   const int bkt = bucket_of(job, p, N, BH, chunk_shift, M2);
   const int pos = bucket_off[bkt] + srank[e];
+  if (!PISA_IN_BOUNDS(pos >= 0 && pos < (long long)BH * N * K)) return;
   list[pos] = ((uint32_t)(job % N) << 5) | (uint32_t)(e % K);
 }
 
@@ -785,6 +789,7 @@ int sm_count() {
 // The persistent leaf kernel over the tiles described by L.tile_desc (their count is
 // L.tile_off[L.nb]); flat != 0 selects the flat output layout.
 cudaError_t launch_leaf_tc_kernel(const LeafTcLaunch& L, int flat, long long flat_stride, cudaStream_t s) {
+  PISA_SET_BOUNDS_STATUS(L.status, s);  // (the flat selector comes here directly)
   const int G = L.Hq / L.Hkv;
   const int Gp = G < 8 ? 8 : G;
   const int R = 128 / Gp;
@@ -831,6 +836,7 @@ cudaError_t launch_leaf_tc_kernel(const LeafTcLaunch& L, int flat, long long fla
 // buckets are [L.b0, L.b1) (whole query chunks, chunk-major buckets).
 cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
   if (L.t1 <= L.t0) return cudaSuccess;
+  PISA_SET_BOUNDS_STATUS(L.status, s);
   const int BH = L.B * L.Hkv;
   const long long span = L.t1 - L.t0;
   const long long entries = (long long)BH * span * L.K;

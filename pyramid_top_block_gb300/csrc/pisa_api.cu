@@ -270,6 +270,7 @@ static void prefill_plan(PrefillPlan& P, const void* Q, int Hq, const pisa_pyram
   W.t0 = 0;
   W.t1 = N;
   W.build_table = true;
+  W.status = reinterpret_cast<int*>(base + w.status);
   LeafTcLaunch& L = P.L;
   L.Q = static_cast<const __nv_bfloat16*>(Q);
   L.keys = static_cast<const __nv_bfloat16*>(pyr->keys);

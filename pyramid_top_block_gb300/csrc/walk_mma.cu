@@ -282,14 +282,14 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
             const uint4 z = make_uint4(0, 0, 0, 0);
             h0[0] = h0[1] = l0[0] = l0[1] = h1[0] = h1[1] = l1[0] = l1[1] = z;
             if (cached) {
-              if (c0i < nC) {
+              if (c0i < nC && PISA_IN_BOUNDS(S.cand[c0i] >= 0 && S.cand[c0i] < lv.M[l])) {
                 const uint4* p = reinterpret_cast<const uint4*>(crow + S.cand[c0i] * kCacheRowBytes + 32 * j);
                 h0[0] = p[0];
                 h0[1] = p[1];
                 l0[0] = p[8];
                 l0[1] = p[9];
               }
-              if (c1i < nC) {
+              if (c1i < nC && PISA_IN_BOUNDS(S.cand[c1i] >= 0 && S.cand[c1i] < lv.M[l])) {
                 const uint4* p = reinterpret_cast<const uint4*>(crow + S.cand[c1i] * kCacheRowBytes + 32 * j);
                 h1[0] = p[0];
                 h1[1] = p[1];
@@ -297,14 +297,14 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
                 l1[1] = p[9];
               }
             } else {
-              if (c0i < nC) {
+              if (c0i < nC && PISA_IN_BOUNDS(S.cand[c0i] >= 0 && S.cand[c0i] < lv.M[l])) {
                 const uint4* p = reinterpret_cast<const uint4*>(lrow + (long long)S.cand[c0i] * kRowBytes + 32 * j);
                 h0[0] = __ldg(p);
                 h0[1] = __ldg(p + 1);
                 l0[0] = __ldg(p + 8);
                 l0[1] = __ldg(p + 9);
               }
-              if (c1i < nC) {
+              if (c1i < nC && PISA_IN_BOUNDS(S.cand[c1i] >= 0 && S.cand[c1i] < lv.M[l])) {
                 const uint4* p = reinterpret_cast<const uint4*>(lrow + (long long)S.cand[c1i] * kRowBytes + 32 * j);
                 h1[0] = __ldg(p);
                 h1[1] = __ldg(p + 1);
@@ -449,7 +449,8 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
       int p = -1;
       if (lane < nS) p = S.cand[S.sel[lane]];
       out[lane] = p;
-      if (p >= 0) srank[job * K + lane] = atomicAdd(count + (((long long)(t >> chunk_shift) * gridDim.y + bh) * M2 + p), 1);
+      if (p >= 0 && PISA_IN_BOUNDS(p < M2))
+        srank[job * K + lane] = atomicAdd(count + (((long long)(t >> chunk_shift) * gridDim.y + bh) * M2 + p), 1);
     }
     __syncwarp();
   }
@@ -650,7 +651,8 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
       const int na = s ? c_oth : c, nb = s ? c : c_oth;
       const bool va = g < nC, vb = g + 8 < nC;
       // candidates >= nC read row 0 of the level (their results are never kept)
-      const int ra_row = va ? na : 0, rb_row = vb ? nb : 0;
+      int ra_row = va ? na : 0, rb_row = vb ? nb : 0;
+      if (!PISA_IN_BOUNDS(ra_row >= 0 && ra_row < lv.M[l] && rb_row >= 0 && rb_row < lv.M[l])) ra_row = rb_row = 0;
       uint4 ra[4], rb[4];
       if (l >= l_lo) {
         const unsigned char* base = cdr + lt4.x + 32 * j;
@@ -757,7 +759,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
       const unsigned bk = __ballot_sync(kFull, keep), b2 = __ballot_sync(kFull, keep && two);
       const int before = s ? __popc(bk & kLo) + __popc(bk & kHi & lt) : __popc(bk & kLo & lt);
       if (l == 2) {
-        if (j < 2 && keep) {
+        if (j < 2 && keep && PISA_IN_BOUNDS(c >= 0 && c < M2 && before < K)) {
           out[before] = c;
           rk[before] = atomicAdd(cnt + c, 1);
         }
@@ -940,7 +942,8 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8s_kernel(
       const int rag = lt4.z;
       const float rnr = __int_as_float(lt4.w);
       const bool va = g < nC, vb = g + 8 < nC;
-      const int ra_row = va ? na : 0, rb_row = vb ? nb : 0;  // (rows >= nC: never kept)
+      int ra_row = va ? na : 0, rb_row = vb ? nb : 0;  // (rows >= nC: never kept)
+      if (!PISA_IN_BOUNDS(ra_row >= 0 && ra_row < lv.M[l] && rb_row >= 0 && rb_row < lv.M[l])) ra_row = rb_row = 0;
       uint4 ra[4], rb[4];
       if (l >= l_lo) {
         const unsigned char* base = cdr + lt4.x + 32 * j;
@@ -1023,7 +1026,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8s_kernel(
         int32_t* out = surv + job * K;
         int32_t* rk = srank + job * K;
         int* cnt = count + ((long long)(t >> chunk_shift) * gridDim.y + bh) * M2;  // chunk-major buckets
-        if (b2 == 0 && keep) {
+        if (b2 == 0 && keep && PISA_IN_BOUNDS(c >= 0 && c < M2 && before < K)) {
           out[before] = c;
           rk[before] = atomicAdd(cnt + c, 1);
         }
@@ -1034,7 +1037,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8s_kernel(
       {
         const float zr = Z + sum_u, zo = fmaf(nr, sum_u, Z);
         int* buf = cbuf + ((l & 1) << 5);
-        if (b2 == 0 && keep) {
+        if (b2 == 0 && keep && PISA_IN_BOUNDS(before + __popc(b2k & below) + (two ? 1 : 0) < 16)) {
           const int pos = before + __popc(b2k & below);
           buf[pos] = 2 * c;
           buf[16 + pos] = __float_as_int(ref1 ? zo : zr);
@@ -1083,6 +1086,7 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
       break;
     }
   cudaError_t e = cudaSuccess;
+  PISA_SET_BOUNDS_STATUS(W.status, s);
   if (W.build_table) {
     const long long thr = (long long)BH * rows * 32;
     route_table_kernel<<<(unsigned)((thr + 255) / 256), 256, 0, s>>>(W.summ, lv, W.N, BH, rows, ro, l_start, W.table);
