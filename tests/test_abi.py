@@ -28,6 +28,17 @@ def test_library_exports_every_declared_function():
         assert hasattr(lib, n), n
 
 
+def test_debug_bounds_build_compiles_and_exports_the_same_functions():
+    """The -DPISA_DEBUG_BOUNDS variant (device-side index checks) builds beside the default
+    library and exports the same C ABI; nothing is launched."""
+    from pyramid_top_block_gb300 import build
+    path = build.build(extra_flags=["-DPISA_DEBUG_BOUNDS"], name="libpisa_debug")
+    assert os.path.basename(path) == "libpisa_debug.so" and path != build.LIB
+    lib = ctypes.CDLL(path)
+    for n in _declared():
+        assert hasattr(lib, n), n
+
+
 @pytest.mark.parametrize("n", [1, 2, 63, 64, 65, 200, 2048, 16421, 131073, 262144, 1 << 30])
 def test_level_geometry_matches_oracle(n):
     assert pisa.num_levels(n) == oracle.num_levels(n)
