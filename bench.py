@@ -83,7 +83,7 @@ def level_sizes(n, C=64):
 
 
 def algorithmic(w):
-    """North-star work model of one pass (non-causal upper bound).
+    """Work model of one selection pass, as the metric defines it (non-causal upper bound).
 
     FLOPs = Hq*B*N*[g*K*C*2d (leaf) + (#scored intermediate levels)*g*K*g*2d]
     bytes = Q + K read once + pyramid written and read once + idx written.
@@ -349,9 +349,9 @@ def run_ours(args):
     ms_stats = {"mean": ms_step, "median": statistics.median(ms), "min": min(ms), "runs": n}
     rates = {"query_rows_per_s": value, "kv_rows_per_s": value * Hkv, "head_rows_per_s": value * Hq}
     work = {"exps": alg["exps"], "leaf_row_gather_bytes": alg["leaf_row_gather_bytes"],
-            "note": "north-star work model (non-causal upper bound); leaf_row_gather_bytes = query rows "
+            "note": "the metric's work model (non-causal upper bound); leaf_row_gather_bytes = query rows "
                     "gathered once per (query, KV head, level-2 survivor)"}
-    # informative third bound (not part of the spec roofline): the work model's
+    # informative third bound (not part of the metric's roofline): the work model's
     # exponentials at the exponential unit's rate measured on this GPU (ex2 ~29 per clock
     # per SM, 152 SMs at 2.07 GHz)
     t_exp = alg["exps"] / (MUFU_EX2_PER_CLK_SM * 152 * 2.07e9) * 1e3

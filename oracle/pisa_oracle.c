@@ -17,7 +17,7 @@
  *        Top-K ..." (news summary)                         -> the same walk, the
  *        latency-benchmark shape (C=64, g=2, K=8, d=64).
  *
- * Readings where the pages are silent (each one is also listed in the design doc):
+ * Readings where the pages are silent:
  *   - logits are scaled by 1/sqrt(d);
  *   - a ragged node is the mean over the tokens actually present;
  *   - causal: a node is eligible for query t iff its first token is <= t; a
