@@ -89,6 +89,12 @@ def _load():
         lib.pisa_oracle_node_score.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, i64,
                                                i32, i64, i32]
         lib.pisa_oracle_node_score.restype = dbl
+        lib.pisa_oracle_check_selection.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, i32, i32, i32,
+                                                    vp, i64, vp, dbl, i32, i32, vp, i32]
+        lib.pisa_oracle_check_selection.restype = i32
+        lib.pisa_oracle_check_last.argtypes = [vp, vp, i32, i64, vp, i32, i32, i32, i32, i32, i32,
+                                               vp, dbl, vp, i32]
+        lib.pisa_oracle_check_last.restype = i32
         _lib = lib
         return lib
 
@@ -261,3 +267,54 @@ def node_score(q_row, keys, level: int, node: int, t: int, kv: int = 0, C: int =
     Hq = qq.shape[0]
     return float(_load().pisa_oracle_node_score(_ptr(qq), _ptr(k), N, Hq, Hkv, d, C, g, int(causal),
                                                 kv, t, level, node, mode))
+
+
+def check_selection(q, keys, t_list, sel, K: int, tie: float = 1e-3, C: int = 64, g: int = 2,
+                    causal: bool = True, flat: bool = False, mode: int = 0, threads: int = 0):
+    """Is each given leaf set one that the walk (or, with flat=True, the flat
+    selector) reaches when near ties -- score differences below ``tie`` -- are
+    broken either way?  The walk is re-taken along the given leaves: every
+    scored level must keep a near Top-K that contains their ancestors (all
+    near-Top-K completions are tried), and the leaf level must keep exactly them.
+
+    q [B, n_t, Hq, d] rows of t_list; keys [B, N, Hkv, d]; sel [B, Hkv, n_t, K].
+    Returns int32 [B, Hkv, n_t]: 1 reachable, 0 not (or malformed), -1 undecided
+    (search budget exhausted)."""
+    k = _f32(keys)
+    B, N, Hkv, d = k.shape
+    qq = _f32(q)
+    Hq = qq.shape[2]
+    t = np.ascontiguousarray(t_list, dtype=np.int64)
+    if qq.shape[1] != len(t):
+        raise ValueError("q must hold one row per listed query position")
+    s = np.ascontiguousarray(sel, dtype=np.int32)
+    if s.shape != (B, Hkv, len(t), K):
+        raise ValueError("sel must be [B, Hkv, n_t, K]")
+    out = np.empty((B, Hkv, len(t)), dtype=np.int32)
+    rc = _load().pisa_oracle_check_selection(_ptr(qq), _ptr(k), B, N, Hq, Hkv, d, C, g, K, int(causal),
+                                             _ptr(t), len(t), _ptr(s), float(tie), int(flat), mode,
+                                             _ptr(out), threads)
+    if rc:
+        raise ValueError("oracle check_selection: bad arguments")
+    return out
+
+
+def check_last(q_new, key_cache, lengths, sel, K: int, tie: float = 1e-3, C: int = 64, g: int = 2,
+               threads: int = 0):
+    """``check_selection`` for decode: sequence b's newest query over its
+    lengths[b] keys.  q_new [B, Hq, d]; key_cache [B, n_cap, Hkv, d];
+    sel [B, Hkv, K].  Returns int32 [B, Hkv]."""
+    k = _f32(key_cache)
+    B, n_cap, Hkv, d = k.shape
+    qq = _f32(q_new)
+    Hq = qq.shape[1]
+    ln = np.ascontiguousarray(lengths, dtype=np.int64)
+    s = np.ascontiguousarray(sel, dtype=np.int32)
+    if s.shape != (B, Hkv, K):
+        raise ValueError("sel must be [B, Hkv, K]")
+    out = np.empty((B, Hkv), dtype=np.int32)
+    rc = _load().pisa_oracle_check_last(_ptr(qq), _ptr(k), B, n_cap, _ptr(ln), Hq, Hkv, d, C, g, K,
+                                        _ptr(s), float(tie), _ptr(out), threads)
+    if rc:
+        raise ValueError("oracle check_last: bad arguments")
+    return out

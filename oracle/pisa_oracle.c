@@ -706,3 +706,357 @@ double pisa_oracle_node_score(const float* q, const float* keys, int64_t N, int 
   free(pyr);
   return s;
 }
+
+/* ------------------------------------------------------------------------------
+ * Checking a selection that differs from the oracle's ([§3.2] walk, ["Scoring:
+ * LogSumExp"] scores).  Where two candidates' scores are closer than `tie`,
+ * either order is a correct answer, so more than one leaf set can be correct.
+ * A leaf set is accepted iff some walk that breaks such near ties either way
+ * produces it:
+ *   - at a level with at most K eligible candidates every candidate is kept;
+ *   - at a scored level the kept set S (|S| = K) is a near Top-K of the
+ *     candidates: every candidate left out scores less than min_{s in S}
+ *     score(s) + tie;
+ *   - at the leaf level the kept set is the given leaf set itself.
+ * At an intermediate level the kept set must contain the ancestors of the given
+ * leaves; the other survivors are not visible in the output, so every near-Top-K
+ * completion is tried (depth first; the number of completions is tiny unless
+ * many candidates sit within `tie` of each other, and a node budget bounds it).
+ * Verdict: 1 reachable, 0 not reachable (or malformed), -1 budget exhausted.
+ * ---------------------------------------------------------------------------- */
+
+typedef struct {
+  walk_ctx* w;
+  int K;
+  double tie;
+  int64_t budget;
+  int cap;               /* g*K + 8: room for one level's candidates           */
+  int64_t* anc;          /* [L+1][K]: ancestors of the given leaves per level */
+  int n_anc[ORACLE_MAX_LEVELS + 1];
+  int64_t* cand;         /* [L+1][cap] candidates per level                   */
+  double* cs;            /* [L+1][cap] their scores                           */
+  int64_t* rest;         /* [L+1][cap] candidates not among the ancestors     */
+  double* rest_s;        /* [L+1][cap]                                        */
+  int64_t* pick;         /* [L+1][cap] chosen completion                      */
+  int64_t* next;         /* [L+1][cap] kept set handed to the level below     */
+} check_ctx;
+
+static int check_level(check_ctx* c, int l, const int64_t* S, int nS);
+
+/* Depth-first search over the completions of level l: rest[] is sorted by score
+ * (descending); `need` more members are still to be chosen from rest[pos..].
+ * cur_min = lowest score kept so far (ancestors included), max_out = highest
+ * score left out so far.  A completion is legal iff max_out - cur_min < tie. */
+static int complete(check_ctx* c, int l, int pos, int nrest, int chosen, int need, double cur_min,
+                    double max_out) {
+  if (--c->budget < 0) return -1;
+  int64_t* rest = c->rest + (int64_t)l * c->cap;
+  double* rs = c->rest_s + (int64_t)l * c->cap;
+  int64_t* pick = c->pick + (int64_t)l * c->cap;
+  if (chosen == need) {
+    double mo = max_out;
+    if (pos < nrest && rs[pos] > mo) mo = rs[pos]; /* the rest are left out */
+    if (!(mo - cur_min < c->tie)) return 0;
+    /* kept set = ancestors + picks, ascending */
+    const int64_t* A = c->anc + (int64_t)l * c->K;
+    int nA = c->n_anc[l];
+    int64_t* nx = c->next + (int64_t)l * c->cap;
+    int n = 0;
+    for (int i = 0; i < nA; ++i) nx[n++] = A[i];
+    for (int i = 0; i < chosen; ++i) nx[n++] = pick[i];
+    for (int i = 1; i < n; ++i) { /* insertion sort by index */
+      int64_t v = nx[i];
+      int j = i - 1;
+      while (j >= 0 && nx[j] > v) {
+        nx[j + 1] = nx[j];
+        --j;
+      }
+      nx[j + 1] = v;
+    }
+    return check_level(c, l - 1, nx, n);
+  }
+  if (nrest - pos < need - chosen) return 0;
+  int undecided = 0;
+  /* keep rest[pos] */
+  double nmin = rs[pos] < cur_min ? rs[pos] : cur_min;
+  if (max_out - nmin < c->tie) {
+    pick[chosen] = rest[pos];
+    int r = complete(c, l, pos + 1, nrest, chosen + 1, need, nmin, max_out);
+    if (r == 1) return 1;
+    if (r < 0) undecided = 1;
+  }
+  /* leave rest[pos] out */
+  double nmax = rs[pos] > max_out ? rs[pos] : max_out;
+  if (nmax - cur_min < c->tie) {
+    int r = complete(c, l, pos + 1, nrest, chosen, need, cur_min, nmax);
+    if (r == 1) return 1;
+    if (r < 0) undecided = 1;
+  }
+  return undecided ? -1 : 0;
+}
+
+/* Level l's candidates are the eligible children of the kept set S of level l+1. */
+static int check_level(check_ctx* c, int l, const int64_t* S, int nS) {
+  walk_ctx* w = c->w;
+  const oracle_levels* lv = w->lv;
+  const int K = c->K;
+  int64_t* cand = c->cand + (int64_t)l * c->cap;
+  double* cs = c->cs + (int64_t)l * c->cap;
+  const int64_t* A = c->anc + (int64_t)l * K;
+  const int nA = c->n_anc[l];
+  int nc = 0;
+  for (int s = 0; s < nS; ++s)
+    for (int k = 0; k < w->g; ++k) {
+      int64_t ch = S[s] * w->g + k;
+      if (ch < lv->M[l] && eligible(w, l, ch)) cand[nc++] = ch;
+    }
+  /* the ancestors must be candidates (both lists ascending) */
+  int member[64 * 2 + 8];
+  int j = 0;
+  for (int i = 0; i < nc; ++i) member[i] = 0;
+  for (int a = 0; a < nA; ++a) {
+    while (j < nc && cand[j] < A[a]) ++j;
+    if (j == nc || cand[j] != A[a]) return 0;
+    member[j] = 1;
+  }
+  if (nc <= K) { /* kept whole, unscored */
+    if (l == 1) return nA == nc;
+    return check_level(c, l - 1, cand, nc);
+  }
+  if (nA > K) return 0;
+  for (int i = 0; i < nc; ++i) cs[i] = block_score(w, l, cand[i]);
+  double min_in = INFINITY;
+  for (int i = 0; i < nc; ++i)
+    if (member[i] && cs[i] < min_in) min_in = cs[i];
+  if (l == 1) { /* the kept set is the given leaf set */
+    if (nA != K) return 0;
+    for (int i = 0; i < nc; ++i)
+      if (!member[i] && !(cs[i] - min_in < c->tie)) return 0;
+    return 1;
+  }
+  /* the other survivors: near-Top-K completions of the ancestors */
+  int64_t* rest = c->rest + (int64_t)l * c->cap;
+  double* rs = c->rest_s + (int64_t)l * c->cap;
+  int nr = 0;
+  for (int i = 0; i < nc; ++i)
+    if (!member[i]) {
+      int p = nr++; /* insertion by (score desc, index asc) */
+      while (p > 0 && (rs[p - 1] < cs[i] || (rs[p - 1] == cs[i] && rest[p - 1] > cand[i]))) {
+        rs[p] = rs[p - 1];
+        rest[p] = rest[p - 1];
+        --p;
+      }
+      rs[p] = cs[i];
+      rest[p] = cand[i];
+    }
+  return complete(c, l, 0, nr, 0, K - nA, min_in, -INFINITY);
+}
+
+/* Well-formed row: ascending distinct leaves, then -1 padding. */
+static int row_well_formed(const int32_t* sel, int K, int64_t M1, int* n_sel) {
+  int n = 0;
+  while (n < K && sel[n] >= 0) ++n;
+  for (int i = n; i < K; ++i)
+    if (sel[i] != -1) return 0;
+  for (int i = 0; i < n; ++i) {
+    if (sel[i] >= M1) return 0;
+    if (i && sel[i] <= sel[i - 1]) return 0;
+  }
+  *n_sel = n;
+  return 1;
+}
+
+/* One query: the walk re-taken along the given leaves (flat = 0), or the flat
+ * selection's near-Top-K rule over every eligible leaf (flat = 1). */
+static int check_one(walk_ctx* w, int K, const int32_t* sel, double tie, int flat, int64_t budget,
+                     check_ctx* c) {
+  const oracle_levels* lv = w->lv;
+  int n_sel;
+  if (!row_well_formed(sel, K, lv->M[1], &n_sel)) return 0;
+  if (flat) {
+    int64_t nc = 0; /* eligible leaves are a prefix */
+    while (nc < lv->M[1] && eligible(w, 1, nc)) ++nc;
+    if (n_sel != (nc < K ? nc : K)) return 0;
+    for (int i = 0; i < n_sel; ++i)
+      if (sel[i] >= nc) return 0;
+    if (nc <= K) return 1;
+    double min_in = INFINITY;
+    for (int i = 0; i < n_sel; ++i) {
+      double s = block_score(w, 1, sel[i]);
+      if (s < min_in) min_in = s;
+    }
+    int j = 0;
+    for (int64_t leaf = 0; leaf < nc; ++leaf) {
+      if (j < n_sel && sel[j] == leaf) {
+        ++j;
+        continue;
+      }
+      if (!(block_score(w, 1, leaf) - min_in < tie)) return 0;
+    }
+    return 1;
+  }
+  if (n_sel == 0) return 0;
+  /* ancestors of the given leaves at every level (distinct, ascending) */
+  for (int l = 1; l <= lv->L; ++l) {
+    int64_t* A = c->anc + (int64_t)l * K;
+    int n = 0;
+    for (int i = 0; i < n_sel; ++i) {
+      int64_t a = sel[i] / (lv->width[l] / lv->width[1]);
+      if (n == 0 || A[n - 1] != a) A[n++] = a;
+    }
+    c->n_anc[l] = n;
+  }
+  if (lv->L == 1) return n_sel == 1 && sel[0] == 0; /* a single leaf is the root */
+  c->w = w;
+  c->K = K;
+  c->tie = tie;
+  c->budget = budget;
+  int64_t root = 0;
+  return check_level(c, lv->L - 1, &root, 1);
+}
+
+static int check_alloc(check_ctx* c, const oracle_levels* lv, int K, int g) {
+  memset(c, 0, sizeof(*c));
+  c->cap = g * K + 8;
+  size_t n = (size_t)(lv->L + 1) * c->cap;
+  c->anc = (int64_t*)malloc(sizeof(int64_t) * (size_t)(lv->L + 1) * K);
+  c->cand = (int64_t*)malloc(sizeof(int64_t) * n);
+  c->cs = (double*)malloc(sizeof(double) * n);
+  c->rest = (int64_t*)malloc(sizeof(int64_t) * n);
+  c->rest_s = (double*)malloc(sizeof(double) * n);
+  c->pick = (int64_t*)malloc(sizeof(int64_t) * n);
+  c->next = (int64_t*)malloc(sizeof(int64_t) * n);
+  return c->anc && c->cand && c->cs && c->rest && c->rest_s && c->pick && c->next ? 0 : -1;
+}
+
+static void check_free(check_ctx* c) {
+  free(c->anc);
+  free(c->cand);
+  free(c->cs);
+  free(c->rest);
+  free(c->rest_s);
+  free(c->pick);
+  free(c->next);
+}
+
+#define CHECK_BUDGET ((int64_t)1 << 22)
+
+/*
+ * Is each given prefill selection one that the walk (flat = 0) or the flat
+ * selector (flat = 1) reaches when near ties (score differences below `tie`)
+ * are broken either way?
+ *   q      : [B][n_t][Hq][d] rows of t_list; keys: [B][N][Hkv][d]
+ *   sel    : [B][Hkv][n_t][K] leaf sets to check (ascending, -1 padded)
+ *   verdict: [B][Hkv][n_t]  1 reachable, 0 not (or malformed), -1 undecided
+ */
+int pisa_oracle_check_selection(const float* q, const float* keys, int B, int64_t N, int Hq, int Hkv,
+                                int d, int C, int g, int K, int causal, const int64_t* t_list,
+                                int64_t n_t, const int32_t* sel, double tie, int flat, int mode,
+                                int32_t* verdict, int n_threads) {
+  oracle_levels lv;
+  if (B <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || K < 1 || K > 64 || g > 2 || !(tie > 0) ||
+      levels_init(&lv, N, C, g))
+    return -1;
+  for (int64_t i = 0; i < n_t; ++i)
+    if (t_list[i] < 0 || t_list[i] >= N) return -1;
+  const int G = Hq / Hkv;
+  double* pyr = NULL;
+  if (!flat) {
+    pyr = (double*)malloc(sizeof(double) * (size_t)B * Hkv * lv.total * d);
+    if (!pyr) return -1;
+    pisa_oracle_build_pyramid(keys, B, N, N, Hkv, d, C, g, 0, pyr);
+  }
+  const int64_t jobs = (int64_t)B * Hkv * n_t;
+  const int nt = resolve_threads(n_threads);
+  int err = 0;
+#pragma omp parallel num_threads(nt)
+  {
+    check_ctx c;
+    double* work = (double*)malloc(sizeof(double) * (C > g ? C : g));
+    if (check_alloc(&c, &lv, K, g) || !work) err = 1;
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t job = 0; job < jobs; ++job) {
+      if (err) continue;
+      int64_t it = job % n_t;
+      int kv = (int)((job / n_t) % Hkv);
+      int b = (int)(job / (n_t * Hkv));
+      walk_ctx w;
+      memset(&w, 0, sizeof(w));
+      w.q = q + ((int64_t)b * n_t + it) * Hq * d;
+      w.keys = keys;
+      w.pyr = pyr ? pyr + ((int64_t)b * Hkv + kv) * lv.total * d : NULL;
+      w.lv = &lv;
+      w.n_cap = N;
+      w.b = b;
+      w.kv = kv;
+      w.Hkv = Hkv;
+      w.G = G;
+      w.d = d;
+      w.g = g;
+      w.causal = causal;
+      w.t = t_list[it];
+      w.scale = 1.0 / sqrt((double)d);
+      w.work = work;
+      w.mode = mode;
+      int64_t o = ((int64_t)b * Hkv + kv) * n_t + it;
+      verdict[o] = check_one(&w, K, sel + o * K, tie, flat, CHECK_BUDGET, &c);
+    }
+    check_free(&c);
+    free(work);
+  }
+  free(pyr);
+  return err ? -1 : 0;
+}
+
+/*
+ * The same check for decode selections: sequence b's newest query (t =
+ * lengths[b] - 1) over its lengths[b] keys, pyramid over those keys only.
+ *   q: [B][Hq][d]; keys: [B][n_cap][Hkv][d]; sel: [B][Hkv][K]; verdict: [B][Hkv]
+ */
+int pisa_oracle_check_last(const float* q, const float* keys, int B, int64_t n_cap,
+                           const int64_t* lengths, int Hq, int Hkv, int d, int C, int g, int K,
+                           const int32_t* sel, double tie, int32_t* verdict, int n_threads) {
+  if (B <= 0 || Hkv <= 0 || Hq % Hkv || K < 1 || K > 64 || g > 2 || !(tie > 0)) return -1;
+  for (int b = 0; b < B; ++b)
+    if (lengths[b] < 1 || lengths[b] > n_cap) return -1;
+  const int G = Hq / Hkv;
+  const int nt = resolve_threads(n_threads);
+  int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+  for (int64_t job = 0; job < (int64_t)B * Hkv; ++job) {
+    int b = (int)(job / Hkv), kv = (int)(job % Hkv);
+    oracle_levels lv;
+    check_ctx c;
+    if (levels_init(&lv, lengths[b], C, g) || check_alloc(&c, &lv, K, g)) {
+      err = 1;
+      continue;
+    }
+    double* pyr = (double*)malloc(sizeof(double) * (size_t)lv.total * d);
+    double* work = (double*)malloc(sizeof(double) * (C > g ? C : g));
+    const float* kb = keys + (int64_t)b * n_cap * Hkv * d;
+    build_direct(kb, n_cap, Hkv, d, 0, kv, &lv, pyr);
+    walk_ctx w;
+    memset(&w, 0, sizeof(w));
+    w.q = q + (int64_t)b * Hq * d;
+    w.keys = kb;
+    w.pyr = pyr;
+    w.lv = &lv;
+    w.n_cap = n_cap;
+    w.b = 0;
+    w.kv = kv;
+    w.Hkv = Hkv;
+    w.G = G;
+    w.d = d;
+    w.g = g;
+    w.causal = 1;
+    w.t = lengths[b] - 1;
+    w.scale = 1.0 / sqrt((double)d);
+    w.work = work;
+    w.mode = 0;
+    verdict[job] = check_one(&w, K, sel + job * K, tie, 0, CHECK_BUDGET, &c);
+    check_free(&c);
+    free(pyr);
+    free(work);
+  }
+  return err ? -1 : 0;
+}

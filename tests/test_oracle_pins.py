@@ -518,3 +518,100 @@ def test_attention_with_constant_keys_averages_the_values():
     np.testing.assert_allclose(got[0, 0, 0], v[0, :101, 0].astype(np.float64).mean(0), rtol=1e-12, atol=1e-12)
     want = np.concatenate([v[0, 64:128, 0], v[0, 192:256, 0]]).astype(np.float64).mean(0)
     np.testing.assert_allclose(got[0, 1, 0], want, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- near-tie checker
+# A selection that differs from the oracle's is still correct when a walk that
+# breaks near ties (score differences below the tie threshold) the other way
+# reaches it.  The checker re-takes the walk along the given leaves; its expected
+# verdicts follow from the hand trees' closed-form scores.
+
+def _check_entries(kind):
+    g = _golden()
+    cases = {c["name"]: c for c in g["cases"]}
+    return [(cases[e["case"]], e) for e in g["check_cases"][kind]]
+
+
+@pytest.mark.parametrize("case,entry", _check_entries("walk"),
+                         ids=lambda x: x["name"][:2] if "name" in x else str(x["sel"]) + "@" + str(x["tie"]))
+def test_checker_on_hand_trees(case, entry):
+    q, keys = _hand_inputs(case)
+    t = case["t"]
+    K = case["K"]
+    sel = np.array(entry["sel"], np.int32).reshape(1, 1, 1, K)
+    v = oracle.check_selection(q[:, t:t + 1], keys, [t], sel, K=K, tie=entry["tie"], causal=case["causal"])
+    assert v[0, 0, 0] == entry["expect"], entry
+
+
+@pytest.mark.parametrize("case,entry", _check_entries("flat"),
+                         ids=lambda x: x["name"][:2] if "name" in x else str(x["sel"]) + "@" + str(x["tie"]))
+def test_flat_checker_on_hand_trees(case, entry):
+    q, keys = _hand_inputs(case)
+    t = case["t"]
+    K = case["K"]
+    sel = np.array(entry["sel"], np.int32).reshape(1, 1, 1, K)
+    v = oracle.check_selection(q[:, t:t + 1], keys, [t], sel, K=K, tie=entry["tie"], causal=case["causal"],
+                               flat=True)
+    assert v[0, 0, 0] == entry["expect"], entry
+
+
+def test_decode_checker_is_the_prefill_checker_of_the_last_query():
+    case = next(c for c in _golden()["cases"] if c["name"].startswith("H_"))
+    q, keys = _hand_inputs(case)
+    for sel, tie, want in (([0, 1], 1e-3, 1), ([0, 1], 1e-4, 0), ([0, 2], 1e-4, 1), ([0, 4], 1e-3, 0)):
+        s = np.array(sel, np.int32).reshape(1, 1, 2)
+        v = oracle.check_last(q[:, -1], keys, np.array([512]), s, K=2, tie=tie)
+        assert v[0, 0] == want, (sel, tie)
+
+
+def test_checker_accepts_the_oracles_own_selections_and_rejects_planted_swaps():
+    """Random inputs: every oracle selection is reachable; replacing one selected
+    leaf by an unselected eligible one is rejected unless it is within the tie of
+    the leaf it replaces at every level the swap touches (verified independently
+    by the flat rule when the walk reduces to flat selection: M_2 <= K)."""
+    rng = np.random.default_rng(31)
+    N, K = 3000, 4
+    q = _rand((1, N, 4, D), rng)
+    keys = _rand((1, N, 2, D), rng)
+    ts = np.arange(300, N, 37)
+    r = oracle.select(q[:, ts], keys, K=K, t_list=ts)
+    v = oracle.check_selection(q[:, ts], keys, ts, r["idx"], K=K)
+    assert (v == 1).all()
+    # plant: swap the lowest-scoring selected leaf for the first unselected eligible leaf
+    bad = r["idx"].copy()
+    planted = 0
+    for kv in range(2):
+        for it, t in enumerate(ts):
+            row = bad[0, kv, it]
+            n_el = t // 64 + 1
+            others = [x for x in range(n_el) if x not in row]
+            if not others:
+                continue
+            j = int(np.argmin(r["scores"][0, kv, it]))
+            row[j] = others[0]
+            row.sort()
+            planted += 1
+    v2 = oracle.check_selection(q[:, ts], keys, ts, bad, K=K)
+    # a swap is legal only where the oracle met a near tie
+    assert planted > 50
+    assert (v2[r["min_gap"] >= 1e-3] == 0).all()
+
+
+def test_flat_checker_agrees_with_brute_force_near_top_k():
+    rng = np.random.default_rng(32)
+    N, K = 1100, 3
+    q = _rand((1, N, 2, D), rng)
+    keys = _rand((1, N, 1, D), rng)
+    ts = np.array([200, 640, 1099])
+    for it, t in enumerate(ts):
+        n_el = t // 64 + 1
+        leaves = np.arange(n_el, dtype=np.int32).reshape(1, 1, 1, n_el)
+        s = oracle.leaf_scores(q[:, [t]], keys, [t], leaves)[0, 0, 0]
+        order = np.argsort(-s, kind="stable")
+        for trial in range(20):
+            pick = np.sort(rng.choice(n_el, K, replace=False)) if trial else np.sort(order[:K])
+            outside = np.setdiff1d(np.arange(n_el), pick)
+            want = int(s[outside].max() - s[pick].min() < 0.3)
+            sel = pick.astype(np.int32).reshape(1, 1, 1, K)
+            got = oracle.check_selection(q[:, [t]], keys, [t], sel, K=K, tie=0.3, flat=True)[0, 0, 0]
+            assert got == want, (t, pick, s[pick], s[outside].max())
