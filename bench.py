@@ -188,7 +188,7 @@ def dist_setup():
     return world, rank, local
 
 
-def oracle_rows_per_s(q, k, w, target_s: float, n_rows: int | None = None):
+def oracle_rows_per_s(q, k, w, target_s: float, n_rows: int | None = None, threads: int = 0):
     """Time the fp64 oracle (as it stands, all host threads) on a bounded sample:
     its pyramid build over all N tokens, plus the walks of n query rows (all KV
     heads) spread evenly over the sequence.  A full pass is then
@@ -205,7 +205,7 @@ def oracle_rows_per_s(q, k, w, target_s: float, n_rows: int | None = None):
         t = np.unique(np.linspace(0, N - 1, n).round().astype(np.int64))
         qr = q[:, t].float().numpy()
         t0 = time.perf_counter()
-        oracle.select(qr, kf, K=w["K"], t_list=t)
+        oracle.select(qr, kf, K=w["K"], t_list=t, threads=threads)
         return len(t), max(time.perf_counter() - t0 - t_build, 1e-9)
 
     # grow the sample until it takes about target_s (per-row cost from a small
@@ -219,11 +219,14 @@ def oracle_rows_per_s(q, k, w, target_s: float, n_rows: int | None = None):
             n, secs = run(int(min(N, n * min(8.0, max(1.5, budget / secs)))))
     t_row = secs / (n * w["B"])
     t_full = t_build + w["B"] * N * t_row
-    return dict(value=w["B"] * N / t_full, unit=UNIT, cores=oracle.max_threads(), kind="oracle",
-                seconds=secs + t_build, rows=n * w["B"],
+    return dict(value=w["B"] * N / t_full, unit=UNIT, cores=threads or oracle.max_threads(), kind="oracle",
+                extrapolated=n < N, rows_timed=n * w["B"], seconds_timed=round(secs + t_build, 3),
+                full_pass_s_extrapolated=round(t_full, 2), rows=n * w["B"],
                 sample=f"fp64 pyramid build over all N={N} tokens ({t_build:.2f} s) + walks of {n} query "
                        f"rows x {w['Hkv']} KV heads evenly spaced over the sequence ({secs:.2f} s); "
-                       f"full pass extrapolated as build + B*N rows")
+                       f"value = B*N / (build + B*N x measured seconds per row)"
+                       + (f": an extrapolation to a full pass ({t_full:.1f} s), not a timed full pass"
+                          if n < N else " (every row walked)"))
 
 
 def run_reference(args):
@@ -233,6 +236,7 @@ def run_reference(args):
     from pyramid_top_block_gb300 import synth
     q, k, w = synth.make(args.workload)
     vals = []
+    secs = []
     info = None
     per_step = max(0.5, min(args.ref_step_s, 150.0 / (args.warmup + args.steps)))
     n_rows = None
@@ -241,14 +245,20 @@ def run_reference(args):
         n_rows = r["rows"] // w["B"]  # the first step sizes the sample, the others reuse it
         if i >= args.warmup:
             vals.append(r["value"])
+            secs.append(r["seconds_timed"])
             info = r
     value = statistics.mean(vals)
+    # a step is one bounded sample (pyramid build + a fixed set of query rows); ms_per_step is
+    # its measured wall time, and value extrapolates the sample's per-row cost to a full pass
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * w["B"] * w["N"] / value,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * statistics.mean(secs),
+            "extrapolated": True, "rows_timed_per_step": info["rows_timed"],
+            "full_pass_ms_extrapolated": 1000.0 * w["B"] * w["N"] / value,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": cfg(w, args),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": info["cores"], "kind": "oracle",
-                             "sample": info["sample"]},
+                             "extrapolated": True, "rows_timed": info["rows_timed"],
+                             "seconds_timed": info["seconds_timed"], "sample": info["sample"]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -453,6 +463,13 @@ def run_ours(args):
                      "note": "stage two over the pass's idx, random bf16 V, fp32 output"}
         del vd, att_out
 
+    per_config = None
+    if args.configs and rank == 0:
+        per_config = {}
+        for name in args.configs.split(","):
+            per_config[name] = bench_config(torch, pisa, synth, dev, name, pk, runs=20,
+                                            cpu_s=0.0 if args.no_cpu_baseline else args.cfg_cpu_s)
+
     flat = None
     if args.flat and rank == 0:
         flat = [bench_flat(torch, pisa, synth, dev, name) for name in args.flat.split(",")]
@@ -471,11 +488,56 @@ def run_ours(args):
                 "rates": rates, "work": work,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
                 "device_status": device_status,
-                "decode": decode, "flat": flat, "score_modes": modes, "attention": attention}
+                "per_config": per_config, "decode": decode, "flat": flat, "score_modes": modes,
+                "attention": attention}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
     return 0
+
+
+def bench_config(torch, pisa, synth, dev, name, pk, runs, cpu_s):
+    """One more workload of the metric's range: median / min ms of a full pass
+    (pyramid build + selection, L2 flushed between passes), query-rows/s, the pass
+    against its roofline, and the oracle on the host cores (all of them; also one
+    thread up to 32K tokens) on a bounded sample of the same workload."""
+    q, k, w = synth.make(name)
+    B, N, Hq, Hkv, K = w["B"], w["N"], w["Hq"], w["Hkv"], w["K"]
+    qd, kd = q.to(dev), k.to(dev)
+    pyr = pisa.Pyramid.allocate(kd)
+    ws = torch.empty(pisa.select_workspace_bytes(B, N, Hq, Hkv, K), dtype=torch.uint8, device=dev)
+    idx = torch.empty(B, Hkv, N, K, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    ms = []
+    for i in range(runs + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        pisa.build_pyramid(pyr)
+        pisa.select_prefill(qd, pyr, K, workspace=ws, out=(idx, None), with_scores=False)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            ms.append(a.elapsed_time(b))
+    st = pisa.check_device_status(ws)
+    alg = algorithmic(w)
+    t_tensor = alg["flops"] / (pk["bf16_tflops"] * 1e12) * 1e3
+    t_hbm = alg["bytes"] / (pk["hbm_gbs"] * 1e9) * 1e3
+    med = statistics.median(ms)
+    out = {"B": B, "N": N, "Hq": Hq, "Hkv": Hkv, "K": K, "ms_median": med, "ms_min": min(ms), "runs": runs,
+           "query_rows_per_s": B * N / (med / 1e3), "status": st,
+           "roofline_pass": {"t_tensor_ms": t_tensor, "t_hbm_ms": t_hbm, "t_roofline_ms": max(t_tensor, t_hbm),
+                             "frac": max(t_tensor, t_hbm) / med}}
+    del qd, kd, pyr, ws, idx, flush
+    if cpu_s > 0:
+        o = oracle_rows_per_s(q, k, w, target_s=cpu_s)
+        out["oracle"] = {x: o[x] for x in ("value", "cores", "extrapolated", "rows_timed", "seconds_timed")}
+        if N <= 32768:
+            o1 = oracle_rows_per_s(q, k, w, target_s=cpu_s, threads=1)
+            out["oracle_1thread"] = {x: o1[x] for x in ("value", "cores", "extrapolated", "rows_timed",
+                                                        "seconds_timed")}
+    return out
 
 
 def bench_flat(torch, pisa, synth, dev, name, runs=5):
@@ -587,8 +649,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--attention", type=int, default=1, help="also time stage-two attention on the selection")
     ap.add_argument("--modes", type=int, default=1, help="also time the PISA-1 / PISA-2 score modes")
-    ap.add_argument("--flat", default="latency-32k",
+    ap.add_argument("--flat", default="latency-4k,latency-8k,latency-16k,latency-32k,latency-64k,latency-128k,"
+                                      "latency-256k",
                     help="comma-separated workloads for the flat-selector comparison ('' to skip)")
+    ap.add_argument("--configs", default="tiny-2k,latency-32k,latency-64k,latency-128k,ragged-16421",
+                    help="comma-separated workloads also timed (per_config; '' to skip)")
+    ap.add_argument("--cfg-cpu-s", type=float, default=3.0, help="seconds of oracle work per per_config entry")
     ap.add_argument("--cpu-s", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=6.0, help="seconds of oracle work per reference step")
     ap.add_argument("--decode-steps", type=int, default=256)

@@ -269,6 +269,21 @@ int pisa_select_prefill_noalloc(const void* Q, int Hq, const pisa_pyramid* pyr, 
                                 int causal, int32_t* idx, float* scores, void* stream);
 
 /*
+ * pisa_noalloc_prepare -- set-up for pisa_select_prefill_noalloc on the current
+ * device: looks up (and caches) the scratch array's device address, loading this
+ * library's device code on the device if it is not loaded yet.  Writes the address
+ * to *scratch when scratch is not NULL (for diagnostics).  Returns PISA_OK or
+ * PISA_ERR_CUDA.
+ *
+ * pisa_noalloc_device_status -- synchronises `stream` and returns the status word
+ * that the kernels of the last pisa_select_prefill_noalloc call on the current
+ * device left in the scratch array (PISA_OK if none), like
+ * pisa_check_device_status does for a caller's workspace.
+ */
+int pisa_noalloc_prepare(void** scratch);
+int pisa_noalloc_device_status(void* stream);
+
+/*
  * pisa_selftest_bounded_wait -- the failure path of the kernels' bounded barrier
  * waits, exercised on the GPU without faulting it: one thread waits on an mbarrier
  * that nothing arrives on, through the same wait routine the tcgen05 kernels use,

@@ -23,6 +23,7 @@ from . import build as _build
 __all__ = [
     "PisaError", "Pyramid", "load", "num_levels", "pyramid_nodes", "level_offset",
     "build_pyramid", "select_workspace_bytes", "select_prefill", "select_prefill_noalloc",
+    "noalloc_prepare", "noalloc_device_status",
     "decode_workspace_bytes",
     "decode_append_and_select", "check_device_status", "status_string", "kernel_launches",
     "prefill_phases", "set_phase_events", "D", "C", "G_MERGE",
@@ -94,6 +95,10 @@ def load(path: str | None = None):
     lib.pisa_prefill_phase_name.restype = ctypes.c_char_p
     lib.pisa_select_prefill_noalloc.argtypes = [vp, i32, vp, i64, i32, i32, vp, vp, vp]
     lib.pisa_select_prefill_noalloc.restype = i32
+    lib.pisa_noalloc_prepare.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+    lib.pisa_noalloc_prepare.restype = i32
+    lib.pisa_noalloc_device_status.argtypes = [vp]
+    lib.pisa_noalloc_device_status.restype = i32
     lib.pisa_event_elapsed_ms.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_float)]
     lib.pisa_event_elapsed_ms.restype = i32
     _lib = lib
@@ -355,6 +360,21 @@ def select_prefill_noalloc(Q: torch.Tensor, pyr: Pyramid, K: int, causal: bool =
                                               _ptr(scores), _stream(stream)),
            "pisa_select_prefill_noalloc")
     return idx, scores
+
+
+def noalloc_prepare() -> int:
+    """Set-up for select_prefill_noalloc on the current device (loads the library's
+    device code there, which is when its scratch array comes into being); returns
+    the scratch's device address."""
+    p = ctypes.c_void_p()
+    _check(load().pisa_noalloc_prepare(ctypes.byref(p)), "pisa_noalloc_prepare")
+    return int(p.value or 0)
+
+
+def noalloc_device_status(stream=None) -> int:
+    """Synchronise the stream and return the status word of the last
+    select_prefill_noalloc call on the current device (0 = ok)."""
+    return int(load().pisa_noalloc_device_status(_stream(stream)))
 
 
 def decode_workspace_bytes(B: int, Hq: int, Hkv: int, K: int) -> int:

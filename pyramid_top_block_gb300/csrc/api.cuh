@@ -75,6 +75,9 @@ struct WalkLaunch {
 };
 
 long long route_rows_per_bh(const Levels& lv);
+// Every argument check of a prefill selection except the workspace's (the status
+// pisa_select_prefill would return for these arguments with a large enough workspace).
+int prefill_check_args(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int mode, const void* idx);
 cudaError_t launch_selftest_wait(int* status, long long delay_cycles, cudaStream_t s);
 cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s);
 

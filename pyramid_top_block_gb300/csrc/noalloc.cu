@@ -15,6 +15,11 @@
 // read.  Calls that overlap on the GPU (on different streams, or from several
 // host threads without ordering) race on the array and give wrong results:
 // order them on one stream.
+//
+// With CUDA's lazy module loading (the default) the array comes into being
+// when this file's device code is first loaded on a device, which the first
+// address lookup triggers: that moment may allocate device memory and
+// synchronise.  pisa_noalloc_prepare() does the lookup up front.
 #include <mutex>
 
 #include "api.cuh"
@@ -47,13 +52,28 @@ int scratch_address(void** out) {
 
 extern "C" int pisa_select_prefill_noalloc(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K,
                                            int causal, int32_t* idx, float* scores, void* stream) {
-  if (!pyr) return PISA_ERR_INVALID_ARG;
+  // the same checks, in the same order, as pisa_select_prefill; then the size limit
+  const int chk = pisa::prefill_check_args(Q, Hq, pyr, N, K, 0, idx);
+  if (chk != PISA_OK) return chk;
   const size_t need = pisa_select_workspace_bytes(pyr->B, N, Hq, pyr->Hkv, K);
-  if (need == 0) return pisa_select_prefill(Q, Hq, pyr, N, K, causal, idx, scores, nullptr, 0, stream);
   if (need > (size_t)PISA_NOALLOC_SCRATCH_BYTES) return PISA_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
   const int st = scratch_address(&ws);
   if (st != PISA_OK) return st;
   return pisa_select_prefill(Q, Hq, pyr, N, K, causal, idx, scores, ws, (size_t)PISA_NOALLOC_SCRATCH_BYTES,
                              stream);
+}
+
+extern "C" int pisa_noalloc_prepare(void** scratch) {
+  void* ws = nullptr;
+  const int st = scratch_address(&ws);
+  if (st == PISA_OK && scratch) *scratch = ws;
+  return st;
+}
+
+extern "C" int pisa_noalloc_device_status(void* stream) {
+  void* ws = nullptr;
+  const int st = scratch_address(&ws);
+  if (st != PISA_OK) return st;
+  return pisa_check_device_status(ws, stream);
 }

@@ -225,20 +225,33 @@ struct PrefillPlan {
   LeafTcLaunch L;
 };
 
-static int prefill_check(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int mode, const void* idx,
-                         const void* ws, size_t ws_bytes) {
+}  // extern "C"
+
+namespace pisa {
+// Every argument check of a prefill selection except the workspace's.
+int prefill_check_args(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int mode, const void* idx) {
   if (mode < 0 || mode > 2) return PISA_ERR_UNSUPPORTED;
   int st = check_pyr(pyr);
   if (st) return st;
-  if (!Q || !idx || !ws) return PISA_ERR_INVALID_ARG;
+  if (!Q || !idx) return PISA_ERR_INVALID_ARG;
   st = check_geometry(pyr->B, N, Hq, pyr->Hkv, pyr->d, pyr->C, pyr->g, K);
   if (st) return st;
   if (N > pyr->n_cap) return PISA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(Q) & 15) || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)))
-    return PISA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(Q) & 15) return PISA_ERR_INVALID_ARG;
   const PrefillWs w = prefill_layout(pyr->B, N, pyr->Hkv, K);
   if (w.nb >= (1LL << 31) || (long long)pyr->B * pyr->n_cap >= (1LL << 31)) return PISA_ERR_UNSUPPORTED;
-  if (ws_bytes < w.total) return PISA_ERR_WORKSPACE_TOO_SMALL;
+  return PISA_OK;
+}
+}  // namespace pisa
+
+extern "C" {
+
+static int prefill_check(const void* Q, int Hq, const pisa_pyramid* pyr, int64_t N, int K, int mode, const void* idx,
+                         const void* ws, size_t ws_bytes) {
+  const int st = prefill_check_args(Q, Hq, pyr, N, K, mode, idx);
+  if (st) return st;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return PISA_ERR_INVALID_ARG;
+  if (ws_bytes < prefill_layout(pyr->B, N, pyr->Hkv, K).total) return PISA_ERR_WORKSPACE_TOO_SMALL;
   return PISA_OK;
 }
 

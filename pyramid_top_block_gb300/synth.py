@@ -78,6 +78,9 @@ def decode_step(g: torch.Generator, B: int, Hq: int, Hkv: int, d: int = 64):
 # Named workloads (sizes of the selection-latency benchmark and its variants).
 WORKLOADS = {
     "tiny-2k": dict(B=1, N=2048, Hq=4, Hkv=1, K=8, kind="iid", seed=0),
+    "latency-4k": dict(B=1, N=4096, Hq=32, Hkv=2, K=8, kind="iid", seed=0),
+    "latency-8k": dict(B=1, N=8192, Hq=32, Hkv=2, K=8, kind="iid", seed=0),
+    "latency-16k": dict(B=1, N=16384, Hq=32, Hkv=2, K=8, kind="iid", seed=0),
     "latency-32k": dict(B=1, N=32768, Hq=32, Hkv=2, K=8, kind="iid", seed=0),
     "latency-64k": dict(B=1, N=65536, Hq=32, Hkv=2, K=8, kind="iid", seed=0),
     "latency-128k": dict(B=1, N=131072, Hq=32, Hkv=2, K=8, kind="iid", seed=0),

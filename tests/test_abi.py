@@ -124,3 +124,28 @@ def test_status_strings():
     for s in range(7):
         assert pisa.status_string(s)
     assert pisa.status_string(99) == "unknown status"
+
+
+def test_noalloc_argument_checks_match_the_workspace_entry_point():
+    """The allocation-free entry point returns the codes pisa_select_prefill returns
+    for the same arguments (same checks, same order) before its own size limit;
+    nothing here reaches a CUDA call."""
+    lib = pisa.load()
+    vp = ctypes.c_void_p
+    st = pisa._PyrStruct(0x1000, 0x2000, None, 1, 2, 64, 64, 2, 128)
+    big = pisa._PyrStruct(0x1000, 0x2000, None, 1, 2, 64, 64, 2, 1 << 22)
+
+    def both(pyr, Hq, N, K, idx=vp(0x5000), Q=vp(0x3000)):
+        a = lib.pisa_select_prefill(Q, Hq, ctypes.byref(pyr), N, K, 1, idx, None, vp(0x4000), 1 << 40, None)
+        b = lib.pisa_select_prefill_noalloc(Q, Hq, ctypes.byref(pyr), N, K, 1, idx, None, None)
+        return a, b
+
+    assert both(st, 32, 128, 33) == (2, 2)                 # K above 32: unsupported
+    assert both(st, 24, 128, 8) == (2, 2)                  # group of 12
+    assert both(st, 32, 129, 8) == (1, 1)                  # N > n_cap
+    assert both(st, 32, 128, 8, idx=None) == (1, 1)        # no output
+    assert both(st, 32, 128, 8, Q=vp(0x3008)) == (1, 1)    # Q not 16-byte aligned
+    assert lib.pisa_select_prefill_noalloc(vp(0x3000), 32, None, 128, 8, 1, vp(0x5000), None, None) == 1
+    # valid arguments beyond the scratch: only the no-allocation entry point refuses
+    assert lib.pisa_select_prefill_noalloc(vp(0x3000), 32, ctypes.byref(big), 1 << 22, 8, 1, vp(0x5000), None,
+                                           None) == 3

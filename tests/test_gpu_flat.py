@@ -7,7 +7,7 @@ import torch
 import pyramid_top_block_gb300 as pisa
 from pyramid_top_block_gb300 import synth
 
-from parity import compare_flat
+from parity import compare_flat, record
 
 pytestmark = pytest.mark.gpu
 
@@ -38,7 +38,7 @@ def test_flat_tiny_all_queries():
     q, k, w = synth.make("tiny-2k")
     idx, sc = _run_flat(q, k, w["K"])
     st = compare_flat(idx, sc, _f32(q), _f32(k), np.arange(w["N"]), w["K"])
-    print("flat tiny", {a: b for a, b in st.items() if a != "messages"})
+    record("flat tiny-2k", st)
     _ok(st)
 
 
@@ -58,7 +58,7 @@ def test_flat_latency_32k_sampled():
     rng = np.random.default_rng(7)
     t = np.unique(np.concatenate([rng.choice(N - 256, 1024, replace=False), np.arange(N - 256, N)]))
     st = compare_flat(idx[:, :, t], sc[:, :, t], _f32(q[:, t]), _f32(k), t, w["K"])
-    print("flat 32k", {a: b for a, b in st.items() if a != "messages"})
+    record("flat latency-32k (sampled)", st)
     _ok(st)
 
 

@@ -8,7 +8,7 @@ import torch
 import pyramid_top_block_gb300 as pisa
 from pyramid_top_block_gb300 import synth
 
-from parity import compare_flat, compare_prefill
+from parity import compare_flat, compare_prefill, record
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +49,7 @@ def test_prefill_modes_ragged_structured(mode):
     idx, sc = _prefill(q, k, w["K"], mode)
     t = np.arange(0, w["N"], 3)
     st = compare_prefill(idx[:, :, t], sc[:, :, t], _f32(q[:, t]), _f32(k), t, w["K"], mode=mode)
-    print("ragged mode", mode, {a: b for a, b in st.items() if a != "messages"})
+    record(f"ragged-16421 mode {mode}", st)
     _ok(st)
 
 

@@ -8,7 +8,7 @@ import oracle
 import pyramid_top_block_gb300 as pisa
 from pyramid_top_block_gb300 import synth
 
-from parity import compare_decode
+from parity import compare_decode, pyramid_tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -24,19 +24,23 @@ def _ragged_cache(n_cap=4200, Hkv=2, seed=8):
     return cache, g
 
 
-def _valid_nodes_equal(got, cache, lengths, rtol, exact=False):
+def _valid_nodes_equal(got, cache, lengths):
     """Every node of sequence b's own levels matches the oracle's mean pyramid over
-    lengths[b] tokens (GPU layout offsets come from n_cap, the oracle's from n)."""
+    lengths[b] tokens within the fp32 summation bound (GPU layout offsets come from
+    n_cap, the oracle's from n)."""
     n_cap = cache.shape[1]
     for b, n in enumerate(lengths):
         if n == 0:
             continue
-        want = oracle.build_pyramid(cache[b:b + 1].float().numpy(), n=n)[0]
+        kb = cache[b:b + 1].float().numpy()
+        want = oracle.build_pyramid(kb, n=n)[0]
+        tol = pyramid_tolerance(kb, n=n)[0]
         off_o = 0
         for lvl, m in enumerate(oracle.level_sizes(n), start=1):
             off_g = pisa.level_offset(n_cap, lvl)
             g = got[b, :, off_g:off_g + m].double().cpu().numpy()
-            np.testing.assert_allclose(g, want[:, off_o:off_o + m], rtol=rtol, atol=1e-6)
+            err = np.abs(g - want[:, off_o:off_o + m])
+            assert (err <= tol[:, off_o:off_o + m]).all(), (b, lvl)
             off_o += m
 
 
@@ -46,7 +50,7 @@ def test_ragged_build_matches_oracle_per_sequence():
     pyr.lengths.copy_(torch.tensor(LENGTHS, dtype=torch.int32))
     pisa.build_pyramid_ragged(pyr)
     torch.cuda.synchronize()
-    _valid_nodes_equal(pyr.summaries, cache, LENGTHS, rtol=1e-5)
+    _valid_nodes_equal(pyr.summaries, cache, LENGTHS)
 
 
 def test_ragged_build_with_equal_lengths_is_the_uniform_build():

@@ -70,3 +70,22 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     rc = lib.pisa_select_prefill_noalloc(ctypes.c_void_p(kd.data_ptr()), 32, ctypes.byref(st), N, 8, 1,
                                          ctypes.c_void_p(kd.data_ptr()), None, None)
     assert rc == 3
+
+
+def test_noalloc_status_word_reads_a_device_side_timeout():
+    """A kernel-side error of this entry point lands in its built-in scratch, where
+    the caller has no workspace to read it from: pisa_noalloc_device_status reads
+    it.  The timeout is planted by the bounded-wait self-test, run on the scratch
+    itself (nothing faults); the next selection clears it."""
+    lib = pisa.load()
+    addr = pisa.noalloc_prepare()
+    assert addr != 0 and addr % 256 == 0
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.pisa_selftest_bounded_wait(ctypes.c_void_p(addr), 256, 0, stream) == 0
+    assert pisa.noalloc_device_status() == 5  # PISA_ERR_DEVICE_TIMEOUT
+    qd, pyr = _problem(43, 3000, 32, 2)
+    idx, _ = pisa.select_prefill_noalloc(qd, pyr, 8, with_scores=False)
+    assert pisa.noalloc_device_status() == 0
+    ref, _ = pisa.select_prefill(qd, pyr, 8, with_scores=False)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, ref)
