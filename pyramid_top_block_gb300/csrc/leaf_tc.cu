@@ -34,23 +34,19 @@
 
 namespace pisa {
 
-constexpr int kAccBufs = 4;       // TMEM accumulators of 128 fp32 columns
-// Query-row stages (16 KB each), one per accumulator: the stage of tile k is free again
-// once tile k's MMAs have completed, which acc_full already signals.
+constexpr int kAccBufs = 4;       // TMEM accumulators of 128 fp32 columns (two pairs of tiles)
+// Query-row stages (16 KB each), one per accumulator: the stages of a pair of tiles are
+// free again once the pair's MMAs have completed, which acc_pair already signals.
 constexpr int kLeafStages = kAccBufs;
-static_assert((kAccBufs & (kAccBufs - 1)) == 0, "stage and accumulator indices are taken with a mask");
-constexpr int kLeafWarps = 16;    // key-block loader, MMA, 2 query-row warps, 3 epilogue warpgroups
-constexpr int kEpiGroups = 3;     // epilogue warpgroups (warps 4..15)
-// A warpgroup waits for tile k only after finishing tile k - kEpiGroups, so with
-// kEpiGroups <= kAccBufs the accumulator barrier it waits on is never more than
-// one phase behind (the MMA warp commits tiles in order).
-static_assert(kEpiGroups <= kAccBufs, "an epilogue warpgroup could run two accumulator phases ahead");
-constexpr int kTileBlock = 32;    // consecutive tiles handled by one CTA in a row
-// Query-row warp w loads tiles k = w (mod 2) and, before refilling the stage of tile
-// k, waits on acc_full for tile k - kLeafStages; with an even stage count that tile
-// was its own, loaded after the previous phase completed, so the wait is never two
-// phases ahead.
-static_assert(kLeafStages % 2 == 0, "query-row warps alternate tiles");
+static_assert(kAccBufs == 4, "two pair stages of two tiles each: indices are taken with masks");
+constexpr int kLeafWarps = 20;    // key-block loader, MMA, 2 query-row warps, 4 epilogue warpgroups
+constexpr int kEpiGroups = 4;     // epilogue warpgroups (warps 4..19)
+// Warpgroup w takes tiles w, w + 4, ...: before waiting for tile k (pair k / 2) it has
+// seen tile k - 4 (pair k / 2 - 2, the same pair stage) complete, so the barrier it waits
+// on is exactly one phase ahead of what it saw, and it cannot run further ahead either:
+// the next phase of that stage needs this tile's own release.
+static_assert(kEpiGroups == kAccBufs, "the phase argument above takes one tile per accumulator and warpgroup");
+constexpr int kTileBlock = 32;    // consecutive tiles handled by one CTA in a row (even: pairs never straddle)
 constexpr int kTileBytes = 128 * 128;  // 128 rows of 64 bf16
 constexpr int kKeyBufs = 4;       // key blocks in flight (the loader runs up to 3 blocks ahead)
 constexpr size_t kLeafSmem = (size_t)(kLeafStages + kKeyBufs) * kTileBytes + 1024;
@@ -160,6 +156,29 @@ struct HalfLse {
       s = t;
     }
   }
+  // One 64-key half from two 32-column chunks (cnt0 + cnt1 keys, cnt0 >= 1); `full`
+  // (warp-uniform) means every lane has 64: one overflow vote for the half.
+  __device__ __forceinline__ void first2(const float (&x)[32], const float (&y)[32], int cnt0, int cnt1, bool full) {
+    ref = x[0];
+    const float nb = -ref * kL2e8;
+    const float t = chunk_exp_sum(x, cnt0, full, nb) + chunk_exp_sum(y, cnt1, full, nb);
+    if (__any_sync(kFull, !(t <= 3.0e38f))) {  // rare: rescale against the half's maximum
+      if (!(t <= 3.0e38f)) {
+        float m = ref;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (c < cnt0) m = fmaxf(m, x[c]);
+          if (c < cnt1) m = fmaxf(m, y[c]);
+        }
+        s = chunk_exp_sum(x, cnt0, false, -m * kL2e8) + chunk_exp_sum(y, cnt1, false, -m * kL2e8);
+        ref = m;
+      } else {
+        s = t;
+      }
+    } else {
+      s = t;
+    }
+  }
   __device__ __forceinline__ float value() const {  // natural-log units
     return ref * 0.125f + lg2_approx(s) * 0.69314718055994531f;
   }
@@ -204,6 +223,10 @@ struct HalfMom {
       n += cnt;
     }
   }
+  __device__ __forceinline__ void first2(const float (&x)[32], const float (&y)[32], int cnt0, int cnt1, bool full) {
+    first(x, cnt0, full);
+    add(y, cnt1, full);
+  }
   __device__ __forceinline__ float value() const {  // natural-log units
     const float inv = 1.f / (float)n, m = s1 * inv;
     float v = (ref + m) * 0.125f;
@@ -222,6 +245,13 @@ __device__ __forceinline__ void reg_fence32(float (&x)[32]) {
 }
 
 // MODE: 0 LSE over each leaf's keys, 1 their mean logit, 2 mean + variance / 2.
+//
+// Tiles are processed in pairs (k, k + 1), k even, CTA-local.  Pair P uses query-row
+// stages and TMEM accumulators 2 (P & 1) and 2 (P & 1) + 1: one barrier a_pair[P & 1]
+// completes when both tiles' query rows have landed, one commit after the pair's eight
+// MMAs completes acc_pair[P & 1] (one commit per two tiles: the issuing thread's chain of
+// waits, MMAs and commits is what bounds this kernel), and the two epilogue warpgroups
+// of the pair release acc_free[P & 1] (256 arrivals).
 template <int MODE>
 __global__ void __launch_bounds__(kLeafWarps * 32, 1)
     leaf_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -230,24 +260,22 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   unsigned char* sA = sm;
   unsigned char* sB = sm + kLeafStages * kTileBytes;
-  __shared__ uint64_t a_full[kLeafStages], b_full[kKeyBufs], b_empty[kKeyBufs];
-  __shared__ uint64_t acc_full[kAccBufs], acc_empty[kAccBufs], mma_done;
+  __shared__ uint64_t a_pair[2], b_full[kKeyBufs], b_empty[kKeyBufs];
+  __shared__ uint64_t acc_pair[2], acc_free[2], mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   volatile int* abort = &abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kLeafStages; ++s) {
-      mbar_init(&a_full[s], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&a_pair[s], 1);
+      mbar_init(&acc_pair[s], 1);
+      mbar_init(&acc_free[s], 2 * 128);
     }
     for (int s = 0; s < kKeyBufs; ++s) {
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
-    }
-    for (int s = 0; s < kAccBufs; ++s) {
-      mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 128);
     }
     mbar_init(&mma_done, 1);
     abort_flag = 0;
@@ -257,21 +285,25 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const int Gp = P.Gp, G = P.G;
+  const int Gp = P.Gp, G = P.G, R = P.R;
   const int first = __ldg(P.tile_off + P.b0);
   const int total = __ldg(P.tile_off + P.b1) - first;
   const int4* __restrict__ tdesc = P.tile_desc + first;
   int my_tiles = 0;
   for (int blk = blockIdx.x; blk * kTileBlock < total; blk += gridDim.x) my_tiles += min(kTileBlock, total - blk * kTileBlock);
+  const int my_pairs = (my_tiles + 1) >> 1;
+  bool mma_ok = true;  // the MMA thread's final wait completed (TMEM may be freed)
 
   if (warp <= 1) {
     // ---------------- warp 0 loads the key block (two sibling leaves, 128 keys) of every
-    // run of tiles with the same (b, kv, p) into a ring of kKeyBufs buffers; warp 1 drives the tensor
-    // core.  Both read this CTA's tile descriptors 32 at a time and find the key-block
+    // run of tiles with the same (b, kv, p) into a ring of kKeyBufs buffers; warp 1 drives the
+    // tensor core, a pair of tiles at a time.  Both read this CTA's tile descriptors 32 at a
+    // time (kTileBlock is even, so a pair never straddles two blocks) and find the key-block
     // changes with a ballot.
     const bool mma = warp == 1;
     const uint32_t idesc = umma_idesc_bf16(128, 128);
     int nchg = 0, cur = 0, prev_p = -1, prev_bh = -1, k = 0;
+    int nissued = 0;  // key blocks whose copy lane 0 of warp 0 started
     bool ok = true;
     for (int blk = blockIdx.x; ok && blk * kTileBlock < total; blk += gridDim.x) {
       const int i0 = blk * kTileBlock;
@@ -298,45 +330,46 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
               mbar_expect_tx(&b_full[bb], kTileBytes);
               tma_load_3d(sB + bb * kTileBytes, &kmap, 0, bh % P.Hkv, (int)((bh / P.Hkv) * P.n_cap + 128LL * pk),
                           &b_full[bb]);
+              ++nissued;
             }
           }
           ok = __shfl_sync(kFull, w, 0);
           ++nchg;
         }
       } else {
-        // the whole warp walks the block's tiles and waits on the barriers (so that it stays
-        // converged); lane 0 alone issues the MMAs and their commits, which tcgen05.commit
-        // tracks per issuing thread.  Stage, accumulator and parity come from shifts,
-        // operand descriptors from a base plus an offset (the descriptor's address field
-        // counts 16-byte units; shared memory stays below 2^18 bytes).
+        // the whole warp walks the block's pairs and waits on the barriers (so that it stays
+        // converged); lane 0 alone issues the MMAs and the commits.
         bool w = true;
         const uint64_t da0 = umma_desc_sw128(sA), db0 = umma_desc_sw128(sB);
         uint64_t db = db0 + (uint64_t)(cur * (kTileBytes >> 4));
-        for (int m = 0; m < n && w; ++m) {
-          const unsigned kt = (unsigned)(k + m);
-          const unsigned s = kt & (kAccBufs - 1), ph = (kt / kAccBufs) & 1;
-          if ((chg >> m) & 1) {  // warp-uniform (a ballot)
-            if (nchg > 0 && lane == 0) umma_commit(&b_empty[cur]);  // fires once the previous block's MMAs are done
-            cur = nchg % kKeyBufs;
-            db = db0 + (uint64_t)(cur * (kTileBytes >> 4));
-            w = mbar_wait(&b_full[cur], (nchg / kKeyBufs) & 1, abort);
-            ++nchg;
-          }
-          w = w && mbar_wait(&a_full[s], ph, abort);
-          w = w && (kt < (unsigned)kAccBufs || mbar_wait(&acc_empty[s], ph ^ 1u, abort));
+        for (int m = 0; m < n && w; m += 2) {
+          const unsigned pr = (unsigned)((k + m) >> 1);
+          const unsigned ps = pr & 1u, ph = (pr >> 1) & 1u;
+          w = mbar_wait(&a_pair[ps], ph, abort);
+          w = w && (pr < 2u || mbar_wait(&acc_free[ps], ph ^ 1u, abort));
           w = __all_sync(kFull, w);
-          if (w) {
-            tc_fence_after();
-            if (lane == 0) {
-              const uint64_t da = da0 + (uint64_t)(s * (kTileBytes >> 4));
-              const uint32_t td = tmem + s * 128;
-              umma_bf16_first(td, da, db, idesc);
-#pragma unroll
-              for (int kk = 1; kk < 4; ++kk) umma_bf16_acc(td, da + 2 * kk, db + 2 * kk, idesc);
-              umma_commit(&acc_full[s]);  // also frees the tile's query-row stage
+          for (int i = 0; i < 2 && w && m + i < n; ++i) {
+            if ((chg >> (m + i)) & 1) {  // warp-uniform (a ballot)
+              if (nchg > 0 && lane == 0) umma_commit(&b_empty[cur]);  // fires once the previous block's MMAs are done
+              cur = nchg % kKeyBufs;
+              db = db0 + (uint64_t)(cur * (kTileBytes >> 4));
+              w = __all_sync(kFull, mbar_wait(&b_full[cur], (nchg / kKeyBufs) & 1, abort));
+              ++nchg;
             }
-            __syncwarp();
+            if (w) {
+              tc_fence_after();
+              if (lane == 0) {
+                const unsigned s = 2 * ps + i;
+                const uint64_t da = da0 + (uint64_t)(s * (kTileBytes >> 4));
+                const uint32_t td = tmem + s * 128;
+                umma_bf16_first(td, da, db, idesc);
+#pragma unroll
+                for (int kk = 1; kk < 4; ++kk) umma_bf16_acc(td, da + 2 * kk, db + 2 * kk, idesc);
+              }
+            }
           }
+          if (w && lane == 0) umma_commit(&acc_pair[ps]);  // also frees the pair's query-row stages
+          __syncwarp();
         }
         k += n;
         ok = w;
@@ -345,65 +378,93 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
     if (!ok && lane == 0) leaf_abort(abort, P.status);
     if (mma && lane == 0) {
       // every MMA this thread issued has completed once mma_done fires (waited for even
-      // after an abort, with a poll limit, so that TMEM is never freed under an MMA)
+      // after an abort, with a poll limit); if it never fires TMEM is not freed
       umma_commit(&mma_done);
-      if (!mbar_wait(&mma_done, 0, nullptr)) leaf_abort(abort, P.status);
+      if (!mbar_wait(&mma_done, 0, nullptr)) {
+        leaf_abort(abort, P.status);
+        mma_ok = false;
+      }
+    }
+    if (!mma && lane == 0 && *abort) {
+      // after an abort, wait (bounded) for the key blocks still in flight into this CTA
+      for (int c = max(0, nissued - kKeyBufs); c < nissued; ++c)
+        mbar_wait(&b_full[c % kKeyBufs], (c / kKeyBufs) & 1, nullptr);
     }
   } else if (warp == 2 || warp == 3) {
-    // ---------------- query-row warps: tile k's rows are loaded by warp 2 + (k & 1), one
-    // TMA box {64 features, G heads, 1 token} per query, completing on a_full.  The
-    // descriptors are read two tiles ahead and the entries one tile ahead.
+    // ---------------- query-row warps: pair P's rows are loaded by warp 2 + (P & 1), one
+    // TMA box {64 features, G heads, 1 token} per query (lane l: tile 2P + l / R, row l % R),
+    // all completing on a_pair[P & 1].  Before refilling the stages of pair P the warp waits
+    // for pair P - 2's MMAs (its own previous pair), so it is never two phases ahead.
     const int tw = warp - 2;
-    int4 d1 = make_int4(0, 0, 0, 0), d2 = make_int4(0, 0, 0, 0);
-    if (tw < my_tiles) d1 = __ldg(tdesc + tile_of(tw));
-    if (tw + 2 < my_tiles) d2 = __ldg(tdesc + tile_of(tw + 2));
-    uint32_t e1 = lane < d1.y ? __ldg(P.list + d1.x + lane) : 0u;
-    for (int k = tw; k < my_tiles; k += 2) {
-      const int4 d = d1;
-      const uint32_t ent = e1;
-      d1 = d2;
-      e1 = (k + 2 < my_tiles && lane < d1.y) ? __ldg(P.list + d1.x + lane) : 0u;
-      if (k + 4 < my_tiles) d2 = __ldg(tdesc + tile_of(k + 4));
-      const int s = k % kLeafStages;
+    const int sub = lane / R, row = lane % R;  // tile of the pair and row this lane loads
+    int issued = -1;  // last pair this warp issued (for the abort drain)
+    for (int pr = tw; pr < my_pairs; pr += 2) {
+      const int kt = 2 * pr + sub;
+      const bool has = sub < 2 && kt < my_tiles;
+      const int4 d = has ? __ldg(tdesc + tile_of(kt)) : make_int4(0, 0, 0, 0);
+      const bool live = has && row < d.y;
+      const uint32_t ent = live ? __ldg(P.list + d.x + row) : 0u;
+      const int ps = pr & 1;
+      int nrows = __reduce_add_sync(kFull, live ? 1 : 0);
       bool w = true;
       if (lane == 0) {
-        if (k >= kLeafStages) w = mbar_wait(&acc_full[s], ((k / kLeafStages) - 1) & 1, abort);
-        if (w) mbar_expect_tx(&a_full[s], (uint32_t)(d.y * G * 128));
+        if (pr >= 2) w = mbar_wait(&acc_pair[ps], ((pr >> 1) - 1) & 1, abort);
+        if (w) mbar_expect_tx(&a_pair[ps], (uint32_t)(nrows * G * 128));
       }
       if (!__shfl_sync(kFull, w, 0)) {
         if (lane == 0) leaf_abort(abort, P.status);
         break;
       }
       __syncwarp();
-      if (lane < d.y) {
+      if (live) {
         const long long tq = PISA_IN_BOUNDS((long long)(ent >> 5) < P.N && d.w >= 0) ? (long long)(ent >> 5) : 0;
-        tma_load_3d(sA + s * kTileBytes + lane * Gp * 128, &qmap, 0, (d.w % P.Hkv) * G,
-                    (int)((d.w / P.Hkv) * P.N + tq), &a_full[s]);
+        tma_load_3d(sA + (2 * ps + sub) * kTileBytes + row * Gp * 128, &qmap, 0, (d.w % P.Hkv) * G,
+                    (int)((d.w / P.Hkv) * P.N + tq), &a_pair[ps]);
       }
+      issued = pr;
     }
+    if (lane == 0 && *abort && issued >= 0) mbar_wait(&a_pair[issued & 1], (issued >> 1) & 1, nullptr);
   } else {
-    // ---------------- epilogue (warps 4..15): warpgroup wg takes tiles wg, wg + 3, ...;
-    // TMEM -> registers 32 columns at a time -> log-sum-exp per key half -> head sum
+    // ---------------- epilogue (warps 4..19): warpgroup wg takes tiles wg, wg + 4, ...;
+    // TMEM -> registers one key half (64 columns, one leaf) at a time -> its log-sum-exp;
+    // the accumulator is released once the second half is in registers.  The head sums
+    // and the store of a tile are done while the next tile's first half is being loaded.
     const int wg = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const int r = row / Gp, h = row % Gp;
+    float pv0 = 0.f, pv1 = 0.f;  // the previous tile's two leaf values (before the head sums)
+    float* pout = nullptr;       // where they go (nullptr: nothing pending)
     int4 dn = wg < my_tiles ? __ldg(tdesc + tile_of(wg)) : make_int4(0, 0, 0, 0);
     for (int k = wg; k < my_tiles; k += kEpiGroups) {
-      const int a = k % kAccBufs;
+      const int pr = k >> 1, ps = pr & 1;
       const int4 d = dn;  // this tile's descriptor (read one tile ahead)
       const bool qvalid = r < d.y;
       const uint32_t ent = qvalid ? __ldg(P.list + d.x + r) : 0u;
       if (k + kEpiGroups < my_tiles) dn = __ldg(tdesc + tile_of(k + kEpiGroups));
-      const bool ok = __all_sync(kFull, mbar_wait(&acc_full[a], (k / kAccBufs) & 1, abort));
+      const bool ok = __all_sync(kFull, mbar_wait(&acc_pair[ps], (pr >> 1) & 1, abort));
       if (!ok) {  // warp-uniform exit
         leaf_abort(abort, P.status);
+        pout = nullptr;
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + a * 128;
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (k & 3) * 128;
       float xa[32], xb[32];
       tmem_ld32(taddr, xa);
+      tmem_ld32(taddr + 32, xb);
+      // the previous tile's head sums and store, while the loads are in flight
+      {
+        float a0 = pv0, a1 = pv1;
+        for (int o = Gp >> 1; o > 0; o >>= 1) {
+          a0 += __shfl_xor_sync(kFull, a0, o);
+          a1 += __shfl_xor_sync(kFull, a1, o);
+        }
+        if (pout) {
+          pout[0] = a0;
+          pout[1] = a1;
+        }
+      }
       const int tp = d.z, tbh = d.w;
       const long long t = ent >> 5;
       const int qslot = ent & 31;
@@ -412,53 +473,51 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
       long long lim = qvalid ? n_eff - 128LL * tp : 128;
       if (lim > 128) lim = 128;
       if (lim < 1) lim = 1;
-      const int l = (int)lim;  // columns [0, l) count; chunk c holds columns [32c, 32c + 32)
+      const int l = (int)lim;  // columns [0, l) count
       const int c0 = min(l, 32), c1 = min(max(l - 32, 0), 32), c2 = min(max(l - 64, 0), 32),
                 c3 = max(l - 96, 0);
-      // columns 0..63 (key half 0) first; columns 64..127 are loaded while half 0 is
-      // summed, and the accumulator is released as soon as they are in registers
       using Acc = typename std::conditional<MODE == 0, HalfLse, HalfMom<MODE>>::type;
       Acc h0, h1;
-      tmem_ld32(taddr + 32, xb);
       tmem_ld_wait();
       reg_fence32(xa);
       reg_fence32(xb);
-      h0.first(xa, c0, __all_sync(kFull, c0 == 32));
+      h0.first2(xa, xb, c0, c1, __all_sync(kFull, l >= 64));
       tmem_ld32(taddr + 64, xa);
-      if (__any_sync(kFull, c1 > 0)) h0.add(xb, c1, __all_sync(kFull, c1 == 32));
       tmem_ld32(taddr + 96, xb);
       tmem_ld_wait();
       reg_fence32(xa);
       reg_fence32(xb);
       tc_fence_before();
-      mbar_arrive(&acc_empty[a]);
+      mbar_arrive(&acc_free[ps]);
       const bool any1 = __any_sync(kFull, c2 > 0);
-      if (any1) h1.first(xa, c2 > 0 ? c2 : 1, __all_sync(kFull, c2 == 32));
-      if (any1 && __any_sync(kFull, c3 > 0)) h1.add(xb, c3, __all_sync(kFull, c3 == 32));
+      if (any1) h1.first2(xa, xb, c2 > 0 ? c2 : 1, c3, __all_sync(kFull, l == 128));
       const bool head = qvalid && h < G;
-      float v0 = head ? h0.value() : 0.f, v1 = (head && any1) ? h1.value() : 0.f;
-      for (int o = Gp >> 1; o > 0; o >>= 1) {
-        v0 += __shfl_xor_sync(kFull, v0, o);
-        v1 += __shfl_xor_sync(kFull, v1, o);
-      }
+      pv0 = head ? h0.value() : 0.f;
+      pv1 = (head && any1) ? h1.value() : 0.f;
+      pout = nullptr;
       if (qvalid && h == 0 && PISA_IN_BOUNDS(t < P.N && (P.flat || qslot < P.K))) {
-        float* out = P.flat ? P.leaf_scores + ((long long)tbh * P.N + t) * P.flat_stride + 2 * tp
-                            : P.leaf_scores + ((long long)tbh * P.N + t) * (2 * P.K) + 2 * qslot;
-        out[0] = v0;
-        out[1] = l > 64 ? v1 : -INFINITY;
+        pout = P.flat ? P.leaf_scores + ((long long)tbh * P.N + t) * P.flat_stride + 2 * tp
+                      : P.leaf_scores + ((long long)tbh * P.N + t) * (2 * P.K) + 2 * qslot;
+        if (l <= 64) pv1 = -INFINITY;  // the second leaf starts after the query
       }
     }
-  }
-  if (threadIdx.x == 0 && *abort) {
-    // after an abort, give copies still in flight into this CTA's shared memory time to land
-    const long long t0 = clock64();
-    while (clock64() - t0 < 4000000) {
+    {  // the last tile's head sums and store
+      float a0 = pv0, a1 = pv1;
+      for (int o = Gp >> 1; o > 0; o >>= 1) {
+        a0 += __shfl_xor_sync(kFull, a0, o);
+        a1 += __shfl_xor_sync(kFull, a1, o);
+      }
+      if (pout) {
+        pout[0] = a0;
+        pout[1] = a1;
+      }
     }
   }
   __syncthreads();
   if (warp == 1) {
+    const bool free_ok = __shfl_sync(kFull, mma_ok, 0);
     tc_fence_after();
-    tmem_dealloc<kAccBufs * 128>(tmem);
+    if (free_ok) tmem_dealloc<kAccBufs * 128>(tmem);
   }
 }
 
