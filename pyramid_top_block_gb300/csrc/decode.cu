@@ -8,10 +8,14 @@
 // One CTA of kDecWarps warps per (b, kv).  Threads 0..63 update the path (one
 // feature each); then every level's candidates are scored one warp per candidate
 // (lanes = child x head for an intermediate node; for a leaf, the exact score on
-// mma.sync with the query heads as rows and the leaf's 64 keys as 8 column tiles)
-// and warp 0 keeps the Top-K and expands the survivors.
+// mma.sync with the query heads as rows and the leaf's 64 keys as 8 column tiles).
+// Every warp then ranks the same scores and expands the same survivors itself, so
+// a level costs one CTA barrier; the keys of the leaf candidates are requested
+// into L2 while level 2 is scored.  The step is a chain of dependent memory round
+// trips (the new length, the path, one per level, the leaf keys) on a grid of
+// B * Hkv CTAs.
 #include "api.cuh"
-#include "walk.cuh"
+#include "tc.cuh"
 
 namespace pisa {
 
@@ -147,15 +151,16 @@ __device__ __forceinline__ float warp_leaf_mma(const __nv_bfloat16* keys_b, int 
   for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      e0 += expf(z[nt][e] - m0);
-      e1 += expf(z[nt][2 + e] - m1);
+      e0 += ex2_approx((z[nt][e] - m0) * 1.4426950408889634f);
+      e1 += ex2_approx((z[nt][2 + e] - m1) * 1.4426950408889634f);
     }
 #pragma unroll
   for (int o = 1; o < 4; o <<= 1) {
     e0 += __shfl_xor_sync(kFull, e0, o);
     e1 += __shfl_xor_sync(kFull, e1, o);
   }
-  float v = (g < G ? m0 + logf(e0) : 0.f) + (g + 8 < G ? m1 + logf(e1) : 0.f);
+  float v = (g < G ? m0 + lg2_approx(e0) * 0.69314718055994531f : 0.f) +
+            (g + 8 < G ? m1 + lg2_approx(e1) * 0.69314718055994531f : 0.f);
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
   return v;
@@ -173,8 +178,10 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
   __shared__ __align__(16) float qs[G * kQStride];
   __shared__ float sib[kMaxLevels + 1][kD];  // siblings along the new token's path
   __shared__ __align__(16) __nv_bfloat16 lk[kC * kD];  // the earlier keys of the new token's leaf
-  __shared__ WarpScratch ws;
-  __shared__ int nC_s;
+  __shared__ int dcand[kDecWarps][2 * kMaxK];   // each warp's copy of the candidate list
+  __shared__ int dnext[kDecWarps][kMaxK];       // each warp's survivor compaction
+  __shared__ float dscore[2][2 * kMaxK];        // candidate scores, by level parity
+  __shared__ float dnext_s[kMaxK];
   const int b = blockIdx.x / Hkv, kv = blockIdx.x % Hkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long p = lengths[b];
@@ -252,77 +259,138 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
   }
   __threadfence_block();
   __syncthreads();
-  if (tid == 0) {
-    // every thread of this CTA has read lengths[b]; the last of the sequence's Hkv CTAs
-    // to get here advances it (none of them reads it again)
-    __threadfence();
-    if (atomicAdd(arrivals + b, 1) == Hkv - 1) lengths[b] = (int32_t)(p + 1);
-  }
 
-  // intermediate levels L-1 .. 2 (levels with at most K candidates are kept whole)
-  int nS = 1, myS = 0;  // survivors, held by warp 0 (lane j < nS holds the j-th)
-  for (int l = lv.L - 1; l >= 2; --l) {
-    if (warp == 0) {
-      const int nC = warp_expand(ws, nS, myS, l, lv.M[l], p, true, lane);
-      if (lane == 0) nC_s = nC;
+  // The walk.  Every warp holds the same survivor list (lane j: the j-th survivor) and
+  // expands it into its own copy of the candidate list; the warps score the candidates
+  // (warp w: candidates w, w + kDecWarps, ...) into a score array shared by the CTA and
+  // double-buffered by level parity; after one barrier every warp ranks the same scores
+  // and compacts the same survivors, so a level costs one barrier.
+  int* cand = dcand[warp];
+  int nS = 1, myS = 0;
+  int par = 0;
+  int nC = 1;
+  if (lv.L == 1) {  // a single leaf, which is the root
+    if (lane == 0) cand[0] = 0;
+    __syncwarp();
+  }
+  for (int l = lv.L - 1; l >= 1; --l) {
+    {  // candidates: the children of the survivors (in decode every existing node is eligible)
+      const bool v0 = lane < nS;
+      const long long c1 = 2LL * myS + 1;
+      const bool v1 = v0 && c1 < lv.M[l];
+      const unsigned b1 = __ballot_sync(kFull, v1);
+      const int pos = lane + __popc(b1 & ((1u << lane) - 1u));
+      nC = nS + __popc(b1);
+      if (v0 && PISA_IN_BOUNDS(pos + (v1 ? 1 : 0) < 2 * kMaxK)) {
+        cand[pos] = 2 * myS;
+        if (v1) cand[pos + 1] = (int)c1;
+      }
+      __syncwarp();
     }
-    __syncthreads();
-    const int nC = nC_s;
-    if (nC > K) {
-      const long long off1 = lv.off[l - 1], M1 = lv.M[l - 1];
-      const long long off2 = l >= 3 ? lv.off[l - 2] : 0, M2 = l >= 3 ? lv.M[l - 2] : 0;
-      for (int ci = warp; ci < nC; ci += kDecWarps) {
-        const float sc = warp_node_score<G>(blk, off1, M1, off2, M2, l, ws.cand[ci], qs, lane);
-        if (lane == 0) ws.score[ci] = sc;
-      }
-      __syncthreads();
-      if (warp == 0) {
-        warp_topk(ws, nC, K, lane);
-        nS = K;
-        myS = lane < K ? ws.next[lane] : 0;
-      }
-    } else if (warp == 0) {
+    if (l == 1) break;
+    if (nC <= K) {  // kept whole, unscored
       nS = nC;
-      myS = lane < nC ? ws.cand[lane] : 0;
+      myS = lane < nC ? cand[lane] : 0;
+      __syncwarp();
+      continue;
+    }
+    float* sc = dscore[par];
+    const long long off1 = lv.off[l - 1], M1 = lv.M[l - 1];
+    const long long off2 = l >= 3 ? lv.off[l - 2] : 0, M2 = l >= 3 ? lv.M[l - 2] : 0;
+    for (int ci = warp; ci < nC; ci += kDecWarps) {
+      const int c = cand[ci];
+      if (l == 2) {  // the keys of c's two leaves go to L2 while the level is scored
+        const long long r0 = 128LL * c;
+        for (int r = lane; r < 128; r += 32)
+          if (r0 + r < n) asm volatile("prefetch.global.L2 [%0];" ::"l"(keys_b + ((r0 + r) * Hkv + kv) * kD));
+      }
+      const float v = warp_node_score<G>(blk, off1, M1, off2, M2, l, c, qs, lane);
+      if (lane == 0) sc[ci] = v;
     }
     __syncthreads();
+    // rank count over the shared scores (candidate i survives iff fewer than K beat it; j
+    // beats i when its score is higher, or equal with j < i, i.e. the lower node index)
+    bool sel[2] = {false, false};
+    unsigned m[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int ci = lane + 32 * u;
+      if (ci < nC) {
+        const float x = sc[ci];
+        int rank = 0;
+        for (int j = 0; j < nC; ++j) {
+          const float y = sc[j];
+          rank += (y > x || (y == x && j < ci));
+        }
+        sel[u] = rank < K;
+      }
+      m[u] = __ballot_sync(kFull, sel[u]);
+    }
+    int* nx = dnext[warp];
+    const unsigned lt = (1u << lane) - 1u;
+    if (sel[0]) nx[__popc(m[0] & lt)] = cand[lane];
+    if (sel[1]) nx[__popc(m[0]) + __popc(m[1] & lt)] = cand[lane + 32];
+    __syncwarp();
+    nS = K;
+    myS = lane < K ? nx[lane] : 0;
+    __syncwarp();
+    par ^= 1;
   }
-  // leaves: children of the level-2 survivors, scored exactly when there are more
-  // than K of them or when scores are requested
-  if (warp == 0) {
-    const int nC = warp_expand(ws, nS, myS, 1, lv.M[1], p, true, lane);
-    if (lane == 0) nC_s = nC;
-  }
-  __syncthreads();
-  const int nC = nC_s;
+  // leaves: the children of the level-2 survivors (cand holds them), scored exactly when
+  // there are more than K of them or when scores are requested
+  float* sc = dscore[par];
   if (nC > K || so != nullptr) {
     uint32_t qa[4][4];
     leaf_q_frags<G>(q_new + ((long long)b * Hq + (long long)kv * G) * kD, lane, qa);
     for (int ci = warp; ci < nC; ci += kDecWarps) {
-      const float sc = warp_leaf_mma<G>(keys_b, Hkv, kv, ws.cand[ci], n, qa, lane);
-      if (lane == 0) ws.score[ci] = sc;
+      const float v = warp_leaf_mma<G>(keys_b, Hkv, kv, cand[ci], n, qa, lane);
+      if (lane == 0) sc[ci] = v;
     }
-    __syncthreads();
   }
+  __syncthreads();
   if (warp != 0) return;
-  int nOut;
-  if (nC > K) {
-    warp_topk(ws, nC, K, lane);
-    nOut = K;
-  } else {
-    if (lane < nC) ws.next[lane] = ws.cand[lane];
-    nOut = nC;
-    __syncwarp();
-  }
-  if (lane < K) {
-    const int lf = lane < nOut ? ws.next[lane] : -1;
-    io[lane] = lf;
-    if (so) {
-      float sc = -INFINITY;
-      for (int ci = 0; ci < nC; ++ci)
-        if (lf >= 0 && ws.cand[ci] == lf) sc = ws.score[ci];
-      so[lane] = sc;
+  bool sel[2] = {false, false};
+  unsigned m[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int ci = lane + 32 * u;
+    if (ci < nC) {
+      bool keep = true;
+      if (nC > K) {
+        const float x = sc[ci];
+        int rank = 0;
+        for (int j = 0; j < nC; ++j) {
+          const float y = sc[j];
+          rank += (y > x || (y == x && j < ci));
+        }
+        keep = rank < K;
+      }
+      sel[u] = keep;
     }
+    m[u] = __ballot_sync(kFull, sel[u]);
+  }
+  const unsigned lt = (1u << lane) - 1u;
+  int* nx = dnext[0];
+  float* nxs = dnext_s;
+  if (sel[0]) {
+    nx[__popc(m[0] & lt)] = cand[lane];
+    nxs[__popc(m[0] & lt)] = so ? sc[lane] : 0.f;
+  }
+  if (sel[1]) {
+    nx[__popc(m[0]) + __popc(m[1] & lt)] = cand[lane + 32];
+    nxs[__popc(m[0]) + __popc(m[1] & lt)] = so ? sc[lane + 32] : 0.f;
+  }
+  __syncwarp();
+  const int nOut = __popc(m[0]) + __popc(m[1]);
+  if (lane < K) {
+    io[lane] = lane < nOut ? nx[lane] : -1;
+    if (so) so[lane] = lane < nOut ? nxs[lane] : -INFINITY;
+  }
+  if (lane == 0) {
+    // every thread of this CTA has read lengths[b] (they all passed the barrier above);
+    // the last of the sequence's Hkv CTAs to get here advances it
+    __threadfence();
+    if (atomicAdd(arrivals + b, 1) == Hkv - 1) lengths[b] = (int32_t)(p + 1);
   }
 }
 

@@ -51,7 +51,11 @@
 
 namespace pisa {
 
-constexpr int kWalkWarps = 8;
+constexpr int kWalkWarps = 8;    // walk_mma_kernel (K <= 32): 8 warps, 3 CTAs per SM
+// walk_k8_kernel / walk_k8s_kernel (K <= 8): one CTA of 24 warps per SM, so that the
+// shared-memory copy of the top levels' rows is held once per SM instead of three times
+// and can cover one more level (the 496 rows of levels 9..5 at 262144 tokens).
+constexpr int kWalk8Warps = 24;
 
 struct RowOffsets {
   long long o[kMaxLevels + 2];
@@ -60,7 +64,8 @@ constexpr int kRowBytes = 256;
 constexpr int kZRows = 2 * kMaxK;    // mean rows of the first scored level (at most 2K nodes)
 constexpr float kRowScale = 0.18033688011112042f;  // log2(e) / sqrt(64)
 constexpr int kCacheRowBytes = 272;  // shared-memory row stride (16-byte pad against bank conflicts)
-constexpr int kCacheRows = 240;      // Delta rows of the top scored levels kept in shared memory
+constexpr int kCacheRows = 240;      // Delta rows of the top scored levels kept in shared memory (K <= 32 kernel)
+constexpr int kCacheRows8 = 496;     // the same for the K <= 8 kernels (one CTA per SM)
 
 // Storage position (in bf16 elements, 0..63) of feature d inside a permuted half-row.
 __host__ __device__ __forceinline__ int perm_pos(int d) {
@@ -537,7 +542,7 @@ __device__ __forceinline__ float keep_mul(float pa, float pb, int s) {
 // (PISA-2).  With children logits z + u and z - r u: mean = z + (1 - r) u / 2, variance / 2 =
 // (1 + r)^2 u^2 / 8 (natural units; ln 2 (1 + r)^2 u^2 / 8 for base-2 logits u).
 template <int NT, int MODE>
-__global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
+__global__ void __launch_bounds__(kWalk8Warps * 32, 1) walk_k8_kernel(
     const __nv_bfloat16* __restrict__ Q, const unsigned char* __restrict__ table, Levels lv, RowOffsets ro,
     LevelTail tail, long long rows_per_bh, int N, int Hq, int Hkv, int K, int causal, int l_start, int l_lo,
     int32_t* __restrict__ surv, int32_t* __restrict__ srank, int* __restrict__ count, int t0, int t1, int chunk_shift,
@@ -587,7 +592,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8_kernel(
   const unsigned lt = (1u << lane) - 1u;
   constexpr unsigned kLo = 0x11111111u, kHi = 0x22222222u;  // lanes owning candidates 0..7 / 8..15 (j = 0 / 1)
 
-  for (int t = t0 + blockIdx.x + gridDim.x * warp; t < t1; t += gridDim.x * kWalkWarps) {
+  for (int t = t0 + blockIdx.x + gridDim.x * warp; t < t1; t += gridDim.x * kWalk8Warps) {
     __syncwarp();  // the previous query's reads of the candidate buffers are done
     const long long job = bh * N + t;
     int32_t* out = surv + job * K;
@@ -845,7 +850,7 @@ __device__ __forceinline__ void tile_dots_s(const uint32_t (&A)[4][4], const uin
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8s_kernel(
+__global__ void __launch_bounds__(kWalk8Warps * 32, 1) walk_k8s_kernel(
     const __nv_bfloat16* __restrict__ Q, const unsigned char* __restrict__ table, Levels lv, RowOffsets ro,
     LevelTail tail, long long rows_per_bh, int N, int Hq, int Hkv, int K, int causal, int l_start, int l_lo,
     int32_t* __restrict__ surv, int32_t* __restrict__ srank, int* __restrict__ count, int t0, int t1, int chunk_shift,
@@ -887,7 +892,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8s_kernel(
           __ldg(reinterpret_cast<const uint4*>(tb + (long long)crow0 * kRowBytes) + e);
   }
   __syncthreads();
-  for (int t = t0 + blockIdx.x + gridDim.x * warp; t < t1; t += gridDim.x * kWalkWarps) {
+  for (int t = t0 + blockIdx.x + gridDim.x * warp; t < t1; t += gridDim.x * kWalk8Warps) {
     __syncwarp();  // the previous query's reads of the candidate buffers are done
     const long long job = bh * N + t;
     if (l_start < 2) {
@@ -1060,6 +1065,18 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_k8s_kernel(
 }
 
 // Host side: table size and launches.
+static int walk_sm_count() {
+  static int n[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (!n[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 152;
+  }
+  return n[dev];
+}
+
 long long route_rows_per_bh(const Levels& lv) {
   long long r = 1 + kZRows;  // the zero row and the mean rows
   for (int l = 2; l <= lv.L; ++l) r += lv.M[l];
@@ -1096,14 +1113,18 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
     mark_phase(1, s);
   }
   if (W.t1 <= W.t0) return cudaSuccess;
-  // the rows of levels [l_lo, l_start] (at most kCacheRows) are cached in shared memory
+  // the rows of levels [l_lo, l_start] (at most kCacheRows / kCacheRows8) are cached in
+  // shared memory
+  const bool k8 = W.K <= 8;
+  const int cache_rows = k8 ? kCacheRows8 : kCacheRows;
   int l_lo = l_start + 1, crows = 0;
-  while (l_start >= 2 && l_lo - 1 >= 2 && crows + lv.M[l_lo - 1] <= kCacheRows) {
+  while (l_start >= 2 && l_lo - 1 >= 2 && crows + lv.M[l_lo - 1] <= cache_rows) {
     --l_lo;
     crows += lv.M[l_lo];
   }
-  // CTAs per (b, kv): about 3 resident CTAs per SM over the whole grid
-  int per_bh = (int)((3LL * 152 + BH - 1) / BH);
+  // CTAs per (b, kv): one CTA per SM (K <= 8) or about three, over the whole grid
+  const long long ctas = (k8 ? 1LL : 3LL) * walk_sm_count();
+  int per_bh = (int)((ctas + BH - 1) / BH);
   if (per_bh > W.t1 - W.t0) per_bh = (int)(W.t1 - W.t0);
   if (per_bh < 1) per_bh = 1;
   dim3 grid((unsigned)per_bh, (unsigned)BH);
@@ -1124,7 +1145,7 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
         }
       }
     }
-    const size_t smem = (size_t)(16 + crows) * kCacheRowBytes + (size_t)kWalkWarps * kCandBuf * 4;
+    const size_t smem = (size_t)(16 + crows) * kCacheRowBytes + (size_t)kWalk8Warps * kCandBuf * 4;
     auto pick = [&](auto nt) {
       constexpr int NT = decltype(nt)::value;
       return W.mode == 1 ? walk_k8_kernel<NT, 1> : W.mode == 2 ? walk_k8_kernel<NT, 2> : walk_k8_kernel<NT, 0>;
@@ -1145,7 +1166,7 @@ cudaError_t launch_prefill_walk_mma(const WalkLaunch& W, cudaStream_t s) {
         attr[G > 8][W.mode] = smem;
       }
     }
-    kern<<<grid, kWalkWarps * 32, smem, s>>>(W.Q, W.table, lv, ro, tail, rows, (int)W.N, W.Hq, W.Hkv, W.K, W.causal,
+    kern<<<grid, kWalk8Warps * 32, smem, s>>>(W.Q, W.table, lv, ro, tail, rows, (int)W.N, W.Hq, W.Hkv, W.K, W.causal,
                                               l_start, l_lo, W.surv, W.srank, W.count, (int)W.t0, (int)W.t1,
                                               W.chunk_shift, W.M2);
     note_launch();
