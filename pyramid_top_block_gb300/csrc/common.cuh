@@ -45,8 +45,8 @@ __host__ __device__ inline int num_levels_for(long long n) {
 
 __host__ __device__ inline long long level_size_for(long long n, int l) {
   if (l == 0) return n;
-  long long w = (long long)kC << (l - 1);
-  return (n + w - 1) / w;
+  const int sh = kLog2C + l - 1;  // a node of level l spans 2^sh tokens
+  return (n + (1LL << sh) - 1) >> sh;
 }
 
 // First token of node i at level l (level 0: the raw key i itself).
@@ -78,10 +78,16 @@ __device__ __forceinline__ void unpack8(const uint4 v, float* f) {
 // parent = (m0 * n0 + m1 * n1) / (n0 + n1).  A parent with one child equals it.
 // Shared by the prefill build and the decode path update so both produce the
 // same bits for the same node.
+// s / n correctly rounded.  When n is a power of two its reciprocal is exact and the
+// product rounds the same exact quotient, so it gives the bits of the division.
+__device__ __forceinline__ float div_count(float s, int n) {
+  return (n & (n - 1)) == 0 ? __fmul_rn(s, __int_as_float((127 - (__ffs(n) - 1)) << 23)) : __fdiv_rn(s, (float)n);
+}
+
 __device__ __forceinline__ float merge_mean(float m0, int n0, float m1, int n1) {
   if (n1 <= 0) return m0;
   float s = __fadd_rn(__fmul_rn(m0, (float)n0), __fmul_rn(m1, (float)n1));
-  return __fdiv_rn(s, (float)(n0 + n1));
+  return div_count(s, n0 + n1);
 }
 
 // Record a device-side error in the caller's workspace status word (first

@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
     float acc = 0.f;
     for (int r = 0; r < (int)(p - leaf * kC); ++r) acc = __fadd_rn(acc, bf2f(lk[r * kD + e]));
     acc = __fadd_rn(acc, bf2f(kn));
-    float m = __fdiv_rn(acc, (float)(p - leaf * kC + 1));
+    float m = div_count(acc, (int)(p - leaf * kC + 1));
     blk[(lv.off[1] + leaf) * kD + e] = m;
     long long i = leaf;
     for (int l = 2; l <= lv.L; ++l) {

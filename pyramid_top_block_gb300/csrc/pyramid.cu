@@ -12,8 +12,13 @@
 //       head and sums that column over the leaf's tokens in token order, so a
 //       warp reads whole 256-byte token rows.  The CTA then merges its LPB
 //       leaves up log2(LPB) levels in shared memory.
-//   pyramid_top_kernel    : one CTA per (b, kv) merges the remaining levels up
-//       to the root.
+//   pyramid_top_reg_kernel: one CTA per (b, kv) merges the remaining levels up to
+//       the root, each warp five levels of its 32 nodes in registers (no CTA
+//       barrier), warp 0 the last three from the warps' roots;
+//   pyramid_top_kernel    : the same level by level through global memory, for
+//       layouts whose merged-in-CTA level is larger (many KV heads).
+// Divisions by a power-of-two count are exact multiplications (div_count), the
+// same bits as the division.
 #include <mutex>
 
 #include "api.cuh"
@@ -68,9 +73,8 @@ __global__ void __launch_bounds__(256) pyramid_leaves_kernel(
         }
       }
     }
-    const float fc = (float)cnt;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = __fdiv_rn(acc[i], fc);
+    for (int i = 0; i < 8; ++i) acc[i] = div_count(acc[i], cnt);
     float4* dst = reinterpret_cast<float4*>(blk + (lv.off[1] + leaf) * kD + c8 * 8);
     dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
@@ -129,53 +133,82 @@ __global__ void __launch_bounds__(256) pyramid_top_kernel(float* __restrict__ su
   }
 }
 
-// The same levels when level first_level - 1 holds at most kTopNodes nodes: that
-// level is staged in shared memory once and every level above is merged there
-// (children read into registers, a barrier, parents written in place and to
-// global memory), so the chain of levels costs no global round trips.  Same
-// merge arithmetic, same bits.
-constexpr int kTopNodes = 256;                            // 64 KB of fp32 rows
-constexpr int kTopThreads = 1024;
-constexpr int kTopPer = (kTopNodes / 2) * kD / kTopThreads;  // outputs per thread at the first level
-__global__ void __launch_bounds__(kTopThreads) pyramid_top_smem_kernel(float* __restrict__ summ, Levels lv,
-                                                                      long long N, int Hkv, int first_level,
-                                                                      const int32_t* __restrict__ lens,
-                                                                      long long n_cap) {
-  extern __shared__ float4 sm4[];
-  float* sm = reinterpret_cast<float*>(sm4);
+constexpr int kTopNodes = 256;  // largest input level the register kernel below takes (8 warps x 32 nodes)
+
+// The same levels when level first_level - 1 holds at most kTopNodes nodes, merged in
+// registers: warp w holds nodes [32 w, 32 w + 32) of that level, lane j features 2 j and
+// 2 j + 1, and merges them five levels up without a CTA barrier (writing every node it
+// forms); the warps' last nodes meet in shared memory, where warp 0 merges the levels
+// above.  Same merge arithmetic, same bits.
+constexpr int kRegWarps = kTopNodes / 32;
+__global__ void __launch_bounds__(kRegWarps * 32) pyramid_top_reg_kernel(float* __restrict__ summ, Levels lv,
+                                                                        long long N, int Hkv, int first_level,
+                                                                        const int32_t* __restrict__ lens,
+                                                                        long long n_cap) {
+  __shared__ float2 roots[kRegWarps][32];
   const int b = blockIdx.x / Hkv, kv = blockIdx.x % Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lens) N = min((long long)max(lens[b], 0), n_cap);
   float* blk = summ + ((long long)b * Hkv + kv) * lv.total * kD;
-  const long long Mc0 = level_size_for(N, first_level - 1);  // <= kTopNodes (checked by the host)
-  const float4* src = reinterpret_cast<const float4*>(blk + lv.off[first_level - 1] * kD);
-  for (long long w = threadIdx.x; w < Mc0 * (kD / 4); w += kTopThreads) sm4[w] = src[w];
+  const int L = lv.L;  // like the level-by-level kernels: every level of the layout is written
+  const int l0 = first_level - 1;  // the input level
+  const long long M0 = level_size_for(N, l0);
+  float2 v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const long long node = 32LL * warp + i;
+    v[i] = node < M0 ? reinterpret_cast<const float2*>(blk + (lv.off[l0] + node) * kD)[lane] : make_float2(0.f, 0.f);
+  }
+  // five levels inside the warp: 32 -> 16 -> 8 -> 4 -> 2 -> 1 nodes
+#pragma unroll
+  for (int j = 0; j < 5; ++j) {
+    const int l = first_level + j;
+    const int cnt = 16 >> j;                       // nodes this warp forms at level l
+    const long long base = (32LL * warp) >> (j + 1);  // the first of them
+    if (l <= L) {
+      const long long M = level_size_for(N, l), Mc = level_size_for(N, l - 1);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (i < cnt) {
+          const long long node = base + i;
+          const long long c0 = 2 * node, c1 = 2 * node + 1;
+          const int n0 = c0 < Mc ? node_count(l - 1, c0, N) : 0;
+          const int n1 = c1 < Mc ? node_count(l - 1, c1, N) : 0;
+          float2 o;
+          o.x = merge_mean(v[2 * i].x, n0, v[2 * i + 1].x, n1);
+          o.y = merge_mean(v[2 * i].y, n0, v[2 * i + 1].y, n1);
+          v[i] = o;
+          if (node < M) reinterpret_cast<float2*>(blk + (lv.off[l] + node) * kD)[lane] = o;
+        }
+      }
+    }
+  }
+  roots[warp][lane] = v[0];
   __syncthreads();
-  for (int l = first_level; l <= lv.L; ++l) {
-    const long long M = level_size_for(N, l), Mc = level_size_for(N, l - 1);
-    float out[kTopPer];
+  if (warp != 0) return;
+  // the levels above: warp 0 merges the kRegWarps warp roots (level first_level + 4)
 #pragma unroll
-    for (int r = 0; r < kTopPer; ++r) {
-      const int w = threadIdx.x + r * kTopThreads;
-      out[r] = 0.f;
-      if (w < M * kD) {
-        const long long i = w / kD;
-        const int e = w % kD;
-        const long long c0 = 2 * i, c1 = 2 * i + 1;
-        const int n0 = node_count(l - 1, c0, N);
-        const int n1 = c1 < Mc ? node_count(l - 1, c1, N) : 0;
-        out[r] = merge_mean(sm[c0 * kD + e], n0, n1 > 0 ? sm[c1 * kD + e] : 0.f, n1);
+  for (int i = 0; i < kRegWarps; ++i) v[i] = roots[i][lane];
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int l = first_level + 5 + j;
+    const int cnt = kRegWarps >> (j + 1);
+    if (l <= L) {
+      const long long M = level_size_for(N, l), Mc = level_size_for(N, l - 1);
+#pragma unroll
+      for (int i = 0; i < kRegWarps / 2; ++i) {
+        if (i < cnt) {
+          const long long c0 = 2LL * i, c1 = 2LL * i + 1;
+          const int n0 = c0 < Mc ? node_count(l - 1, c0, N) : 0;
+          const int n1 = c1 < Mc ? node_count(l - 1, c1, N) : 0;
+          float2 o;
+          o.x = merge_mean(v[2 * i].x, n0, v[2 * i + 1].x, n1);
+          o.y = merge_mean(v[2 * i].y, n0, v[2 * i + 1].y, n1);
+          v[i] = o;
+          if (i < M) reinterpret_cast<float2*>(blk + (lv.off[l] + i) * kD)[lane] = o;
+        }
       }
     }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < kTopPer; ++r) {
-      const int w = threadIdx.x + r * kTopThreads;
-      if (w < M * kD) {
-        sm[w] = out[r];
-        blk[lv.off[l] * kD + w] = out[r];
-      }
-    }
-    __syncthreads();
   }
 }
 
@@ -203,13 +236,8 @@ cudaError_t launch_build_pyramid(const __nv_bfloat16* keys, float* summ, const L
   if (e != cudaSuccess) return e;
   if (merge_levels + 2 <= lv.L) {
     const int first = merge_levels + 2;
-    if (lv.M[first - 1] <= kTopNodes) {
-      const size_t smem = (size_t)kTopNodes * kD * sizeof(float);
-      static std::once_flag once;
-      std::call_once(once, [smem] {
-        cudaFuncSetAttribute(pyramid_top_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      });
-      pyramid_top_smem_kernel<<<B * Hkv, kTopThreads, smem, s>>>(summ, lv, N, Hkv, first, lens, n_cap);
+    if (lv.M[first - 1] <= kTopNodes && lv.L - first + 1 <= 8) {
+      pyramid_top_reg_kernel<<<B * Hkv, kRegWarps * 32, 0, s>>>(summ, lv, N, Hkv, first, lens, n_cap);
     } else {
       pyramid_top_kernel<<<B * Hkv, 256, 0, s>>>(summ, lv, N, Hkv, first, lens, n_cap);
     }
