@@ -41,9 +41,9 @@ MUFU_EX2_PER_CLK_SM = 29.0  # measured ex2.approx throughput per SM and clock on
 KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
                   "walk": ["walk_mma.cu", "tc.cuh", "common.cuh", "api.cuh"]}
 NCU_TRAFFIC = {
-    ("leaf", "latency-256k"): {"bytes": 1888564000 + 35622912, "src_sha1": "0b4fa4031203dddd429dfd661fa75d4ab9d19b73",
+    ("leaf", "latency-256k"): {"bytes": 1770239000 + 34918656, "src_sha1": "d0a6343b4f5dce88e793241dfbb2de98bc6f21bf",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
-    ("walk", "latency-256k"): {"bytes": 1076219000 + 34968064, "src_sha1": "bb6c12db10106a570e3947e0faea7bd22e02bb79",
+    ("walk", "latency-256k"): {"bytes": 1076117000 + 34946304, "src_sha1": "fc088a3dad3a4cca1dac24fd34bc7058bf14fb0f",
                                "profile": "profiles/walk_k8s_kernel_latency-256k.md"},
 }
 
