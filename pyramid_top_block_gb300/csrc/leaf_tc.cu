@@ -482,6 +482,8 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
       reg_fence32(xa);
       reg_fence32(xb);
       h0.first2(xa, xb, c0, c1, __all_sync(kFull, l >= 64));
+      const bool head = qvalid && h < G;
+      pv0 = head ? h0.value() : 0.f;  // (h0 is dead from here on: fewer live registers)
       tmem_ld32(taddr + 64, xa);
       tmem_ld32(taddr + 96, xb);
       tmem_ld_wait();
@@ -491,8 +493,6 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
       mbar_arrive(&acc_free[ps]);
       const bool any1 = __any_sync(kFull, c2 > 0);
       if (any1) h1.first2(xa, xb, c2 > 0 ? c2 : 1, c3, __all_sync(kFull, l == 128));
-      const bool head = qvalid && h < G;
-      pv0 = head ? h0.value() : 0.f;
       pv1 = (head && any1) ? h1.value() : 0.f;
       pout = nullptr;
       if (qvalid && h == 0 && PISA_IN_BOUNDS(t < P.N && (P.flat || qslot < P.K))) {
