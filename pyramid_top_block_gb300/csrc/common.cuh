@@ -120,10 +120,4 @@ __device__ __forceinline__ bool in_bounds(bool ok) {
   } while (0)
 #endif
 
-// log(exp(a) + exp(b)) without overflow.
-__device__ __forceinline__ float lse2(float a, float b) {
-  float m = fmaxf(a, b);
-  return m + log1pf(expf(-fabsf(a - b)));
-}
-
 }  // namespace pisa

@@ -6,63 +6,24 @@
 // summaries and accumulation.
 //
 // One CTA of kDecWarps warps per (b, kv).  Threads 0..63 update the path (one
-// feature each); then every level's candidates are scored one warp per candidate
-// (lanes = child x head for an intermediate node; for a leaf, the exact score on
-// mma.sync with the query heads as rows and the leaf's 64 keys as 8 column tiles).
-// Every warp then ranks the same scores and expands the same survivors itself, so
-// a level costs one CTA barrier; the keys of the leaf candidates are requested
-// into L2 while level 2 is scored.  The step is a chain of dependent memory round
-// trips (the new length, the path, one per level, the leaf keys) on a grid of
-// B * Hkv CTAs.
+// feature each).  Warps 0..kWalkWarps - 1 then walk the intermediate levels: every
+// level's candidates are scored four to a warp on mma.sync (query heads as the A
+// operand, the children's fp32 summary rows as bf16 high + low B columns), every
+// walking warp ranks the same scores and expands the same survivors itself, so a
+// level costs one barrier of the walking warps.  The other warps are handed the
+// level-2 candidates and ask their leaves' keys into L2 meanwhile; then all warps
+// score the leaf candidates exactly (mma.sync, the query heads as rows and a leaf's
+// 64 keys as 8 column tiles) and warp 0 ranks them.  The step is a chain of
+// dependent memory round trips (the new length, the path, one per level, the leaf
+// keys) on a grid of B * Hkv CTAs.
 #include "api.cuh"
 #include "tc.cuh"
 
 namespace pisa {
 
 constexpr int kDecWarps = 16;
-constexpr int kQStride = kD + 4;  // padded row of the query heads in shared memory (conflict-free float4 reads)
-
-// Head-summed LSE score of candidate c at level l >= 2 over its children's
-// summaries (level l - 1: row offset off1, size M1); lane = (child lane >> 4, head
-// lane & 15).  In decode the query is the newest token, so every existing child is
-// eligible.  Lanes 0..15 return it.  While the rows are in flight, lanes 0..7 ask L1
-// for the rows of c's grandchildren (level l - 2: offset off2, size M2), which are
-// the rows the next level reads for whichever of c's children it keeps.
-template <int G>
-__device__ __forceinline__ float warp_node_score(const float* blk, long long off1, long long M1, long long off2,
-                                                 long long M2, int l, int c, const float* qs, int lane) {
-  const int ch = lane >> 4, h = lane & 15;
-  if (!PISA_IN_BOUNDS(c >= 0 && 2LL * c < M1)) c = 0;
-  const long long node = 2LL * c + ch;
-  const bool two = 2LL * c + 1 < M1;
-  float z = 0.f;
-  if (l >= 3 && lane < 8) {
-    const long long gc = 4LL * c + (lane >> 1);
-    if (gc < M2) {
-      const float* a = blk + (off2 + gc) * kD + (lane & 1) * (kD / 2);
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
-    }
-  }
-  if (h < G && (ch == 0 || two)) {
-    const float4* r = reinterpret_cast<const float4*>(blk + (off1 + node) * kD);
-    const float4* qv = reinterpret_cast<const float4*>(qs + h * kQStride);
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // four chains for latency
-#pragma unroll
-    for (int j = 0; j < kD / 4; ++j) {
-      const float4 k = r[j], q = qv[j];
-      a0 = fmaf(q.x, k.x, a0);
-      a1 = fmaf(q.y, k.y, a1);
-      a2 = fmaf(q.z, k.z, a2);
-      a3 = fmaf(q.w, k.w, a3);
-    }
-    z = ((a0 + a1) + (a2 + a3)) * kScale;
-  }
-  const float z1 = __shfl_xor_sync(kFull, z, 16);
-  float v = (ch == 0 && h < G) ? (two ? lse2(z, z1) : z) : 0.f;
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  return v;
-}
+constexpr int kWalkWarps = 4;  // warps that walk the intermediate levels
+constexpr int kPfThreads = (kDecWarps - kWalkWarps + 1) * 32;  // warp 0 + the other warps, at named barrier 2
 
 // bf16 m16n8k16 MMA with fp32 accumulation (D = A B + C).
 __device__ __forceinline__ void dec_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -166,6 +127,89 @@ __device__ __forceinline__ float warp_leaf_mma(const __nv_bfloat16* keys_b, int 
   return v;
 }
 
+// Scores of candidates 4 tile .. 4 tile + 3 at level l (children at level l - 1, rows1,
+// M1 rows) on mma.sync: the query heads are the A operand (qa, as for the leaf scores), the
+// 8 children rows the B columns (column g: child g & 1 of candidate 4 tile + (g >> 1); a
+// lane takes dims 16 j .. 16 j + 15 of it, the same k order as the A fragments).  The fp32
+// summaries enter as bf16 high and low parts (x = hi + lo to 16 bits), two MMAs per
+// k-step.  After the MMAs lane (g, j) holds heads g and g + 8 of both children of candidate
+// 4 tile + j: the two-child log-sum-exp per head, then the head sum over g.  While the rows
+// are in flight the children's own children (rows2, level l - 2) are asked into L1.
+template <int G>
+__device__ __forceinline__ void tile_node_scores(const float* rows1, long long M1, const float* rows2, long long M2,
+                                                 const int* cand, int nC, int tile, const uint32_t (&qa)[4][4],
+                                                 int lane, float* sc) {
+  const int g = lane >> 2, j = lane & 3;
+  const int cb = 4 * tile + (g >> 1);
+  const int c = cb < nC ? cand[cb] : -1;
+  const long long child = 2LL * c + (g & 1);
+  const bool have = c >= 0 && PISA_IN_BOUNDS(child < M1 || (g & 1));
+  float4 x[4];
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) x[ks] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (have && child < M1) {
+    const float4* r = reinterpret_cast<const float4*>(rows1 + child * kD) + 4 * j;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) x[ks] = r[ks];
+    if (rows2 != nullptr) {
+      const long long gc = 2 * child + (j >> 1);
+      if (gc < M2) asm volatile("prefetch.global.L1 [%0];" ::"l"(rows2 + gc * kD + (j & 1) * (kD / 2)));
+    }
+  }
+  float dh[4] = {0.f, 0.f, 0.f, 0.f}, dl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) {
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(x[ks].x, x[ks].y), h1 = __floats2bfloat162_rn(x[ks].z, x[ks].w);
+    const uint32_t u0 = *reinterpret_cast<const uint32_t*>(&h0), u1 = *reinterpret_cast<const uint32_t*>(&h1);
+    const __nv_bfloat162 l0 = __floats2bfloat162_rn(x[ks].x - __uint_as_float(u0 << 16),
+                                                    x[ks].y - __uint_as_float(u0 & 0xffff0000u));
+    const __nv_bfloat162 l1 = __floats2bfloat162_rn(x[ks].z - __uint_as_float(u1 << 16),
+                                                    x[ks].w - __uint_as_float(u1 & 0xffff0000u));
+    dec_mma(dh, qa[ks], u0, u1);
+    dec_mma(dl, qa[ks], *reinterpret_cast<const uint32_t*>(&l0), *reinterpret_cast<const uint32_t*>(&l1));
+  }
+  const int cj = 4 * tile + j;
+  const int cc = cj < nC ? cand[cj] : -1;
+  const bool two = cc >= 0 && 2LL * cc + 1 < M1;
+  // log(e^z0 + e^z1) = max + log(1 + e^-|z0 - z1|), in base 2 on the exponential unit
+  constexpr float kL2e = 1.4426950408889634f, kLn2 = 0.69314718055994531f;
+  float v = 0.f;
+  if (g < G) {
+    const float z0 = (dh[0] + dl[0]) * kScale, z1 = (dh[1] + dl[1]) * kScale;
+    v += two ? fmaxf(z0, z1) + kLn2 * lg2_approx(1.f + ex2_approx(-fabsf(z0 - z1) * kL2e)) : z0;
+  }
+  if (g + 8 < G) {
+    const float z0 = (dh[2] + dl[2]) * kScale, z1 = (dh[3] + dl[3]) * kScale;
+    v += two ? fmaxf(z0, z1) + kLn2 * lg2_approx(1.f + ex2_approx(-fabsf(z0 - z1) * kL2e)) : z0;
+  }
+  v += __shfl_xor_sync(kFull, v, 4);
+  v += __shfl_xor_sync(kFull, v, 8);
+  v += __shfl_xor_sync(kFull, v, 16);
+  if (g == 0 && cj < nC) sc[cj] = v;
+}
+
+// Candidate i of nC (scores sc) survives iff fewer than K candidates beat it: j beats i
+// when its score is higher, or equal with j < i (the lower node index).  sel[u] is the
+// verdict for i = lane + 32 u; the scores travel by shuffles.
+__device__ __forceinline__ void shuffle_rank(const float* sc, int nC, int K, int lane, bool (&sel)[2]) {
+  const float x0 = lane < nC ? sc[lane] : 0.f;
+  const float x1 = lane + 32 < nC ? sc[lane + 32] : 0.f;
+  int r0 = 0, r1 = 0;
+  const int n0 = min(nC, 32);
+  for (int j = 0; j < n0; ++j) {
+    const float y = __shfl_sync(kFull, x0, j);
+    r0 += (y > x0 || (y == x0 && j < lane));
+    r1 += (y >= x1);  // j < 32 <= lane + 32
+  }
+  for (int j = 32; j < nC; ++j) {
+    const float y = __shfl_sync(kFull, x1, j - 32);
+    r0 += (y > x0);  // j >= 32 > lane
+    r1 += (y > x1 || (y == x1 && j < lane + 32));
+  }
+  sel[0] = lane < nC && r0 < K;
+  sel[1] = lane + 32 < nC && r1 < K;
+}
+
 // One decode step for one (b, kv): append k_new at position p = lengths[b],
 // refresh the leaf mean and its ancestor path, then walk for the query at t = p
 // over the n = p + 1 tokens present.
@@ -175,13 +219,16 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
     __nv_bfloat16* keys, float* summ, int32_t* lengths, Levels cap_lv,
     long long n_cap, int Hq, int Hkv, int K, int32_t* __restrict__ idx, float* __restrict__ scores,
     int* status, int* arrivals) {
-  __shared__ __align__(16) float qs[G * kQStride];
   __shared__ float sib[kMaxLevels + 1][kD];  // siblings along the new token's path
   __shared__ __align__(16) __nv_bfloat16 lk[kC * kD];  // the earlier keys of the new token's leaf
   __shared__ int dcand[kDecWarps][2 * kMaxK];   // each warp's copy of the candidate list
   __shared__ int dnext[kDecWarps][kMaxK];       // each warp's survivor compaction
   __shared__ float dscore[2][2 * kMaxK];        // candidate scores, by level parity
   __shared__ float dnext_s[kMaxK];
+  __shared__ float dleaf[2 * kMaxK];  // leaf scores
+  __shared__ int leaf_nc;             // leaf candidates
+  __shared__ int pf_cand[2 * kMaxK];  // level-2 candidates, whose leaves' keys the other warps ask into L2
+  __shared__ int pf_n;
   const int b = blockIdx.x / Hkv, kv = blockIdx.x % Hkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long p = lengths[b];
@@ -220,9 +267,6 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
 #pragma unroll
     for (int l = 2; l <= kMaxLevels; ++l)
       if (l <= lv.L) sib[l][e] = v[l];
-  } else if (tid >= 64 && tid < 64 + G * kD) {
-    for (int i = tid - 64; i < G * kD; i += kDecWarps * 32 - 64)
-      qs[(i / kD) * kQStride + (i % kD)] = bf2f(q_new[((long long)b * Hq + (long long)kv * G) * kD + i]);
   }
   {  // the leaf's earlier keys, 16 bytes per thread
     const int nprev = (int)(p - leaf * kC);  // 0..63
@@ -260,85 +304,96 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
   __threadfence_block();
   __syncthreads();
 
-  // The walk.  Every warp holds the same survivor list (lane j: the j-th survivor) and
-  // expands it into its own copy of the candidate list; the warps score the candidates
-  // (warp w: candidates w, w + kDecWarps, ...) into a score array shared by the CTA and
-  // double-buffered by level parity; after one barrier every warp ranks the same scores
-  // and compacts the same survivors, so a level costs one barrier.
-  int* cand = dcand[warp];
-  int nS = 1, myS = 0;
-  int par = 0;
-  int nC = 1;
-  if (lv.L == 1) {  // a single leaf, which is the root
-    if (lane == 0) cand[0] = 0;
-    __syncwarp();
-  }
-  for (int l = lv.L - 1; l >= 1; --l) {
-    {  // candidates: the children of the survivors (in decode every existing node is eligible)
-      const bool v0 = lane < nS;
-      const long long c1 = 2LL * myS + 1;
-      const bool v1 = v0 && c1 < lv.M[l];
-      const unsigned b1 = __ballot_sync(kFull, v1);
-      const int pos = lane + __popc(b1 & ((1u << lane) - 1u));
-      nC = nS + __popc(b1);
-      if (v0 && PISA_IN_BOUNDS(pos + (v1 ? 1 : 0) < 2 * kMaxK)) {
-        cand[pos] = 2 * myS;
-        if (v1) cand[pos + 1] = (int)c1;
-      }
+  // The walk, by warps 0 .. kWalkWarps - 1.  Each holds the same survivor list (lane j:
+  // the j-th survivor) and expands it into its own copy of the candidate list; the
+  // candidates are scored four to a warp-tile on mma.sync, into a score array shared by
+  // the walking warps and double-buffered by level parity; after one barrier of the
+  // walking warps every one of them ranks the same scores and compacts the same
+  // survivors.  The other warps wait for the leaf candidates.
+  if (warp < kWalkWarps) {
+    int* cand = dcand[warp];
+    int nS = 1, myS = 0;
+    int par = 0;
+    int nC = 1;
+    bool pf_sent = false;
+    uint32_t qa[4][4];
+    leaf_q_frags<G>(q_new + ((long long)b * Hq + (long long)kv * G) * kD, lane, qa);
+    if (lv.L == 1) {  // a single leaf, which is the root
+      if (lane == 0) cand[0] = 0;
       __syncwarp();
     }
-    if (l == 1) break;
-    if (nC <= K) {  // kept whole, unscored
-      nS = nC;
-      myS = lane < nC ? cand[lane] : 0;
-      __syncwarp();
-      continue;
-    }
-    float* sc = dscore[par];
-    const long long off1 = lv.off[l - 1], M1 = lv.M[l - 1];
-    const long long off2 = l >= 3 ? lv.off[l - 2] : 0, M2 = l >= 3 ? lv.M[l - 2] : 0;
-    for (int ci = warp; ci < nC; ci += kDecWarps) {
-      const int c = cand[ci];
-      if (l == 2) {  // the keys of c's two leaves go to L2 while the level is scored
-        const long long r0 = 128LL * c;
-        for (int r = lane; r < 128; r += 32)
-          if (r0 + r < n) asm volatile("prefetch.global.L2 [%0];" ::"l"(keys_b + ((r0 + r) * Hkv + kv) * kD));
-      }
-      const float v = warp_node_score<G>(blk, off1, M1, off2, M2, l, c, qs, lane);
-      if (lane == 0) sc[ci] = v;
-    }
-    __syncthreads();
-    // rank count over the shared scores (candidate i survives iff fewer than K beat it; j
-    // beats i when its score is higher, or equal with j < i, i.e. the lower node index)
-    bool sel[2] = {false, false};
-    unsigned m[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int ci = lane + 32 * u;
-      if (ci < nC) {
-        const float x = sc[ci];
-        int rank = 0;
-        for (int j = 0; j < nC; ++j) {
-          const float y = sc[j];
-          rank += (y > x || (y == x && j < ci));
+    for (int l = lv.L - 1; l >= 1; --l) {
+      {  // candidates: the children of the survivors (in decode every existing node is eligible)
+        const bool v0 = lane < nS;
+        const long long c1 = 2LL * myS + 1;
+        const bool v1 = v0 && c1 < lv.M[l];
+        const unsigned b1 = __ballot_sync(kFull, v1);
+        const int pos = lane + __popc(b1 & ((1u << lane) - 1u));
+        nC = nS + __popc(b1);
+        if (v0 && PISA_IN_BOUNDS(pos + (v1 ? 1 : 0) < 2 * kMaxK)) {
+          cand[pos] = 2 * myS;
+          if (v1) cand[pos + 1] = (int)c1;
         }
-        sel[u] = rank < K;
+        __syncwarp();
       }
-      m[u] = __ballot_sync(kFull, sel[u]);
+      if (l == 1) break;
+      if (l == 2 && warp == 0) {  // hand the level-2 candidates to the warps that do not walk
+        for (int i = lane; i < nC; i += 32) pf_cand[i] = cand[i];
+        if (lane == 0) pf_n = nC;
+        pf_sent = true;
+        asm volatile("bar.arrive 2, %0;" ::"n"(kPfThreads) : "memory");
+      }
+      if (nC <= K) {  // kept whole, unscored
+        nS = nC;
+        myS = lane < nC ? cand[lane] : 0;
+        __syncwarp();
+        continue;
+      }
+      float* sc = dscore[par];
+      const float* rows1 = blk + lv.off[l - 1] * kD;
+      const float* rows2 = l >= 3 ? blk + lv.off[l - 2] * kD : nullptr;
+      const long long M1 = lv.M[l - 1], M2 = l >= 3 ? lv.M[l - 2] : 0;
+      for (int tile = warp; 4 * tile < nC; tile += kWalkWarps) {
+        tile_node_scores<G>(rows1, M1, rows2, M2, cand, nC, tile, qa, lane, sc);
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kWalkWarps * 32) : "memory");
+      // rank count over the shared scores (candidate i survives iff fewer than K beat it; j
+      // beats i when its score is higher, or equal with j < i, i.e. the lower node index)
+      bool sel[2];
+      shuffle_rank(sc, nC, K, lane, sel);
+      unsigned m[2] = {__ballot_sync(kFull, sel[0]), __ballot_sync(kFull, sel[1])};
+      int* nx = dnext[warp];
+      const unsigned lt = (1u << lane) - 1u;
+      if (sel[0]) nx[__popc(m[0] & lt)] = cand[lane];
+      if (sel[1]) nx[__popc(m[0]) + __popc(m[1] & lt)] = cand[lane + 32];
+      __syncwarp();
+      nS = K;
+      myS = lane < K ? nx[lane] : 0;
+      __syncwarp();
+      par ^= 1;
     }
-    int* nx = dnext[warp];
-    const unsigned lt = (1u << lane) - 1u;
-    if (sel[0]) nx[__popc(m[0] & lt)] = cand[lane];
-    if (sel[1]) nx[__popc(m[0]) + __popc(m[1] & lt)] = cand[lane + 32];
-    __syncwarp();
-    nS = K;
-    myS = lane < K ? nx[lane] : 0;
-    __syncwarp();
-    par ^= 1;
+    if (warp == 0) {
+      if (lane == 0) leaf_nc = nC;  // warp 0's candidate list holds the leaves
+      if (!pf_sent) {  // no level 2 (a tree of one or two levels): nothing to prefetch
+        if (lane == 0) pf_n = 0;
+        asm volatile("bar.arrive 2, %0;" ::"n"(kPfThreads) : "memory");
+      }
+    }
+  } else {
+    // the keys of the level-2 candidates' leaves go to L2 while the walking warps score level 2
+    asm volatile("bar.sync 2, %0;" ::"n"(kPfThreads) : "memory");
+    const int np = pf_n;
+    for (int i = tid - kWalkWarps * 32; i < np * 128; i += (kDecWarps - kWalkWarps) * 32) {
+      const long long r = 128LL * pf_cand[i >> 7] + (i & 127);
+      if (r < n) asm volatile("prefetch.global.L2 [%0];" ::"l"(keys_b + (r * Hkv + kv) * kD));
+    }
   }
-  // leaves: the children of the level-2 survivors (cand holds them), scored exactly when
-  // there are more than K of them or when scores are requested
-  float* sc = dscore[par];
+  __syncthreads();
+  // leaves: the children of the level-2 survivors, scored exactly when there are more than
+  // K of them or when scores are requested
+  const int nC = leaf_nc;
+  const int* cand = dcand[0];
+  float* sc = dleaf;
   if (nC > K || so != nullptr) {
     uint32_t qa[4][4];
     leaf_q_frags<G>(q_new + ((long long)b * Hq + (long long)kv * G) * kD, lane, qa);
@@ -349,26 +404,9 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
   }
   __syncthreads();
   if (warp != 0) return;
-  bool sel[2] = {false, false};
-  unsigned m[2];
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int ci = lane + 32 * u;
-    if (ci < nC) {
-      bool keep = true;
-      if (nC > K) {
-        const float x = sc[ci];
-        int rank = 0;
-        for (int j = 0; j < nC; ++j) {
-          const float y = sc[j];
-          rank += (y > x || (y == x && j < ci));
-        }
-        keep = rank < K;
-      }
-      sel[u] = keep;
-    }
-    m[u] = __ballot_sync(kFull, sel[u]);
-  }
+  bool sel[2] = {lane < nC, lane + 32 < nC};  // K or fewer leaves: all kept
+  if (nC > K) shuffle_rank(sc, nC, K, lane, sel);
+  unsigned m[2] = {__ballot_sync(kFull, sel[0]), __ballot_sync(kFull, sel[1])};
   const unsigned lt = (1u << lane) - 1u;
   int* nx = dnext[0];
   float* nxs = dnext_s;
