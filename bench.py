@@ -41,7 +41,7 @@ MUFU_EX2_PER_CLK_SM = 29.0  # measured ex2.approx throughput per SM and clock on
 KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
                   "walk": ["walk_mma.cu", "tc.cuh", "common.cuh", "api.cuh"]}
 NCU_TRAFFIC = {
-    ("leaf", "latency-256k"): {"bytes": 1770239000 + 34918656, "src_sha1": "d0a6343b4f5dce88e793241dfbb2de98bc6f21bf",
+    ("leaf", "latency-256k"): {"bytes": 1769847000 + 35434752, "src_sha1": "a2ce2416e1fa99897de013ea4f0113386c76571d",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
     ("walk", "latency-256k"): {"bytes": 1076117000 + 34946304, "src_sha1": "fc088a3dad3a4cca1dac24fd34bc7058bf14fb0f",
                                "profile": "profiles/walk_k8s_kernel_latency-256k.md"},
