@@ -2,8 +2,8 @@
 // and ancestor path, and walk the cached pyramid for the newest query.
 // "Block Sparse Attention with Log-Linear Complexity", §5.1 (decoding keeps the
 // mean pyramid cached and touches only the new token's path) and §3.2 / Scoring
-// / §4.1 for the walk.  fp32 arithmetic on the CUDA cores: bf16 inputs, fp32
-// summaries and accumulation.
+// / §4.1 for the walk.  bf16 inputs, fp32 summaries (the path update on the CUDA
+// cores), dot products on mma.sync with fp32 accumulation.
 //
 // One CTA of kDecWarps warps per (b, kv).  Threads 0..63 update the path (one
 // feature each).  Warps 0..kWalkWarps - 1 then walk the intermediate levels: every
