@@ -43,7 +43,7 @@ KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
 NCU_TRAFFIC = {
     ("leaf", "latency-256k"): {"bytes": 1769847000 + 35434752, "src_sha1": "a2ce2416e1fa99897de013ea4f0113386c76571d",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
-    ("walk", "latency-256k"): {"bytes": 1076117000 + 34946304, "src_sha1": "fc088a3dad3a4cca1dac24fd34bc7058bf14fb0f",
+    ("walk", "latency-256k"): {"bytes": 1076089000 + 34977024, "src_sha1": "abe8d19b29004b4127823e9af4a0f696b86f6b4f",
                                "profile": "profiles/walk_k8s_kernel_latency-256k.md"},
 }
 

@@ -124,6 +124,36 @@ def test_decode_steps_match_oracle_and_rebuild():
     assert torch.equal(fresh.summaries, pyr.summaries)
 
 
+
+@pytest.mark.parametrize("G,K", [(1, 1), (2, 3), (4, 16), (8, 32), (16, 32), (16, 1), (1, 32), (4, 8)])
+def test_decode_group_sizes_and_k(G, K):
+    """Decode steps for every supported query-group size and K from 1 to 32 (up
+    to 64 candidates per level, i.e. 16 tiles of four over the walking warps and
+    the second word of the rank), each checked step compared with the oracle's
+    walk of the newest query; a 12000-token context keeps levels of more than 32
+    nodes."""
+    B, Hkv, n_ctx, steps = 2, 2, 12000, 20
+    Hq = G * Hkv
+    n_cap = n_ctx + steps
+    cache, g = synth.decode_context(B, n_ctx, n_cap, Hkv, seed=5 + G + K)
+    pyr = pisa.Pyramid.allocate(cache.to(DEV), with_lengths=True)
+    pisa.build_pyramid(pyr, N=n_ctx)
+    ws = torch.empty(pisa.decode_workspace_bytes(B, Hq, Hkv, K), dtype=torch.uint8, device=DEV)
+    for s in range(steps):
+        qn, kn = synth.decode_step(g, B, Hq, Hkv)
+        idx, sc = pisa.decode_append_and_select(qn.to(DEV), kn.to(DEV), pyr, K, workspace=ws)
+        cache[:, n_ctx + s] = kn
+        if s in (0, 9, steps - 1):
+            torch.cuda.synchronize()
+            assert pisa.check_device_status(ws) == 0
+            lengths = np.full(B, n_ctx + s + 1)
+            st = compare_decode(idx.cpu().numpy(), sc.cpu().numpy(), _f32(qn), _f32(cache), lengths, K)
+            assert st["unexcused"] == 0 and st["score_bad"] == 0, st["messages"]
+    torch.cuda.synchronize()
+    fresh = pisa.build_pyramid(cache.to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(fresh.summaries, pyr.summaries)
+
 def test_decode_full_cache_reports_bounds():
     B, Hq, Hkv, K = 2, 8, 2, 4
     cache, g = synth.decode_context(B, 100, 100, Hkv, seed=3)
