@@ -128,6 +128,28 @@ __device__ __forceinline__ float chunk_exp_sum(const float (&x)[32], int cnt, bo
   return (s0 + s1) + (s2 + s3);
 }
 
+// sum over one full 64-key half (two 32-column chunks x, y) of 2^(x_i log2(e)/8 + nb):
+// both chunks into the same four packed accumulators, reduced once.
+__device__ __forceinline__ float half_exp_sum_full(const float (&x)[32], const float (&y)[32], float nb) {
+  const unsigned long long k2 = f2_pack(kL2e8, kL2e8), n2 = f2_pack(nb, nb);
+  unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    float a, b;
+    f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), k2, n2), a, b);
+    acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(ex2_approx(a), ex2_approx(b)));
+  }
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    float a, b;
+    f2_unpack(f2_fma(f2_pack(y[c], y[c + 1]), k2, n2), a, b);
+    acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(ex2_approx(a), ex2_approx(b)));
+  }
+  float p, q;
+  f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), p, q);
+  return p + q;
+}
+
 // Running masked log-sum-exp of one 64-key half, fed 32 columns at a time.
 // Exponents are taken relative to the half's first key (no max pass); if a
 // chunk would overflow the running sum, the reference moves up to that chunk's
@@ -161,7 +183,7 @@ struct HalfLse {
   __device__ __forceinline__ void first2(const float (&x)[32], const float (&y)[32], int cnt0, int cnt1, bool full) {
     ref = x[0];
     const float nb = -ref * kL2e8;
-    const float t = chunk_exp_sum(x, cnt0, full, nb) + chunk_exp_sum(y, cnt1, full, nb);
+    const float t = full ? half_exp_sum_full(x, y, nb) : chunk_exp_sum(x, cnt0, false, nb) + chunk_exp_sum(y, cnt1, false, nb);
     if (__any_sync(kFull, !(t <= 3.0e38f))) {  // rare: rescale against the half's maximum
       if (!(t <= 3.0e38f)) {
         float m = ref;
@@ -398,6 +420,8 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
     const int tw = warp - 2;
     const int sub = lane / R, row = lane % R;  // tile of the pair and row this lane loads
     int issued = -1;  // last pair this warp issued (for the abort drain)
+    int last_bh = -1, head0 = 0;  // this lane's last (b, kv) and its first head / token row
+    long long row0 = 0;
     for (int pr = tw; pr < my_pairs; pr += 2) {
       const int kt = 2 * pr + sub;
       const bool has = sub < 2 && kt < my_tiles;
@@ -418,8 +442,13 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
       __syncwarp();
       if (live) {
         const long long tq = PISA_IN_BOUNDS((long long)(ent >> 5) < P.N && d.w >= 0) ? (long long)(ent >> 5) : 0;
-        tma_load_3d(sA + (2 * ps + sub) * kTileBytes + row * Gp * 128, &qmap, 0, (d.w % P.Hkv) * G,
-                    (int)((d.w / P.Hkv) * P.N + tq), &a_pair[ps]);
+        if (d.w != last_bh) {
+          last_bh = d.w;
+          head0 = (d.w % P.Hkv) * G;
+          row0 = (long long)(d.w / P.Hkv) * P.N;
+        }
+        tma_load_3d(sA + (2 * ps + sub) * kTileBytes + row * Gp * 128, &qmap, 0, head0, (int)(row0 + tq),
+                    &a_pair[ps]);
       }
       issued = pr;
     }
@@ -456,9 +485,12 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
       // the previous tile's head sums and store, while the loads are in flight
       {
         float a0 = pv0, a1 = pv1;
-        for (int o = Gp >> 1; o > 0; o >>= 1) {
-          a0 += __shfl_xor_sync(kFull, a0, o);
-          a1 += __shfl_xor_sync(kFull, a1, o);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+          if (o < Gp) {
+            a0 += __shfl_xor_sync(kFull, a0, o);
+            a1 += __shfl_xor_sync(kFull, a1, o);
+          }
         }
         if (pout) {
           pout[0] = a0;
@@ -466,14 +498,12 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
         }
       }
       const int tp = d.z, tbh = d.w;
-      const long long t = ent >> 5;
+      const int t = (int)(ent >> 5);  // < 2^27
       const int qslot = ent & 31;
+      const int Ni = (int)P.N;
       // keys of this tile that count for the query: [128p, n_eff)
-      const long long n_eff = P.causal ? (t + 1 < P.N ? t + 1 : P.N) : P.N;
-      long long lim = qvalid ? n_eff - 128LL * tp : 128;
-      if (lim > 128) lim = 128;
-      if (lim < 1) lim = 1;
-      const int l = (int)lim;  // columns [0, l) count
+      const int n_eff = P.causal ? min(t + 1, Ni) : Ni;
+      const int l = qvalid ? max(1, min(128, n_eff - 128 * tp)) : 128;  // columns [0, l) count
       const int c0 = min(l, 32), c1 = min(max(l - 32, 0), 32), c2 = min(max(l - 64, 0), 32),
                 c3 = max(l - 96, 0);
       using Acc = typename std::conditional<MODE == 0, HalfLse, HalfMom<MODE>>::type;
@@ -495,17 +525,20 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
       if (any1) h1.first2(xa, xb, c2 > 0 ? c2 : 1, c3, __all_sync(kFull, l == 128));
       pv1 = (head && any1) ? h1.value() : 0.f;
       pout = nullptr;
-      if (qvalid && h == 0 && PISA_IN_BOUNDS(t < P.N && (P.flat || qslot < P.K))) {
-        pout = P.flat ? P.leaf_scores + ((long long)tbh * P.N + t) * P.flat_stride + 2 * tp
-                      : P.leaf_scores + ((long long)tbh * P.N + t) * (2 * P.K) + 2 * qslot;
+      if (qvalid && h == 0 && PISA_IN_BOUNDS(t < Ni && (P.flat || qslot < P.K))) {
+        const long long job = (long long)tbh * Ni + t;
+        pout = P.flat ? P.leaf_scores + job * P.flat_stride + 2 * tp : P.leaf_scores + job * (2 * P.K) + 2 * qslot;
         if (l <= 64) pv1 = -INFINITY;  // the second leaf starts after the query
       }
     }
     {  // the last tile's head sums and store
       float a0 = pv0, a1 = pv1;
-      for (int o = Gp >> 1; o > 0; o >>= 1) {
-        a0 += __shfl_xor_sync(kFull, a0, o);
-        a1 += __shfl_xor_sync(kFull, a1, o);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) {
+        if (o < Gp) {
+          a0 += __shfl_xor_sync(kFull, a0, o);
+          a1 += __shfl_xor_sync(kFull, a1, o);
+        }
       }
       if (pout) {
         pout[0] = a0;
