@@ -787,46 +787,61 @@ __global__ void leaf_final8_kernel(const int32_t* __restrict__ surv, const float
   }
 }
 
-// Jobs (b * Hkv + kv) * N + t for t in [t0, t1).
-__global__ void leaf_final_kernel(const int32_t* __restrict__ surv, const float* __restrict__ leaf_scores,
-                                  long long t0, long long t1, int BH, long long N, int K, int32_t* __restrict__ idx,
-                                  float* __restrict__ scores) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (t1 - t0) * BH) return;
-  const long long job = (i / (t1 - t0)) * N + t0 + i % (t1 - t0);
-  const int32_t* s2 = surv + job * K;
+// Final Top-K of the leaf stage for any K <= 32: one warp per (b, kv, t).  Lane l holds
+// survivor slot l and its two leaves (the second absent when its score is -inf: past
+// the query or past the last token); the candidates' order is the walk's (node order).
+// The scores go to shared memory in that order, each lane ranks its two candidates
+// against all of them (j beats i when its score is higher, or equal with j before i),
+// and the kept ones are written in candidate order, then -1 / -inf padding.
+constexpr int kFinalWarps = 4;
+__global__ void __launch_bounds__(kFinalWarps * 32) leaf_final_kernel(
+    const int32_t* __restrict__ surv, const float* __restrict__ leaf_scores, long long t0, long long t1, int BH,
+    long long N, int K, int32_t* __restrict__ idx, float* __restrict__ scores) {
+  __shared__ float sh[kFinalWarps][2 * kMaxK];
+  const int lane = threadIdx.x & 31, wb = threadIdx.x >> 5;
+  const long long span = t1 - t0;
+  const long long wid = (long long)blockIdx.x * kFinalWarps + wb;
+  if (wid >= span * BH) return;  // warp-uniform
+  const long long job = (wid / span) * N + t0 + wid % span;
+  const int p = lane < K ? __ldg(surv + job * K + lane) : -1;
   const float* ls = leaf_scores + job * 2 * K;
-  int cid[2 * kMaxK];
-  float csc[2 * kMaxK];
-  int nC = 0;
-  for (int j = 0; j < K; ++j) {
-    const int p = s2[j];
-    if (p < 0) break;
-    cid[nC] = 2 * p;
-    csc[nC++] = ls[2 * j];
-    const float s1 = ls[2 * j + 1];
-    if (s1 != -INFINITY) {
-      cid[nC] = 2 * p + 1;
-      csc[nC++] = s1;
+  const bool va = p >= 0;
+  const float sa = va ? __ldg(ls + 2 * lane) : -INFINITY;
+  const float sb = va ? __ldg(ls + 2 * lane + 1) : -INFINITY;
+  const bool vb = va && sb != -INFINITY;
+  const unsigned lt = (1u << lane) - 1u;
+  const unsigned ma = __ballot_sync(kFull, va), mb = __ballot_sync(kFull, vb);
+  const int pa = __popc(ma & lt) + __popc(mb & lt);  // position of this lane's first leaf
+  const int nC = __popc(ma) + __popc(mb);
+  float* sw = sh[wb];
+  if (va) sw[pa] = sa;
+  if (vb) sw[pa + 1] = sb;
+  __syncwarp();
+  bool ka = va, kb = vb;
+  if (nC > K) {
+    int ra = 0, rb = 0;
+    for (int j = 0; j < nC; ++j) {
+      const float y = sw[j];
+      ra += (y > sa) || (y == sa && j < pa);
+      rb += (y > sb) || (y == sb && j < pa + 1);
     }
+    ka = va && ra < K;
+    kb = vb && rb < K;
   }
+  const unsigned ka_m = __ballot_sync(kFull, ka), kb_m = __ballot_sync(kFull, kb);
+  const int oa = __popc(ka_m & lt) + __popc(kb_m & lt);
+  const int nOut = __popc(ka_m) + __popc(kb_m);
   int32_t* io = idx + job * K;
   float* so = scores ? scores + job * K : nullptr;
-  int w = 0;
-  for (int i = 0; i < nC; ++i) {
-    bool keep = true;
-    if (nC > K) {
-      int rank = 0;
-      for (int j = 0; j < nC; ++j) rank += (csc[j] > csc[i]) || (csc[j] == csc[i] && j < i);
-      keep = rank < K;
-    }
-    if (keep) {
-      io[w] = cid[i];
-      if (so) so[w] = csc[i];
-      ++w;
-    }
+  if (ka && PISA_IN_BOUNDS(oa < K)) {
+    io[oa] = 2 * p;
+    if (so) so[oa] = sa;
   }
-  for (; w < K; ++w) {
+  if (kb && PISA_IN_BOUNDS(oa + (ka ? 1 : 0) < K)) {
+    io[oa + (ka ? 1 : 0)] = 2 * p + 1;
+    if (so) so[oa + (ka ? 1 : 0)] = sb;
+  }
+  for (int w = nOut + lane; w < K; w += 32) {
     io[w] = -1;
     if (so) so[w] = -INFINITY;
   }
@@ -968,8 +983,8 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
     leaf_final8_kernel<<<(unsigned)((BH * span + 127) / 128), 128, 0, s>>>(L.surv, L.leaf_scores, L.t0, L.t1, BH,
                                                                           L.N, L.idx, L.scores);
   else
-    leaf_final_kernel<<<(unsigned)((BH * span + 127) / 128), 128, 0, s>>>(L.surv, L.leaf_scores, L.t0, L.t1, BH, L.N,
-                                                                         L.K, L.idx, L.scores);
+    leaf_final_kernel<<<(unsigned)((BH * span + kFinalWarps - 1) / kFinalWarps), kFinalWarps * 32, 0, s>>>(
+        L.surv, L.leaf_scores, L.t0, L.t1, BH, L.N, L.K, L.idx, L.scores);
   note_launch();
   e = cudaGetLastError();
   mark_phase(5, s);
