@@ -41,7 +41,7 @@ MUFU_EX2_PER_CLK_SM = 29.0  # measured ex2.approx throughput per SM and clock on
 KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
                   "walk": ["walk_mma.cu", "tc.cuh", "common.cuh", "api.cuh"]}
 NCU_TRAFFIC = {
-    ("leaf", "latency-256k"): {"bytes": 1768049000 + 35337472, "src_sha1": "383de7af4fe6a2a6af854636a837c16e76634e84",
+    ("leaf", "latency-256k"): {"bytes": 1767983000 + 34985984, "src_sha1": "c9a3e2dcc05b3215104608cbcc98fff61d06c8f6",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
     ("walk", "latency-256k"): {"bytes": 1076089000 + 34977024, "src_sha1": "abe8d19b29004b4127823e9af4a0f696b86f6b4f",
                                "profile": "profiles/walk_k8s_kernel_latency-256k.md"},
