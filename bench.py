@@ -33,6 +33,8 @@ METRIC = "selection ms/pass and query-rows/s at 32K–256K; % of roofline (1×GB
 UNIT = "query-rows/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 MUFU_EX2_PER_CLK_SM = 29.0  # measured ex2.approx throughput per SM and clock on GB300 (probe, 1 GPU)
+kC_TOKENS = 64  # tokens per leaf (C)
+L2_GATHER_TBS = 11.6  # measured rate of random 256-byte gathers served by L2 on GB300 (probe, 1 GPU), TB/s
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # kernels that can dominate a pass, from one ncu capture of the workload named
@@ -365,10 +367,13 @@ def run_ours(args):
     # exponentials at the exponential unit's rate measured on this GPU (ex2 ~29 per clock
     # per SM, 152 SMs at 2.07 GHz)
     t_exp = alg["exps"] / (MUFU_EX2_PER_CLK_SM * 152 * 2.07e9) * 1e3
+    # and the leaf stage's query-row gathers at the measured L2 random-gather rate
+    t_l2 = alg["leaf_row_gather_bytes"] / (L2_GATHER_TBS * 1e12) * 1e3
     pass_roof = {"flops": alg["flops"], "min_bytes": alg["bytes"], "t_tensor_ms": t_tensor, "t_hbm_ms": t_hbm,
                  "t_roofline_ms": max(t_tensor, t_hbm), "frac": max(t_tensor, t_hbm) / ms_step,
                  "peaks": f"{pk_kind}: {tf_peak} TFLOP/s bf16 burst, {pk['hbm_gbs']} GB/s",
-                 "t_exp_ms": t_exp, "frac_with_exp_bound": max(t_tensor, t_hbm, t_exp) / ms_step}
+                 "t_exp_ms": t_exp, "t_l2_gather_ms": t_l2,
+                 "frac_with_exp_bound": max(t_tensor, t_hbm, t_exp) / ms_step}
 
     # end to end through the public API with host buffers (pinned): every step copies K and
     # Q in and the indices out (pisa_select_prefill_host overlaps the copies with the
@@ -632,9 +637,17 @@ def bench_decode(torch, pisa, synth, dev, args):
     graph.replay()
     ee.record(stream)
     torch.cuda.synchronize()
+    # byte floor of a step: per (sequence, KV head) the keys of the 2K leaf candidates, the children
+    # rows of 2K candidates at each scored level (fp32 summaries) and the path's siblings and new
+    # means, at the HBM copy rate
+    levels = len(level_sizes(n_ctx + 1))
+    per_bh = 2 * K * kC_TOKENS * 64 * 2 + (levels - 2) * 2 * (2 * K) * 64 * 4 + 2 * levels * 64 * 4
+    step_bytes = B * Hkv * per_bh
     return {"us_per_step": us_eager, "us_per_step_graph": es.elapsed_time(ee) * 1000.0 / steps, "steps": steps,
             "B": B, "n_ctx": n_ctx, "Hq": Hq, "Hkv": Hkv, "K": K, "status": st,
-            "status_graph": pisa.check_device_status(ws)}
+            "status_graph": pisa.check_device_status(ws),
+            "bytes_per_step_model": step_bytes,
+            "byte_floor_us": step_bytes / (peaks()[0]["hbm_gbs"] * 1e9) * 1e6}
 
 
 def main():
