@@ -243,13 +243,10 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
     return;
   }
   const long long n = p + 1;
-  Levels lv;
-  lv.L = num_levels_for(n);
-  lv.total = cap_lv.total;
-  for (int l = 0; l <= lv.L; ++l) {
-    lv.M[l] = (int)level_size_for(n, l);
-    lv.off[l] = cap_lv.off[l];
-  }
+  // level sizes for the n tokens present (shifts), row offsets from the capacity layout
+  const int Ln = num_levels_for(n);
+  auto Mof = [n](int l) -> long long { return level_size_for(n, l); };
+  auto Oof = [&cap_lv](int l) -> long long { return cap_lv.off[l]; };
   __nv_bfloat16* keys_b = keys + (long long)b * n_cap * Hkv * kD;
   float* blk = summ + ((long long)b * Hkv + kv) * cap_lv.total * kD;
   const long long leaf = p >> kLog2C;
@@ -262,11 +259,11 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
 #pragma unroll
     for (int l = 2; l <= kMaxLevels; ++l) {
       const long long s = (leaf >> (l - 2)) ^ 1;
-      v[l] = (l <= lv.L && s < lv.M[l - 1]) ? blk[(lv.off[l - 1] + s) * kD + e] : 0.f;
+      v[l] = (l <= Ln && s < Mof(l - 1)) ? blk[(Oof(l - 1) + s) * kD + e] : 0.f;
     }
 #pragma unroll
     for (int l = 2; l <= kMaxLevels; ++l)
-      if (l <= lv.L) sib[l][e] = v[l];
+      if (l <= Ln) sib[l][e] = v[l];
   }
   {  // the leaf's earlier keys, 16 bytes per thread
     const int nprev = (int)(p - leaf * kC);  // 0..63
@@ -287,18 +284,18 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
     for (int r = 0; r < (int)(p - leaf * kC); ++r) acc = __fadd_rn(acc, bf2f(lk[r * kD + e]));
     acc = __fadd_rn(acc, bf2f(kn));
     float m = div_count(acc, (int)(p - leaf * kC + 1));
-    blk[(lv.off[1] + leaf) * kD + e] = m;
+    blk[(Oof(1) + leaf) * kD + e] = m;
     long long i = leaf;
-    for (int l = 2; l <= lv.L; ++l) {
+    for (int l = 2; l <= Ln; ++l) {
       const long long child = i;
       i >>= 1;
       const long long c0 = 2 * i, c1 = 2 * i + 1;
       const int n0 = node_count(l - 1, c0, n);
-      const int n1 = c1 < lv.M[l - 1] ? node_count(l - 1, c1, n) : 0;
+      const int n1 = c1 < Mof(l - 1) ? node_count(l - 1, c1, n) : 0;
       const float m0 = c0 == child ? m : sib[l][e];
       const float m1 = n1 > 0 ? (c1 == child ? m : sib[l][e]) : 0.f;
       m = merge_mean(m0, n0, m1, n1);
-      blk[(lv.off[l] + i) * kD + e] = m;
+      blk[(Oof(l) + i) * kD + e] = m;
     }
   }
   __threadfence_block();
@@ -318,15 +315,15 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
     bool pf_sent = false;
     uint32_t qa[4][4];
     leaf_q_frags<G>(q_new + ((long long)b * Hq + (long long)kv * G) * kD, lane, qa);
-    if (lv.L == 1) {  // a single leaf, which is the root
+    if (Ln == 1) {  // a single leaf, which is the root
       if (lane == 0) cand[0] = 0;
       __syncwarp();
     }
-    for (int l = lv.L - 1; l >= 1; --l) {
+    for (int l = Ln - 1; l >= 1; --l) {
       {  // candidates: the children of the survivors (in decode every existing node is eligible)
         const bool v0 = lane < nS;
         const long long c1 = 2LL * myS + 1;
-        const bool v1 = v0 && c1 < lv.M[l];
+        const bool v1 = v0 && c1 < Mof(l);
         const unsigned b1 = __ballot_sync(kFull, v1);
         const int pos = lane + __popc(b1 & ((1u << lane) - 1u));
         nC = nS + __popc(b1);
@@ -350,9 +347,9 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
         continue;
       }
       float* sc = dscore[par];
-      const float* rows1 = blk + lv.off[l - 1] * kD;
-      const float* rows2 = l >= 3 ? blk + lv.off[l - 2] * kD : nullptr;
-      const long long M1 = lv.M[l - 1], M2 = l >= 3 ? lv.M[l - 2] : 0;
+      const float* rows1 = blk + Oof(l - 1) * kD;
+      const float* rows2 = l >= 3 ? blk + Oof(l - 2) * kD : nullptr;
+      const long long M1 = Mof(l - 1), M2 = l >= 3 ? Mof(l - 2) : 0;
       for (int tile = warp; 4 * tile < nC; tile += kWalkWarps) {
         tile_node_scores<G>(rows1, M1, rows2, M2, cand, nC, tile, qa, lane, sc);
       }
