@@ -231,6 +231,8 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
   __shared__ int pf_n;
   const int b = blockIdx.x / Hkv, kv = blockIdx.x % Hkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t qa[4][4];  // the walking warps' query fragments, requested before anything else
+  if (warp < kWalkWarps) leaf_q_frags<G>(q_new + ((long long)b * Hq + (long long)kv * G) * kD, lane, qa);
   const long long p = lengths[b];
   int32_t* io = idx + (long long)blockIdx.x * K;
   float* so = scores ? scores + (long long)blockIdx.x * K : nullptr;
@@ -313,8 +315,6 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
     int par = 0;
     int nC = 1;
     bool pf_sent = false;
-    uint32_t qa[4][4];
-    leaf_q_frags<G>(q_new + ((long long)b * Hq + (long long)kv * G) * kD, lane, qa);
     if (Ln == 1) {  // a single leaf, which is the root
       if (lane == 0) cand[0] = 0;
       __syncwarp();
