@@ -97,26 +97,9 @@ __device__ __forceinline__ void leaf_abort(volatile int* abort, int* status) {
 constexpr float kL2e8 = 0.18033688011112042f;  // log2(e) / sqrt(64)
 
 // sum_{i < cnt} 2^(x_i * log2(e)/8 + nb) over one 32-column chunk of raw q.k dot
-// products (nb = -ref * log2(e)/8 for the half's reference logit ref).  `full`
-// (warp-uniform) means every lane has cnt == 32: packed f32x2 arithmetic, one
-// fma.f32x2 and one add.f32x2 per two keys into four pair accumulators.
-__device__ __forceinline__ float chunk_exp_sum(const float (&x)[32], int cnt, bool full, float nb) {
-  if (full) {
-    const unsigned long long k2 = f2_pack(kL2e8, kL2e8), n2 = f2_pack(nb, nb);
-    unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-    for (int c = 0; c < 32; c += 2) {
-      float a, b;
-      f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), k2, n2), a, b);
-      acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(ex2_approx(a), ex2_approx(b)));
-    }
-    float p0, p1, p2, p3, p4, p5, p6, p7;
-    f2_unpack(acc[0], p0, p1);
-    f2_unpack(acc[1], p2, p3);
-    f2_unpack(acc[2], p4, p5);
-    f2_unpack(acc[3], p6, p7);
-    return ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7));
-  }
+// products (nb = -ref * log2(e)/8 for the half's reference logit ref), for halves
+// that some lane does not have in full (the causal edge): four scalar accumulators.
+__device__ __forceinline__ float chunk_exp_sum(const float (&x)[32], int cnt, float nb) {
   float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
   for (int c = 0; c < 32; c += 4) {
@@ -129,7 +112,8 @@ __device__ __forceinline__ float chunk_exp_sum(const float (&x)[32], int cnt, bo
 }
 
 // sum over one full 64-key half (two 32-column chunks x, y) of 2^(x_i log2(e)/8 + nb):
-// both chunks into the same four packed accumulators, reduced once.
+// packed f32x2 arithmetic (one fma.f32x2 and one add.f32x2 per two keys), both chunks
+// into the same four pair accumulators, reduced once.
 __device__ __forceinline__ float half_exp_sum_full(const float (&x)[32], const float (&y)[32], float nb) {
   const unsigned long long k2 = f2_pack(kL2e8, kL2e8), n2 = f2_pack(nb, nb);
   unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
@@ -150,40 +134,18 @@ __device__ __forceinline__ float half_exp_sum_full(const float (&x)[32], const f
   return p + q;
 }
 
-// Running masked log-sum-exp of one 64-key half, fed 32 columns at a time.
-// Exponents are taken relative to the half's first key (no max pass); if a
-// chunk would overflow the running sum, the reference moves up to that chunk's
-// maximum and the sum so far is rescaled.
+// Masked log-sum-exp of one 64-key half (one leaf) from two 32-column chunks.
+// Exponents are taken relative to the half's first key (no max pass); if the sum
+// would overflow, the reference moves up to the half's maximum and the sum is
+// taken again.
 struct HalfLse {
   float ref, s;
-  __device__ __forceinline__ void first(const float (&x)[32], int cnt, bool full) {
-    ref = x[0];
-    s = 0.f;
-    add(x, cnt, full);
-  }
-  __device__ __forceinline__ void add(const float (&x)[32], int cnt, bool full) {
-    const float t = s + chunk_exp_sum(x, cnt, full, -ref * kL2e8);
-    if (__any_sync(kFull, !(t <= 3.0e38f))) {  // rare: rescale against the chunk maximum
-      if (!(t <= 3.0e38f)) {
-        float m = ref;
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (c < cnt) m = fmaxf(m, x[c]);
-        s = s * ex2_approx((ref - m) * kL2e8) + chunk_exp_sum(x, cnt, false, -m * kL2e8);
-        ref = m;
-      } else {
-        s = t;
-      }
-    } else {
-      s = t;
-    }
-  }
   // One 64-key half from two 32-column chunks (cnt0 + cnt1 keys, cnt0 >= 1); `full`
   // (warp-uniform) means every lane has 64: one overflow vote for the half.
   __device__ __forceinline__ void first2(const float (&x)[32], const float (&y)[32], int cnt0, int cnt1, bool full) {
     ref = x[0];
     const float nb = -ref * kL2e8;
-    const float t = full ? half_exp_sum_full(x, y, nb) : chunk_exp_sum(x, cnt0, false, nb) + chunk_exp_sum(y, cnt1, false, nb);
+    const float t = full ? half_exp_sum_full(x, y, nb) : chunk_exp_sum(x, cnt0, nb) + chunk_exp_sum(y, cnt1, nb);
     if (__any_sync(kFull, !(t <= 3.0e38f))) {  // rare: rescale against the half's maximum
       if (!(t <= 3.0e38f)) {
         float m = ref;
@@ -192,7 +154,7 @@ struct HalfLse {
           if (c < cnt0) m = fmaxf(m, x[c]);
           if (c < cnt1) m = fmaxf(m, y[c]);
         }
-        s = chunk_exp_sum(x, cnt0, false, -m * kL2e8) + chunk_exp_sum(y, cnt1, false, -m * kL2e8);
+        s = chunk_exp_sum(x, cnt0, -m * kL2e8) + chunk_exp_sum(y, cnt1, -m * kL2e8);
         ref = m;
       } else {
         s = t;
