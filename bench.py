@@ -43,7 +43,7 @@ L2_GATHER_TBS = 11.6  # measured rate of random 256-byte gathers served by L2 on
 KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
                   "walk": ["walk_mma.cu", "tc.cuh", "common.cuh", "api.cuh"]}
 NCU_TRAFFIC = {
-    ("leaf", "latency-256k"): {"bytes": 1767983000 + 34985984, "src_sha1": "c9a3e2dcc05b3215104608cbcc98fff61d06c8f6",
+    ("leaf", "latency-256k"): {"bytes": 1768698000 + 35501568, "src_sha1": "23e2418b8dbf322b555b5553202c5221699c08e2",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
     ("walk", "latency-256k"): {"bytes": 1076089000 + 34977024, "src_sha1": "abe8d19b29004b4127823e9af4a0f696b86f6b4f",
                                "profile": "profiles/walk_k8s_kernel_latency-256k.md"},
