@@ -47,3 +47,24 @@ def test_forward_on_the_selection():
     pyr = pisa.build_pyramid(k.to(DEV))
     idx, _ = pisa.select_prefill(q.to(DEV), pyr, w["K"], with_scores=False)
     _check(q, k, v, idx.cpu(), np.arange(0, w["N"], 5), True)
+
+
+def test_forward_at_full_size_sampled():
+    """Stage two at the benchmark's own size (256K tokens, the pass's selection, the
+    launch configuration the benchmark times), checked at a seeded sample of positions
+    plus the last 64."""
+    q, k, w = synth.make("latency-256k")
+    _, v = synth.iid(1, w["N"], w["Hq"], w["Hkv"], seed=77)
+    qd, kd = q.to(DEV), k.to(DEV)
+    pyr = pisa.build_pyramid(kd)
+    idx, _ = pisa.select_prefill(qd, pyr, w["K"], with_scores=False)
+    got = pisa.sparse_attention(qd, kd, v.to(DEV), idx, causal=True)
+    rng = np.random.default_rng(7)
+    N = w["N"]
+    t = np.unique(np.concatenate([rng.choice(N - 64, 2048, replace=False), np.arange(N - 64, N)]))
+    tt = torch.from_numpy(t).to(DEV)
+    got_t = got[:, tt].cpu().numpy()
+    idx_t = idx[:, :, tt].cpu().numpy()
+    del got
+    want = oracle.attention(q[:, t].float().numpy(), k.float().numpy(), v.float().numpy(), idx_t, t, causal=True)
+    np.testing.assert_allclose(got_t, want, rtol=1e-2, atol=1e-2)
