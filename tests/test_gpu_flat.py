@@ -62,6 +62,18 @@ def test_flat_latency_32k_sampled():
     _ok(st)
 
 
+def test_flat_latency_256k_sampled():
+    """The flat selector at the largest benchmark size (4096 leaves per query), sampled."""
+    q, k, w = synth.make("latency-256k")
+    idx, sc = _run_flat(q, k, w["K"])
+    N = w["N"]
+    rng = np.random.default_rng(11)
+    t = np.unique(np.concatenate([rng.choice(N - 64, 512, replace=False), np.arange(N - 64, N)]))
+    st = compare_flat(idx[:, :, t], sc[:, :, t], _f32(q[:, t]), _f32(k), t, w["K"])
+    record("flat latency-256k (sampled)", st)
+    _ok(st)
+
+
 def test_flat_equals_pyramid_when_every_leaf_reaches_the_leaf_level():
     """M_2 <= K: the walk scores every eligible leaf, exactly like the flat selector."""
     q, k = synth.iid(1, 2048, 32, 2, seed=23)  # M_2 = 16
