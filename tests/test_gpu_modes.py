@@ -54,6 +54,20 @@ def test_prefill_modes_ragged_structured(mode):
 
 
 @pytest.mark.parametrize("mode", [1, 2])
+def test_prefill_modes_at_256k_sampled(mode):
+    """The score modes at the benchmark's largest size (the launch configuration the
+    benchmark times for them), compared at a seeded sample of positions plus the last 1024."""
+    q, k, w = synth.make("latency-256k")
+    idx, sc = _prefill(q, k, w["K"], mode)
+    N = w["N"]
+    rng = np.random.default_rng(3 + mode)
+    t = np.unique(np.concatenate([rng.choice(N - 1024, 8192, replace=False), np.arange(N - 1024, N)]))
+    st = compare_prefill(idx[:, :, t], sc[:, :, t], _f32(q[:, t]), _f32(k), t, w["K"], mode=mode)
+    record(f"latency-256k mode {mode} (sampled)", st)
+    _ok(st)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
 def test_flat_modes(mode):
     q, k = synth.iid(1, 2000, 16, 1, seed=37)
     pyr = pisa.Pyramid.allocate(k.to(DEV))
