@@ -389,27 +389,39 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
           nS = nC;
           if (lane < nC) S.sel[lane] = lane;
         } else {
-          bool keep[2];
-          unsigned m[2];
+          // rank keys: the score's bits made order-preserving as an unsigned, the low six bits
+          // replaced by 63 - candidate index (ties, and scores within 2^-17 relative, go to the
+          // lower index); slots past nC hold 0, below every key
+          unsigned* keys = reinterpret_cast<unsigned*>(S.score);
+          unsigned ky[2];
 #pragma unroll
           for (int s2 = 0; s2 < 2; ++s2) {
             const int ci = lane + 32 * s2;
-            keep[s2] = false;
+            ky[s2] = 0u;
             if (ci < nC) {
-              const float sc = S.score[ci];
-              int rank = 0;
-              const float4* s4 = reinterpret_cast<const float4*>(S.score);
-              for (int q4 = 0; q4 * 4 < nC; ++q4) {
-                const float4 o = s4[q4];
-                const int q = 4 * q4;
-                rank += (q < nC && (o.x > sc || (o.x == sc && q < ci)));
-                rank += (q + 1 < nC && (o.y > sc || (o.y == sc && q + 1 < ci)));
-                rank += (q + 2 < nC && (o.z > sc || (o.z == sc && q + 2 < ci)));
-                rank += (q + 3 < nC && (o.w > sc || (o.w == sc && q + 3 < ci)));
-              }
-              keep[s2] = rank < K;
+              const unsigned fb = __float_as_uint(S.score[ci]);
+              ky[s2] = ((fb ^ ((unsigned)((int)fb >> 31) | 0x80000000u)) & ~63u) | (unsigned)(63 - ci);
             }
-            m[s2] = __ballot_sync(kFull, keep[s2]);
+          }
+          __syncwarp();
+          const int nC4 = (nC + 3) & ~3;
+          if (lane < nC4) keys[lane] = ky[0];
+          if (lane + 32 < nC4) keys[lane + 32] = ky[1];
+          __syncwarp();
+          bool keep[2];
+          unsigned m[2];
+          {
+            int r0 = 0, r1 = 0;
+            const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+            for (int q4 = 0; q4 * 4 < nC; ++q4) {
+              const uint4 o = k4[q4];
+              r0 += (o.x > ky[0]) + (o.y > ky[0]) + (o.z > ky[0]) + (o.w > ky[0]);
+              r1 += (o.x > ky[1]) + (o.y > ky[1]) + (o.z > ky[1]) + (o.w > ky[1]);
+            }
+            keep[0] = lane < nC && r0 < K;
+            keep[1] = lane + 32 < nC && r1 < K;
+            m[0] = __ballot_sync(kFull, keep[0]);
+            m[1] = __ballot_sync(kFull, keep[1]);
           }
           const unsigned lt = (1u << lane) - 1u;
           if (keep[0]) S.sel[__popc(m[0] & lt)] = lane;
