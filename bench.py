@@ -45,7 +45,7 @@ KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
 NCU_TRAFFIC = {
     ("leaf", "latency-256k"): {"bytes": 1768698000 + 35501568, "src_sha1": "23e2418b8dbf322b555b5553202c5221699c08e2",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
-    ("walk", "latency-256k"): {"bytes": 1076089000 + 34977024, "src_sha1": "abe8d19b29004b4127823e9af4a0f696b86f6b4f",
+    ("walk", "latency-256k"): {"bytes": 1076220000 + 34937344, "src_sha1": "f212ac6467192b5341354319d6225fab4d530aa6",
                                "profile": "profiles/walk_k8s_kernel_latency-256k.md"},
 }
 
