@@ -76,19 +76,6 @@ __device__ __forceinline__ int tile_of(int k) {
   return (blockIdx.x + gridDim.x * (k / kTileBlock)) * kTileBlock + (k % kTileBlock);
 }
 
-// Largest bucket whose first tile is <= tile (tile_off is non-decreasing).
-__device__ __forceinline__ int find_bucket(const int* tile_off, int nb, int tile) {
-  int lo = 0, hi = nb - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(tile_off + mid) <= tile)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  return lo;
-}
-
 __device__ __forceinline__ void leaf_abort(volatile int* abort, int* status) {
   *abort = 1;
   set_status(status, PISA_ERR_DEVICE_TIMEOUT);
@@ -520,27 +507,43 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
 
 // Buckets are chunk-major, (query chunk, b * Hkv + kv, level-2 node p), so that the buckets
 // and tiles of a run of query chunks are contiguous.
-__device__ __forceinline__ int bucket_of(long long job, int p, long long N, int BH, int chunk_shift, int M2) {
-  const long long t = job % N;
-  const long long bkv = job / N;
-  return (int)(((t >> chunk_shift) * BH + bkv) * M2 + p);
-}
 
-// Entries of query positions [t0, t1) of every (b, kv): e = ((b * Hkv + kv) * N + t) * K + slot.
-__global__ void leaf_scatter_kernel(const int32_t* __restrict__ surv, long long t0, long long t1, int BH, int K,
-                                    long long N, int chunk_shift, int M2, const int* __restrict__ bucket_off,
-                                    const int32_t* __restrict__ srank, uint32_t* __restrict__ list) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long per_bh = (t1 - t0) * K;
-  if (i >= per_bh * BH) return;
-  const long long e = ((i / per_bh) * N + t0) * K + i % per_bh;
-  const int p = surv[e];
-  if (p < 0) return;
-  const long long job = e / K;
-  const int bkt = bucket_of(job, p, N, BH, chunk_shift, M2);
-  const int pos = bucket_off[bkt] + srank[e];
-  if (!PISA_IN_BOUNDS(pos >= 0 && pos < (long long)BH * N * K)) return;
-  list[pos] = ((uint32_t)(job % N) << 5) | (uint32_t)(e % K);
+// Entries of query positions [t0, t0 + span) of (b, kv) = blockIdx.y, entry
+// e = ((b * Hkv + kv) * N + t) * K + slot.  Each thread takes kScatterItems entries
+// a block apart and issues all their loads before any store, so that the dependent
+// round trips (survivor, then its bucket's offset) of several entries overlap.
+// (Every index fits in 32 bits: the entry point rejects B * Hkv * N * K >= 2^31 and
+// bucket counts >= 2^31.)
+constexpr int kScatterThreads = 256, kScatterItems = 4;
+__global__ void __launch_bounds__(kScatterThreads) leaf_scatter_kernel(
+    const int32_t* __restrict__ surv, int t0, int span, int K, int N, int BH, int chunk_shift, int M2,
+    const int* __restrict__ bucket_off, const int32_t* __restrict__ srank, uint32_t* __restrict__ list) {
+  const int bh = blockIdx.y;
+  const int nE = span * K;
+  const int x0 = blockIdx.x * (kScatterThreads * kScatterItems) + threadIdx.x;
+  int p[kScatterItems], r[kScatterItems], t[kScatterItems], slot[kScatterItems];
+#pragma unroll
+  for (int u = 0; u < kScatterItems; ++u) {
+    const int x = x0 + u * kScatterThreads;
+    const unsigned jt = (unsigned)x / (unsigned)K;
+    slot[u] = x - (int)jt * K;
+    t[u] = t0 + (int)jt;
+    p[u] = -1;
+    r[u] = 0;
+    if (x < nE) {
+      const int e = (bh * N + t[u]) * K + slot[u];
+      p[u] = surv[e];
+      r[u] = srank[e];
+    }
+  }
+  int pos[kScatterItems];
+#pragma unroll
+  for (int u = 0; u < kScatterItems; ++u)
+    pos[u] = p[u] >= 0 ? bucket_off[((t[u] >> chunk_shift) * BH + bh) * M2 + p[u]] + r[u] : -1;
+#pragma unroll
+  for (int u = 0; u < kScatterItems; ++u)
+    if (p[u] >= 0 && PISA_IN_BOUNDS(pos[u] >= 0 && pos[u] < BH * N * K))
+      list[pos[u]] = ((uint32_t)t[u] << 5) | (uint32_t)slot[u];
 }
 
 // Exclusive scans of the bucket sizes (entries) and of their tile counts
@@ -667,85 +670,114 @@ __global__ void __launch_bounds__(1024) leaf_scan_kernel(const int* __restrict__
 
 // Descriptor of leaf tile i among the tiles of buckets [b0, b1): its bucket is the
 // largest one whose first tile is <= i; {first entry, rows, level-2 survivor p,
-// b * Hkv + kv}.
-__global__ void leaf_tile_desc_kernel(const int* __restrict__ tile_off, const int* __restrict__ bucket_off, int b0,
-                                      int b1, long long max_tiles, int R, int M2, int BH, int4* __restrict__ desc) {
-  const long long i = tile_off[b0] + (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= tile_off[b0] + max_tiles || i >= tile_off[b1]) return;
-  const int bkt = b0 + find_bucket(tile_off + b0, b1 - b0, (int)i);
-  const int e0 = bucket_off[bkt] + ((int)i - tile_off[bkt]) * R;
-  const int nrows = min(R, bucket_off[bkt + 1] - e0);
-  desc[i] = make_int4(e0, nrows, bkt % M2, (bkt / M2) % BH);
+// b * Hkv + kv}.  Each thread takes kDescItems tiles a block apart and runs their
+// binary searches side by side (a fixed number of halvings each), so that the
+// searches' dependent loads overlap.
+constexpr int kDescThreads = 256, kDescItems = 4;
+__global__ void __launch_bounds__(kDescThreads) leaf_tile_desc_kernel(
+    const int* __restrict__ tile_off, const int* __restrict__ bucket_off, int b0, int b1, long long max_tiles, int R,
+    int M2, int BH, int4* __restrict__ desc) {
+  const int first = __ldg(tile_off + b0);
+  const int end = min((long long)__ldg(tile_off + b1), first + max_tiles);
+  const int i0 = first + blockIdx.x * (kDescThreads * kDescItems) + threadIdx.x;
+  // lo = the largest bucket b in [b0, b1) with tile_off[b] <= tile: the answer stays in
+  // [lo, lo + len) (tile_off[b0] <= tile), and len - half >= half keeps it there
+  int lo[kDescItems];
+#pragma unroll
+  for (int u = 0; u < kDescItems; ++u) lo[u] = b0;
+  for (int len = b1 - b0; len > 1;) {
+    const int half = len >> 1;
+#pragma unroll
+    for (int u = 0; u < kDescItems; ++u)
+      if (__ldg(tile_off + lo[u] + half) <= i0 + u * kDescThreads) lo[u] += half;
+    len -= half;
+  }
+#pragma unroll
+  for (int u = 0; u < kDescItems; ++u) {
+    const int i = i0 + u * kDescThreads;
+    if (i >= end) break;
+    const int bkt = lo[u];
+    const int e0 = __ldg(bucket_off + bkt) + (i - __ldg(tile_off + bkt)) * R;
+    const int nrows = min(R, __ldg(bucket_off + bkt + 1) - e0);
+    desc[i] = make_int4(e0, nrows, bkt % M2, (bkt / M2) % BH);
+  }
 }
 
 // Final Top-K per (b, kv, t) over the leaf candidates (children of the level-2
 // survivors, ascending); ineligible children carry -inf and are skipped.
-// The same for K <= 8, in registers: candidate slot q = 2 j + child (child 0 is
-// the left leaf of survivor j); a slot counts if its survivor exists and, for a
-// right child, its score is not -inf.  The compacted order of the generic kernel
-// is the slot order, so its tie rule (earlier candidate first) is the lower slot.
-__global__ void leaf_final8_kernel(const int32_t* __restrict__ surv, const float* __restrict__ leaf_scores,
-                                   long long t0, long long t1, int BH, long long N, int32_t* __restrict__ idx,
-                                   float* __restrict__ scores) {
-  constexpr int K = 8;
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (t1 - t0) * BH) return;
-  const long long job = (i / (t1 - t0)) * N + t0 + i % (t1 - t0);
-  const int4* s4 = reinterpret_cast<const int4*>(surv + job * K);
-  const int4 pa = __ldg(s4), pb = __ldg(s4 + 1);
-  const int p[K] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
-  const float4* l4 = reinterpret_cast<const float4*>(leaf_scores + job * 2 * K);
-  float sc[2 * K];
+// The same for K = 8: eight lanes per (b, kv, t), four rows per warp, (b, kv) =
+// blockIdx.y.  Lane l of a row's group holds survivor slot l and its two leaves,
+// candidates 2 l and 2 l + 1 (the second absent when its score is -inf); a slot
+// counts only if no slot before it is empty (survivors are ascending with -1 padding
+// at the end).  Each lane ranks its two candidates against the row's sixteen by
+// shuffles inside its group (j beats i when its score is higher, or equal with j
+// before i, the generic kernel's rule); the kept ones are written in candidate order.
+constexpr int kFinal8Threads = 256, kFinal8Items = 4;  // rows per 8-lane group, a block apart
+constexpr int kFinal8Rows = kFinal8Threads / 8 * kFinal8Items;  // rows per block
+__global__ void __launch_bounds__(kFinal8Threads) leaf_final8_kernel(
+    const int32_t* __restrict__ surv, const float* __restrict__ leaf_scores, int t0, int span, int N,
+    int32_t* __restrict__ idx, float* __restrict__ scores) {
+  constexpr int K = 8, kRowsPerBlock = kFinal8Threads / 8;
+  const int lane = threadIdx.x & 31, sl = lane & 7, gbase = lane & ~7;
+  const int row0 = blockIdx.x * (kRowsPerBlock * kFinal8Items) + (threadIdx.x >> 3);
+  const long long job0 = (long long)blockIdx.y * N + t0;
+  // every row's loads first, then the rows one by one (rows past the end still take
+  // part in the shuffles)
+  int p[kFinal8Items];
+  float2 s2[kFinal8Items];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float4 v = __ldg(l4 + q);
-    sc[4 * q] = v.x;
-    sc[4 * q + 1] = v.y;
-    sc[4 * q + 2] = v.z;
-    sc[4 * q + 3] = v.w;
-  }
-  unsigned valid = 0;
-  bool alive = true;  // survivors are ascending with -1 padding at the end
-#pragma unroll
-  for (int j = 0; j < K; ++j) {
-    alive = alive && p[j] >= 0;
-    if (alive) valid |= (1u << (2 * j)) | (sc[2 * j + 1] != -INFINITY ? 1u << (2 * j + 1) : 0u);
-  }
-  const int nC = __popc(valid);
-  int out_i[K];
-  float out_s[K];
-  int w = 0;
-#pragma unroll
-  for (int q = 0; q < 2 * K; ++q) {
-    bool keep = (valid >> q) & 1;
-    if (keep && nC > K) {
-      int rank = 0;
-#pragma unroll
-      for (int r = 0; r < 2 * K; ++r)
-        rank += ((valid >> r) & 1) && (sc[r] > sc[q] || (sc[r] == sc[q] && r < q));
-      keep = rank < K;
+  for (int u = 0; u < kFinal8Items; ++u) {
+    const int jt = row0 + u * kRowsPerBlock;
+    p[u] = -1;
+    s2[u] = make_float2(-INFINITY, -INFINITY);
+    if (jt < span) {
+      p[u] = __ldg(surv + (job0 + jt) * K + sl);
+      s2[u] = __ldg(reinterpret_cast<const float2*>(leaf_scores + (job0 + jt) * 2 * K) + sl);
     }
+  }
+  const unsigned below = (1u << sl) - 1u;
 #pragma unroll
-    for (int o = 0; o < K; ++o)  // out[w] = candidate q, with register-resident outputs
-      if (keep && o == w) {
-        out_i[o] = 2 * p[q >> 1] + (q & 1);
-        out_s[o] = sc[q];
+  for (int u = 0; u < kFinal8Items; ++u) {
+    const int jt = row0 + u * kRowsPerBlock;
+    const unsigned dead = (__ballot_sync(kFull, p[u] < 0) >> gbase) & 0xFFu;
+    const bool va = (dead & (below | (1u << sl))) == 0u;  // no empty slot up to this one
+    const bool vb = va && s2[u].y != -INFINITY;
+    const unsigned ma = (__ballot_sync(kFull, va) >> gbase) & 0xFFu;
+    const unsigned mb = (__ballot_sync(kFull, vb) >> gbase) & 0xFFu;
+    const int nC = __popc(ma) + __popc(mb);
+    // absent candidates become NaN, which compares false with everything
+    const float sa = va ? s2[u].x : __int_as_float(0x7fc00000), sb = vb ? s2[u].y : __int_as_float(0x7fc00000);
+    int ra = 0, rb = 0;
+#pragma unroll
+    for (int o = 0; o < 8; ++o) {
+      const float ya = __shfl_sync(kFull, sa, gbase | o), yb = __shfl_sync(kFull, sb, gbase | o);
+      // candidates 2 o and 2 o + 1 against this lane's 2 sl and 2 sl + 1
+      ra += (ya > sa) || (ya == sa && o < sl);
+      ra += (yb > sa) || (yb == sa && o < sl);
+      rb += (ya > sb) || (ya == sb && o <= sl);
+      rb += (yb > sb) || (yb == sb && o < sl);
+    }
+    const bool ka = va && (nC <= K || ra < K), kb = vb && (nC <= K || rb < K);
+    const unsigned kam = (__ballot_sync(kFull, ka) >> gbase) & 0xFFu;
+    const unsigned kbm = (__ballot_sync(kFull, kb) >> gbase) & 0xFFu;
+    if (jt < span) {
+      const int oa = __popc(kam & below) + __popc(kbm & below);
+      const int nOut = __popc(kam) + __popc(kbm);
+      int32_t* io = idx + (job0 + jt) * K;
+      float* so = scores ? scores + (job0 + jt) * K : nullptr;
+      if (ka && oa < K) {  // (always below K unless the scores hold NaN)
+        io[oa] = 2 * p[u];
+        if (so) so[oa] = sa;
       }
-    w += keep;
-  }
-#pragma unroll
-  for (int o = 0; o < K; ++o)
-    if (o >= w) {
-      out_i[o] = -1;
-      out_s[o] = -INFINITY;
+      if (kb && oa + ka < K) {
+        io[oa + ka] = 2 * p[u] + 1;
+        if (so) so[oa + ka] = sb;
+      }
+      if (sl >= nOut) {
+        io[sl] = -1;
+        if (so) so[sl] = -INFINITY;
+      }
     }
-  int4* io = reinterpret_cast<int4*>(idx + job * K);
-  io[0] = make_int4(out_i[0], out_i[1], out_i[2], out_i[3]);
-  io[1] = make_int4(out_i[4], out_i[5], out_i[6], out_i[7]);
-  if (scores) {
-    float4* so = reinterpret_cast<float4*>(scores + job * K);
-    so[0] = make_float4(out_s[0], out_s[1], out_s[2], out_s[3]);
-    so[1] = make_float4(out_s[4], out_s[5], out_s[6], out_s[7]);
   }
 }
 
@@ -923,13 +955,15 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
                                             L.tile_off + L.b0);
     note_launch();
   }
-  leaf_scatter_kernel<<<(unsigned)((entries + 255) / 256), 256, 0, s>>>(
-      L.surv, L.t0, L.t1, BH, L.K, L.N, L.chunk_shift, L.M2, L.bucket_off, L.srank, L.list);
+  constexpr int kScatterSpan = kScatterThreads * kScatterItems;
+  leaf_scatter_kernel<<<dim3((unsigned)((span * L.K + kScatterSpan - 1) / kScatterSpan), BH), kScatterThreads, 0, s>>>(
+      L.surv, (int)L.t0, (int)span, L.K, (int)L.N, BH, L.chunk_shift, L.M2, L.bucket_off, L.srank, L.list);
   note_launch();
   // a tile holds R >= 8 entries of one bucket: at most entries / 8 + (buckets) tiles
   const long long max_tiles = entries / 8 + (L.b1 - L.b0) + 1;
-  leaf_tile_desc_kernel<<<(unsigned)((max_tiles + 255) / 256), 256, 0, s>>>(L.tile_off, L.bucket_off, L.b0, L.b1,
-                                                                          max_tiles, R, L.M2, BH, L.tile_desc);
+  constexpr int kDescSpan = kDescThreads * kDescItems;
+  leaf_tile_desc_kernel<<<(unsigned)((max_tiles + kDescSpan - 1) / kDescSpan), kDescThreads, 0, s>>>(
+      L.tile_off, L.bucket_off, L.b0, L.b1, max_tiles, R, L.M2, BH, L.tile_desc);
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -938,12 +972,9 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
   e = launch_leaf_tc_kernel(L, 0, 0, s);
   if (e != cudaSuccess) return e;
   mark_phase(4, s);
-  // (the K = 8 kernel's vector accesses need 16-byte aligned idx / scores: true for the
-  // torch allocations the binding makes, checked here for any caller)
-  const bool vec = L.K == 8 && ((reinterpret_cast<uintptr_t>(L.idx) | reinterpret_cast<uintptr_t>(L.scores)) & 15) == 0;
-  if (vec)
-    leaf_final8_kernel<<<(unsigned)((BH * span + 127) / 128), 128, 0, s>>>(L.surv, L.leaf_scores, L.t0, L.t1, BH,
-                                                                          L.N, L.idx, L.scores);
+  if (L.K == 8)
+    leaf_final8_kernel<<<dim3((unsigned)((span + kFinal8Rows - 1) / kFinal8Rows), BH), kFinal8Threads, 0, s>>>(
+        L.surv, L.leaf_scores, (int)L.t0, (int)span, (int)L.N, L.idx, L.scores);
   else
     leaf_final_kernel<<<(unsigned)((BH * span + kFinalWarps - 1) / kFinalWarps), kFinalWarps * 32, 0, s>>>(
         L.surv, L.leaf_scores, L.t0, L.t1, BH, L.N, L.K, L.idx, L.scores);

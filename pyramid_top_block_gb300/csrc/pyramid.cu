@@ -57,14 +57,14 @@ __global__ void __launch_bounds__(256) pyramid_leaves_kernel(
     const int cnt = node_count(1, leaf, N);
     const __nv_bfloat16* src = keys + (((long long)b * n_cap + leaf * kC) * Hkv + kv) * kD + c8 * 8;
     const long long stride = (long long)Hkv * kD;
-    for (int r0 = 0; r0 < cnt; r0 += 8) {
-      uint4 v[8];
+    for (int r0 = 0; r0 < cnt; r0 += 16) {
+      uint4 v[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
+      for (int u = 0; u < 16; ++u)
         v[u] = (r0 + u < cnt) ? __ldg(reinterpret_cast<const uint4*>(src + (r0 + u) * stride))
                               : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         if (r0 + u < cnt) {
           float f[8];
           unpack8(v[u], f);

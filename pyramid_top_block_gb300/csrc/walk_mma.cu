@@ -219,6 +219,11 @@ __global__ void __launch_bounds__(kWalkWarps * 32, 3) walk_mma_kernel(
     const int kv = (int)(bh % Hkv);
     const long long b = bh / Hkv;
     const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + ((b * N + t) * Hq + (long long)kv * G) * kD);
+    {  // the warp's next query: its G head rows into L2 while this one walks
+      const int tn = t + gridDim.x * kWalkWarps;
+      if (tn < t1 && lane < G)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(Q + ((b * N + tn) * Hq + (long long)kv * G + lane) * kD));
+    }
     int nS;  // survivors (candidate indices in S.sel) at the last processed level
     if (l_start < 2) {
       // at most K nodes at level 2: every eligible level-2 node survives unscored
@@ -622,6 +627,11 @@ __global__ void __launch_bounds__(kWalk8Warps * 32, 1) walk_k8_kernel(
       continue;
     }
     const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + ((b * N + t) * Hq + (long long)kv * G) * kD);
+    {  // the warp's next query: its G head rows into L2 while this one walks
+      const int tn = t + gridDim.x * kWalk8Warps;
+      if (tn < t1 && lane < G)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(Q + ((b * N + tn) * Hq + (long long)kv * G + lane) * kD));
+    }
     // Q^T fragments (the MMA's B operand): [ks][nt] / [ks][nt + 2] = words (8ks + j, 8ks + j + 4)
     // of head g + 8 nt; heads >= G are zero
     uint32_t A[4][4];
@@ -921,6 +931,11 @@ __global__ void __launch_bounds__(kWalk8Warps * 32, 1) walk_k8s_kernel(
       continue;
     }
     const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + ((b * N + t) * Hq + (long long)kv * G) * kD);
+    {  // the warp's next query: its G head rows into L2 while this one walks
+      const int tn = t + gridDim.x * kWalk8Warps;
+      if (tn < t1 && lane < G)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(Q + ((b * N + tn) * Hq + (long long)kv * G + lane) * kD));
+    }
     // Q as the A operand: [ks] = {head g word 8ks + j, head g + 8 same word, head g word
     // 8ks + j + 4, head g + 8 same word} (all 16 heads are real: G = 16)
     uint32_t A[4][4];
