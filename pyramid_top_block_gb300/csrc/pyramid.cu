@@ -12,9 +12,8 @@
 //       head and sums that column over the leaf's tokens in token order, so a
 //       warp reads whole 256-byte token rows.  The CTA then merges its LPB
 //       leaves up log2(LPB) levels in shared memory.
-//   pyramid_top_reg_kernel: one CTA per (b, kv) merges the remaining levels up to
-//       the root, each warp five levels of its 32 nodes in registers (no CTA
-//       barrier), warp 0 the last three from the warps' roots;
+//   pyramid_top_col_kernel: one warp per (b, kv, feature) merges the remaining
+//       levels up to the root, three in each lane's registers, five by shuffles;
 //   pyramid_top_kernel    : the same level by level through global memory, for
 //       layouts whose merged-in-CTA level is larger (many KV heads).
 // Divisions by a power-of-two count are exact multiplications (div_count), the
@@ -133,81 +132,68 @@ __global__ void __launch_bounds__(256) pyramid_top_kernel(float* __restrict__ su
   }
 }
 
-constexpr int kTopNodes = 256;  // largest input level the register kernel below takes (8 warps x 32 nodes)
+constexpr int kTopNodes = 256;  // largest input level the column kernel below takes (32 lanes x 8 nodes)
 
-// The same levels when level first_level - 1 holds at most kTopNodes nodes, merged in
-// registers: warp w holds nodes [32 w, 32 w + 32) of that level, lane j features 2 j and
-// 2 j + 1, and merges them five levels up without a CTA barrier (writing every node it
-// forms); the warps' last nodes meet in shared memory, where warp 0 merges the levels
-// above.  Same merge arithmetic, same bits.
-constexpr int kRegWarps = kTopNodes / 32;
-__global__ void __launch_bounds__(kRegWarps * 32) pyramid_top_reg_kernel(float* __restrict__ summ, Levels lv,
-                                                                        long long N, int Hkv, int first_level,
-                                                                        const int32_t* __restrict__ lens,
-                                                                        long long n_cap) {
-  __shared__ float2 roots[kRegWarps][32];
-  const int b = blockIdx.x / Hkv, kv = blockIdx.x % Hkv;
+// The same levels, one warp per (b, kv, feature): lane j holds nodes [8 j, 8 j + 8) of
+// the input level (at most kTopNodes nodes) for one feature, merges them three levels
+// up in its registers, then five more levels by shuffles between lanes (writing every
+// node it forms).  Same merges in the same pairs, hence the same bits as the kernels
+// above; a warp's chain is eight merges long instead of a CTA's thirty-one.
+constexpr int kColWarps = 8;  // warps (feature columns) per CTA
+__global__ void __launch_bounds__(kColWarps * 32) pyramid_top_col_kernel(float* __restrict__ summ, Levels lv,
+                                                                         long long N, int Hkv, int first_level,
+                                                                         const int32_t* __restrict__ lens,
+                                                                         long long n_cap, int columns) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = blockIdx.x * kColWarps + warp;  // (b * Hkv + kv) * kD + feature
+  if (col >= columns) return;  // warp-uniform
+  const int bkv = col / kD, f = col % kD;
+  const int b = bkv / Hkv;
   if (lens) N = min((long long)max(lens[b], 0), n_cap);
-  float* blk = summ + ((long long)b * Hkv + kv) * lv.total * kD;
-  const int L = lv.L;  // like the level-by-level kernels: every level of the layout is written
+  float* blk = summ + (long long)bkv * lv.total * kD + f;
+  const int L = lv.L;
   const int l0 = first_level - 1;  // the input level
   const long long M0 = level_size_for(N, l0);
-  float2 v[32];
+  float v[8];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const long long node = 32LL * warp + i;
-    v[i] = node < M0 ? reinterpret_cast<const float2*>(blk + (lv.off[l0] + node) * kD)[lane] : make_float2(0.f, 0.f);
+  for (int u = 0; u < 8; ++u) {
+    const long long node = 8LL * lane + u;
+    v[u] = node < M0 ? blk[(lv.off[l0] + node) * kD] : 0.f;
   }
-  // five levels inside the warp: 32 -> 16 -> 8 -> 4 -> 2 -> 1 nodes
+  // three levels inside the lane: 8 -> 4 -> 2 -> 1 nodes
 #pragma unroll
-  for (int j = 0; j < 5; ++j) {
+  for (int j = 0; j < 3; ++j) {
     const int l = first_level + j;
-    const int cnt = 16 >> j;                       // nodes this warp forms at level l
-    const long long base = (32LL * warp) >> (j + 1);  // the first of them
     if (l <= L) {
       const long long M = level_size_for(N, l), Mc = level_size_for(N, l - 1);
+      const int cnt = 4 >> j;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < 4; ++i) {
         if (i < cnt) {
-          const long long node = base + i;
+          const long long node = (long long)cnt * lane + i;
           const long long c0 = 2 * node, c1 = 2 * node + 1;
           const int n0 = c0 < Mc ? node_count(l - 1, c0, N) : 0;
           const int n1 = c1 < Mc ? node_count(l - 1, c1, N) : 0;
-          float2 o;
-          o.x = merge_mean(v[2 * i].x, n0, v[2 * i + 1].x, n1);
-          o.y = merge_mean(v[2 * i].y, n0, v[2 * i + 1].y, n1);
-          v[i] = o;
-          if (node < M) reinterpret_cast<float2*>(blk + (lv.off[l] + node) * kD)[lane] = o;
+          v[i] = merge_mean(v[2 * i], n0, v[2 * i + 1], n1);
+          if (node < M) blk[(lv.off[l] + node) * kD] = v[i];
         }
       }
     }
   }
-  roots[warp][lane] = v[0];
-  __syncthreads();
-  if (warp != 0) return;
-  // the levels above: warp 0 merges the kRegWarps warp roots (level first_level + 4)
+  // five levels across lanes: node lane >> (j + 1) from the lanes 2^j apart
+  float x = v[0];
 #pragma unroll
-  for (int i = 0; i < kRegWarps; ++i) v[i] = roots[i][lane];
-#pragma unroll
-  for (int j = 0; j < 3; ++j) {
-    const int l = first_level + 5 + j;
-    const int cnt = kRegWarps >> (j + 1);
-    if (l <= L) {
+  for (int j = 0; j < 5; ++j) {
+    const int l = first_level + 3 + j;
+    const float y = __shfl_down_sync(kFull, x, 1 << j);
+    if (l <= L && (lane & ((2 << j) - 1)) == 0) {
       const long long M = level_size_for(N, l), Mc = level_size_for(N, l - 1);
-#pragma unroll
-      for (int i = 0; i < kRegWarps / 2; ++i) {
-        if (i < cnt) {
-          const long long c0 = 2LL * i, c1 = 2LL * i + 1;
-          const int n0 = c0 < Mc ? node_count(l - 1, c0, N) : 0;
-          const int n1 = c1 < Mc ? node_count(l - 1, c1, N) : 0;
-          float2 o;
-          o.x = merge_mean(v[2 * i].x, n0, v[2 * i + 1].x, n1);
-          o.y = merge_mean(v[2 * i].y, n0, v[2 * i + 1].y, n1);
-          v[i] = o;
-          if (i < M) reinterpret_cast<float2*>(blk + (lv.off[l] + i) * kD)[lane] = o;
-        }
-      }
+      const long long node = lane >> (j + 1);
+      const long long c0 = 2 * node, c1 = 2 * node + 1;
+      const int n0 = c0 < Mc ? node_count(l - 1, c0, N) : 0;
+      const int n1 = c1 < Mc ? node_count(l - 1, c1, N) : 0;
+      x = merge_mean(x, n0, y, n1);
+      if (node < M) blk[(lv.off[l] + node) * kD] = x;
     }
   }
 }
@@ -237,7 +223,9 @@ cudaError_t launch_build_pyramid(const __nv_bfloat16* keys, float* summ, const L
   if (merge_levels + 2 <= lv.L) {
     const int first = merge_levels + 2;
     if (lv.M[first - 1] <= kTopNodes && lv.L - first + 1 <= 8) {
-      pyramid_top_reg_kernel<<<B * Hkv, kRegWarps * 32, 0, s>>>(summ, lv, N, Hkv, first, lens, n_cap);
+      const int columns = B * Hkv * kD;
+      pyramid_top_col_kernel<<<(columns + kColWarps - 1) / kColWarps, kColWarps * 32, 0, s>>>(summ, lv, N, Hkv, first,
+                                                                                             lens, n_cap, columns);
     } else {
       pyramid_top_kernel<<<B * Hkv, 256, 0, s>>>(summ, lv, N, Hkv, first, lens, n_cap);
     }

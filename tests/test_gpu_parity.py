@@ -73,11 +73,13 @@ def test_group_sizes(G):
     _assert_stats(st)
 
 
-def test_edge_lengths():
+@pytest.mark.parametrize("K", [2, 8])
+def test_edge_lengths(K):
+    # K = 8 takes the eight-lanes-per-row final Top-K, whose last block holds rows past N
     for N in (1, 2, 63, 64, 65, 127, 128, 129, 513):
         q, k = synth.iid(1, N, 4, 1, seed=N)
-        _, idx, sc = _run_prefill(q, k, 2)
-        st = compare_prefill(idx, sc, _f32(q), _f32(k), np.arange(N), 2)
+        _, idx, sc = _run_prefill(q, k, K)
+        st = compare_prefill(idx, sc, _f32(q), _f32(k), np.arange(N), K)
         _assert_stats(st)
 
 
