@@ -53,13 +53,17 @@ Levels make_levels(long long n, long long n_cap) {
   return lv;
 }
 
+// Largest grid y extent of a launch: the build, walk, scatter and final Top-K index
+// (b, kv) or b along y.
+constexpr long long kMaxGridY = 65535;
+
 // Sizes the library handles; returns PISA_OK or the status to report.
 int check_geometry(int B, long long N, int Hq, int Hkv, int d, int C, int g, int K) {
   if (B < 1 || N < 1 || Hq < 1 || Hkv < 1 || d < 1 || C < 1 || g < 1 || K < 1)
     return PISA_ERR_INVALID_ARG;
   if (Hq % Hkv) return PISA_ERR_UNSUPPORTED;
   if (d != kD || C != kC || g != 2) return PISA_ERR_UNSUPPORTED;
-  if (K > kMaxK || !pow2_group(Hq / Hkv) || Hkv > 32) return PISA_ERR_UNSUPPORTED;
+  if (K > kMaxK || !pow2_group(Hq / Hkv) || Hkv > 32 || (long long)B * Hkv > kMaxGridY) return PISA_ERR_UNSUPPORTED;
   if (N > (1LL << 27)) return PISA_ERR_UNSUPPORTED;
   if ((long long)B * Hkv * N * K >= (1LL << 31) || (long long)B * N >= (1LL << 31)) return PISA_ERR_UNSUPPORTED;
   return PISA_OK;
@@ -69,6 +73,7 @@ int check_pyr(const pisa_pyramid* p) {
   if (!p || !p->summaries || !p->keys) return PISA_ERR_INVALID_ARG;
   if (p->B < 1 || p->Hkv < 1 || p->n_cap < 1) return PISA_ERR_INVALID_ARG;
   if (p->d != kD || p->C != kC || p->g != 2 || p->Hkv > 32) return PISA_ERR_UNSUPPORTED;
+  if ((long long)p->B * p->Hkv > kMaxGridY) return PISA_ERR_UNSUPPORTED;  // grids index (b, kv) along y
   if ((reinterpret_cast<uintptr_t>(p->summaries) | reinterpret_cast<uintptr_t>(p->keys)) & 15)
     return PISA_ERR_INVALID_ARG;
   return PISA_OK;

@@ -64,6 +64,8 @@ def test_argument_errors_without_launch():
     assert lib.pisa_build_pyramid(None, 10, None) == 1
     st = pisa._PyrStruct(0x1000, 0x2000, None, 1, 2, 32, 64, 2, 128)   # d = 32
     assert lib.pisa_build_pyramid(ctypes.byref(st), 10, None) == 2
+    st = pisa._PyrStruct(0x1000, 0x2000, None, 40000, 2, 64, 64, 2, 128)  # B * Hkv > 65535
+    assert lib.pisa_build_pyramid(ctypes.byref(st), 10, None) == 2
     st = pisa._PyrStruct(0x1000, 0x2000, None, 1, 2, 64, 64, 2, 128)
     assert lib.pisa_build_pyramid(ctypes.byref(st), 129, None) == 1      # N > n_cap
     assert lib.pisa_build_pyramid(ctypes.byref(st), 0, None) == 1
