@@ -43,7 +43,7 @@ L2_GATHER_TBS = 11.6  # measured rate of random 256-byte gathers served by L2 on
 KERNEL_SOURCES = {"leaf": ["leaf_tc.cu", "tc.cuh", "common.cuh", "api.cuh"],
                   "walk": ["walk_mma.cu", "tc.cuh", "common.cuh", "api.cuh"]}
 NCU_TRAFFIC = {
-    ("leaf", "latency-256k"): {"bytes": 1769321000 + 35451648, "src_sha1": "657da88526a9981d8dbc60b9838dadc31af65144",
+    ("leaf", "latency-256k"): {"bytes": 1769379000 + 35506176, "src_sha1": "4c8daeb457facef3737fc6ddefe12e4b78bfbc2c",
                                "profile": "profiles/leaf_tc_kernel_latency-256k.md"},
     ("walk", "latency-256k"): {"bytes": 1076080000 + 34955520, "src_sha1": "5cd82d08856d78649f5c6e6712f0c125b751f054",
                                "profile": "profiles/walk_k8s_kernel_latency-256k.md"},

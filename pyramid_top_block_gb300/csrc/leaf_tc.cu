@@ -781,43 +781,51 @@ __global__ void __launch_bounds__(kFinal8Threads) leaf_final8_kernel(
   }
 }
 
-// Final Top-K of the leaf stage for any K <= 32: one warp per (b, kv, t).  Lane l holds
-// survivor slot l and its two leaves (the second absent when its score is -inf: past
-// the query or past the last token); the candidates' order is the walk's (node order).
-// The scores go to shared memory in that order, each lane ranks its two candidates
-// against all of them (j beats i when its score is higher, or equal with j before i),
-// and the kept ones are written in candidate order, then -1 / -inf padding.
+// Final Top-K of the leaf stage for any K <= 32: one warp per (b, kv, t), (b, kv) =
+// blockIdx.y.  Lane l holds survivor slot l and its two leaves (the second absent when
+// its score is -inf: past the query or past the last token); the candidates' order is
+// the walk's (node order).  Each candidate's 64-bit key, the order-preserving bits of
+// its score above the complement of its position, goes to shared memory in that order:
+// j beats i exactly when key j > key i (a higher score, or an equal one with j before
+// i), so a lane ranks its two candidates by one unsigned compare per candidate, and the
+// kept ones are written in candidate order, then -1 / -inf padding.
 constexpr int kFinalWarps = 4;
+__device__ __forceinline__ unsigned long long final_key(float s, int pos) {
+  const unsigned b = __float_as_uint(s + 0.f);  // (-0 becomes +0: the two compare equal)
+  const unsigned ord = b ^ ((unsigned)((int)b >> 31) | 0x80000000u);
+  return ((unsigned long long)ord << 32) | (unsigned)(0xFFFFFFFFu - (unsigned)pos);
+}
 __global__ void __launch_bounds__(kFinalWarps * 32) leaf_final_kernel(
-    const int32_t* __restrict__ surv, const float* __restrict__ leaf_scores, long long t0, long long t1, int BH,
-    long long N, int K, int32_t* __restrict__ idx, float* __restrict__ scores) {
-  __shared__ float sh[kFinalWarps][2 * kMaxK];
+    const int32_t* __restrict__ surv, const float* __restrict__ leaf_scores, int t0, int span, int N, int K,
+    int32_t* __restrict__ idx, float* __restrict__ scores) {
+  __shared__ unsigned long long sh[kFinalWarps][2 * kMaxK];
   const int lane = threadIdx.x & 31, wb = threadIdx.x >> 5;
-  const long long span = t1 - t0;
-  const long long wid = (long long)blockIdx.x * kFinalWarps + wb;
-  if (wid >= span * BH) return;  // warp-uniform
-  const long long job = (wid / span) * N + t0 + wid % span;
+  const int jt = blockIdx.x * kFinalWarps + wb;
+  if (jt >= span) return;  // warp-uniform
+  const long long job = (long long)blockIdx.y * N + t0 + jt;
   const int p = lane < K ? __ldg(surv + job * K + lane) : -1;
-  const float* ls = leaf_scores + job * 2 * K;
   const bool va = p >= 0;
-  const float sa = va ? __ldg(ls + 2 * lane) : -INFINITY;
-  const float sb = va ? __ldg(ls + 2 * lane + 1) : -INFINITY;
+  const float2 s2 = va ? __ldg(reinterpret_cast<const float2*>(leaf_scores + job * 2 * K) + lane)
+                       : make_float2(-INFINITY, -INFINITY);
+  const float sa = s2.x, sb = s2.y;
   const bool vb = va && sb != -INFINITY;
   const unsigned lt = (1u << lane) - 1u;
   const unsigned ma = __ballot_sync(kFull, va), mb = __ballot_sync(kFull, vb);
   const int pa = __popc(ma & lt) + __popc(mb & lt);  // position of this lane's first leaf
   const int nC = __popc(ma) + __popc(mb);
-  float* sw = sh[wb];
-  if (va) sw[pa] = sa;
-  if (vb) sw[pa + 1] = sb;
-  __syncwarp();
   bool ka = va, kb = vb;
-  if (nC > K) {
+  if (nC > K) {  // warp-uniform
+    unsigned long long* sw = sh[wb];
+    const unsigned long long kA = final_key(sa, pa), kB = final_key(sb, pa + 1);
+    if (va) sw[pa] = kA;
+    if (vb) sw[pa + 1] = kB;
+    __syncwarp();
     int ra = 0, rb = 0;
+#pragma unroll 4
     for (int j = 0; j < nC; ++j) {
-      const float y = sw[j];
-      ra += (y > sa) || (y == sa && j < pa);
-      rb += (y > sb) || (y == sb && j < pa + 1);
+      const unsigned long long y = sw[j];
+      ra += y > kA;
+      rb += y > kB;
     }
     ka = va && ra < K;
     kb = vb && rb < K;
@@ -976,8 +984,8 @@ cudaError_t launch_prefill_leaf_tc(const LeafTcLaunch& L, cudaStream_t s) {
     leaf_final8_kernel<<<dim3((unsigned)((span + kFinal8Rows - 1) / kFinal8Rows), BH), kFinal8Threads, 0, s>>>(
         L.surv, L.leaf_scores, (int)L.t0, (int)span, (int)L.N, L.idx, L.scores);
   else
-    leaf_final_kernel<<<(unsigned)((BH * span + kFinalWarps - 1) / kFinalWarps), kFinalWarps * 32, 0, s>>>(
-        L.surv, L.leaf_scores, L.t0, L.t1, BH, L.N, L.K, L.idx, L.scores);
+    leaf_final_kernel<<<dim3((unsigned)((span + kFinalWarps - 1) / kFinalWarps), BH), kFinalWarps * 32, 0, s>>>(
+        L.surv, L.leaf_scores, (int)L.t0, (int)span, (int)L.N, L.K, L.idx, L.scores);
   note_launch();
   e = cudaGetLastError();
   mark_phase(5, s);
