@@ -1,6 +1,6 @@
 // common.cuh -- shared device helpers of the GB300 PISA selector.
 //
-// Fixed geometry of this build: head dim d = 64, leaf size C = 64, merge
+// Fixed geometry of the library: head dim d = 64, leaf size C = 64, merge
 // factor g = 2 ("Block Sparse Attention with Log-Linear Complexity", §7.3:
 // d = 64, C = 64, g = 2).  A node of level l >= 1 spans 64 * 2^(l-1) tokens;
 // level 0 is the raw keys.

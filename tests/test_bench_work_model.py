@@ -40,3 +40,24 @@ def test_256k_figures():
 def test_no_scored_level_when_everything_fits_in_k():
     a = bench.algorithmic(_shape(512, K=8))  # 8 leaves: every level kept whole
     assert a["flops"] == 0 and a["scored_intermediate_levels"] == 0
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    """The ncu traffic figure is tied to the kernel's code: a comment or blank-line
+    edit keeps the hash, any code edit changes it."""
+    src = "// header\n__global__ void k(int* a) {\n  /* block\n comment */ a[0] = 1;  // tail\n\n}\n"
+    same = "__global__ void k(int* a) {\n  a[0] = 1;\n}\n// another note\n"
+    other = "__global__ void k(int* a) {\n  a[0] = 2;\n}\n"
+    assert bench.code_only(src) == bench.code_only(same)
+    assert bench.code_only(src) != bench.code_only(other)
+    files = {"x.cu": src}
+    bench.KERNEL_SOURCES["_probe"] = ["x.cu"]
+    try:
+        h1 = bench.source_sha1("_probe", read=files.get)
+        files["x.cu"] = same
+        h2 = bench.source_sha1("_probe", read=files.get)
+        files["x.cu"] = other
+        h3 = bench.source_sha1("_probe", read=files.get)
+    finally:
+        del bench.KERNEL_SOURCES["_probe"]
+    assert h1 == h2 != h3
