@@ -196,11 +196,14 @@ __device__ __forceinline__ void shuffle_rank(const float* sc, int nC, int K, int
   const float x1 = lane + 32 < nC ? sc[lane + 32] : 0.f;
   int r0 = 0, r1 = 0;
   const int n0 = min(nC, 32);
+  // (unrolled: the shuffles of several j are in flight together)
+#pragma unroll 8
   for (int j = 0; j < n0; ++j) {
     const float y = __shfl_sync(kFull, x0, j);
     r0 += (y > x0 || (y == x0 && j < lane));
     r1 += (y >= x1);  // j < 32 <= lane + 32
   }
+#pragma unroll 8
   for (int j = 32; j < nC; ++j) {
     const float y = __shfl_sync(kFull, x1, j - 32);
     r0 += (y > x0);  // j >= 32 > lane
@@ -233,6 +236,8 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t qa[4][4];  // the walking warps' query fragments, requested before anything else
   if (warp < kWalkWarps) leaf_q_frags<G>(q_new + ((long long)b * Hq + (long long)kv * G) * kD, lane, qa);
+  // the new key's feature of the path-update threads, likewise (it does not depend on the length)
+  const __nv_bfloat16 kn = tid < kD ? k_new[((long long)b * Hkv + kv) * kD + tid] : __float2bfloat16(0.f);
   const long long p = lengths[b];
   int32_t* io = idx + (long long)blockIdx.x * K;
   float* so = scores ? scores + (long long)blockIdx.x * K : nullptr;
@@ -280,14 +285,17 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(
     // path update, feature e = tid: the leaf mean over its tokens in order, then the
     // count-weighted merges up to the root (the same formula as the build)
     const int e = tid;
-    const __nv_bfloat16 kn = k_new[((long long)b * Hkv + kv) * kD + e];
     keys_b[(p * Hkv + kv) * kD + e] = kn;
-    float acc = 0.f;
+    float acc = 0.f;  // (unrolled: the shared-memory loads run ahead of the chain of adds)
+#pragma unroll 8
     for (int r = 0; r < (int)(p - leaf * kC); ++r) acc = __fadd_rn(acc, bf2f(lk[r * kD + e]));
     acc = __fadd_rn(acc, bf2f(kn));
     float m = div_count(acc, (int)(p - leaf * kC + 1));
     blk[(Oof(1) + leaf) * kD + e] = m;
     long long i = leaf;
+    // (unrolled by four: the counts and addresses of the next levels are ready before
+    // the chain of merges reaches them)
+#pragma unroll 4
     for (int l = 2; l <= Ln; ++l) {
       const long long child = i;
       i >>= 1;
