@@ -26,7 +26,7 @@
  *     Query head h belongs to KV head h / (Hq/Hkv) (contiguous groups).
  *   - Supported sizes: d = 64, C = 64, g = 2, 1 <= K <= 32,
  *     Hq/Hkv in {1, 2, 4, 8, 16}, 1 <= Hkv <= 32, N <= 2^27,
- *     B * Hkv <= 65535, B * Hkv * N * K < 2^31.  Anything
+ *     B * Hkv <= 65535, B * Hkv * N * K < 2^31 - 2^20.  Anything
  *     else returns PISA_ERR_UNSUPPORTED (or PISA_ERR_INVALID_ARG when
  *     malformed).
  *   - Readings fixed by this library where the method's description is

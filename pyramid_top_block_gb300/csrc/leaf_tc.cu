@@ -512,8 +512,8 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 1)
 // e = ((b * Hkv + kv) * N + t) * K + slot.  Each thread takes kScatterItems entries
 // a block apart and issues all their loads before any store, so that the dependent
 // round trips (survivor, then its bucket's offset) of several entries overlap.
-// (Every index fits in 32 bits: the entry point rejects B * Hkv * N * K >= 2^31 and
-// bucket counts >= 2^31.)
+// (Every index fits in 32 bits: the entry point rejects B * Hkv * N * K >= 2^31 - 2^20,
+// which leaves room for the last block's threads past the end, and bucket counts >= 2^31.)
 constexpr int kScatterThreads = 256, kScatterItems = 4;
 __global__ void __launch_bounds__(kScatterThreads) leaf_scatter_kernel(
     const int32_t* __restrict__ surv, int t0, int span, int K, int N, int BH, int chunk_shift, int M2,

@@ -56,6 +56,9 @@ Levels make_levels(long long n, long long n_cap) {
 // Largest grid y extent of a launch: the build, walk, scatter and final Top-K index
 // (b, kv) or b along y.
 constexpr long long kMaxGridY = 65535;
+// Entries (b, kv, t, slot) a prefill call may hold: the bucketing kernels index them, and
+// their blocks' threads past the end, in 32-bit integers.
+constexpr long long kMaxEntries = (1LL << 31) - (1LL << 20);
 
 // Sizes the library handles; returns PISA_OK or the status to report.
 int check_geometry(int B, long long N, int Hq, int Hkv, int d, int C, int g, int K) {
@@ -65,7 +68,8 @@ int check_geometry(int B, long long N, int Hq, int Hkv, int d, int C, int g, int
   if (d != kD || C != kC || g != 2) return PISA_ERR_UNSUPPORTED;
   if (K > kMaxK || !pow2_group(Hq / Hkv) || Hkv > 32 || (long long)B * Hkv > kMaxGridY) return PISA_ERR_UNSUPPORTED;
   if (N > (1LL << 27)) return PISA_ERR_UNSUPPORTED;
-  if ((long long)B * Hkv * N * K >= (1LL << 31) || (long long)B * N >= (1LL << 31)) return PISA_ERR_UNSUPPORTED;
+  // 32-bit entry and tile indices, with headroom for a grid's last block past the end
+  if ((long long)B * Hkv * N * K >= kMaxEntries || (long long)B * N >= (1LL << 31)) return PISA_ERR_UNSUPPORTED;
   return PISA_OK;
 }
 

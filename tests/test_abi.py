@@ -56,6 +56,9 @@ def test_workspace_sizes():
     assert pisa.select_workspace_bytes(1, 100, 32, 2, 33) == 0      # K too large
     assert pisa.select_workspace_bytes(1, 100, 24, 2, 8) == 0       # group of 12
     assert pisa.select_workspace_bytes(1, 100, 30, 4, 8) == 0       # Hq % Hkv != 0
+    # entries (b, kv, t, slot) are indexed in 32 bits with room for a block past the end
+    assert pisa.select_workspace_bytes(1, (1 << 26) - 31, 16, 1, 32) == 0   # 2^31 - 992 entries
+    assert pisa.select_workspace_bytes(1, (1 << 26) - 32769, 16, 1, 32) > 0  # just below 2^31 - 2^20
     assert pisa.decode_workspace_bytes(16, 32, 2, 8) >= 4
 
 
